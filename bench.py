@@ -1,0 +1,421 @@
+"""Benchmark of the WTConv layer's training step (forward + fused backward) on GB300.
+
+One step = wtconv_forward + wtconv_backward (dx and every parameter gradient) over one batch of
+the seeded synthetic workload, through the C ABI.  Default workload: the ConvNeXt-T stage-1
+shape B=64, C=96, H=W=56, L=3, k=5, fp32 activations (the paper's WTConvNeXt-T setting).
+
+Prints ONE JSON line (rank 0).  `value` is fwd+bwd throughput in Gpixel*ch/s = B*C*H*W / step
+time over all ranks (replicas: each rank runs its own copy of the workload, "scaling": "weak").
+Timing: W untimed warm-up steps, then K timed steps; L2 is flushed (256 MiB write) before each
+timed step and each step is bracketed by CUDA events on the launching stream (the flush is not
+inside the bracket).  Also reported: per-kernel roofline of the dominant kernel, an end-to-end
+number with host buffers (pinned host -> device copies of x and dy and device -> host copies of
+y, dx and the gradients inside the timed region), the CPU oracle baseline, and SM clocks sampled
+during the timed region.
+
+`--impl reference` times the CPU oracle (the plain fp64 reference pipeline) instead, on the host
+cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from memory_bound_cnn_gb300 import wtconv as W  # noqa: E402
+from memory_bound_cnn_gb300.inputs import WORKLOADS, LayerShape, make_inputs  # noqa: E402
+
+PARAMS = ("base_w", "base_bias", "base_scale", "wavelet_w", "wavelet_scale")
+GRADS = ("d_base_w", "d_base_bias", "d_base_scale", "d_wavelet_w", "d_wavelet_scale")
+METRIC = "WTConv fwd+bwd Gpixel·ch/s and achieved HBM GB/s as % of GB300 peak"
+UNIT = "Gpixel·ch/s"
+# FP32 FMA peak from unit counts and the maximum clock: 152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+HBM_FALLBACK_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def s_levels(L: int) -> float:
+    """Sum over levels of the level-input size relative to the full plane: sum_{l=1..L} 4^(1-l)."""
+    return sum(4.0 ** (1 - l) for l in range(1, L + 1))
+
+
+def algorithmic(shape: LayerShape) -> dict:
+    """Per-layer algorithmic FLOPs and HBM bytes (conv multiply-adds x 2; one read of each input
+    activation and one write of each output activation)."""
+    n = shape.numel
+    e = 2 if shape.dtype in ("bf16", "f16") else 4
+    conv = 2.0 * shape.k * shape.k * (1.0 + s_levels(shape.L)) * n
+    return {
+        "fwd_flop": conv, "bwd_flop": 2.0 * conv,
+        "fwd_bytes": 2.0 * n * e, "bwd_bytes": 3.0 * n * e,
+    }
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "memory_bound_cnn_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, or None if it is missing or was taken
+    on kernel sources other than the current ones."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != source_hash():
+        return None
+    return float(m.group(1))
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            return json.load(open(path))
+        except ValueError:
+            pass
+    return {}
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,utilization.gpu,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "20", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 9:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        loaded = [r for r in rows if r[2] > 0] or rows
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in loaded for n, v in zip(names, r[3][1:]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(loaded)}
+
+
+# ------------------------------------------------------------------------ distributed bits
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest value over all ranks (identity for one process)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def whole_job_throughput(elements_per_rank: int, world: int, seconds_max: float) -> float:
+    """Gpixel*ch/s of the whole job: every rank processes its own copy of the workload."""
+    return elements_per_rank * world / seconds_max / 1e9
+
+
+# ------------------------------------------------------------------------------- CUDA arm
+
+def run_gpu(args, world, rank, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    shapes = WORKLOADS[args.workload]
+    layers = []
+    for i, s in enumerate(shapes):
+        host = make_inputs(s, seed=i)
+        d = {k: v.to(dev) for k, v in host.items()}
+        ws = torch.empty(max(1, W.wtconv_workspace_size(W.OP_BACKWARD, s.B, s.C, s.H, s.W, s.L, s.k,
+                                                        W.DTYPE_CODE[d["x"].dtype])), dtype=torch.uint8, device=dev)
+        out = {"y": torch.empty_like(d["x"]), "dx": torch.empty_like(d["x"]),
+               "grads": {g: torch.empty_like(d[p]) for g, p in zip(GRADS, PARAMS)}}
+        layers.append((s, host, d, ws, out))
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        for i, (s, _, d, ws, out) in enumerate(layers):
+            p = [d[n] for n in PARAMS]
+            if ev is not None:
+                ev[i][0].record(stream)
+            W.wtconv_forward(d["x"], *p, y=out["y"], stream=stream)
+            if ev is not None:
+                ev[i][1].record(stream)
+            W.wtconv_backward(d["x"], d["dy"], *p, dx=out["dx"], grads=out["grads"], workspace=ws, stream=stream)
+            if ev is not None:
+                ev[i][2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    nl = len(layers)
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nl)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        for k in range(args.steps):
+            flush.zero_()
+            step(events[k])
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    fwd_ms = [sum(events[k][i][0].elapsed_time(events[k][i][1]) for k in range(args.steps)) / args.steps for i in range(nl)]
+    bwd_ms = [sum(events[k][i][1].elapsed_time(events[k][i][2]) for k in range(args.steps)) / args.steps for i in range(nl)]
+    step_ms_local = sum(fwd_ms) + sum(bwd_ms)
+    step_ms = max_over_ranks(step_ms_local, world)
+    elements = sum(s.numel for s, *_ in layers)
+    value = whole_job_throughput(elements, world, step_ms / 1e3)
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    pinned = []
+    for s, host, d, ws, out in layers:
+        pinned.append({"x": host["x"].pin_memory(), "dy": host["dy"].pin_memory(),
+                       "y": torch.empty(host["x"].shape, dtype=host["x"].dtype).pin_memory(),
+                       "dx": torch.empty(host["x"].shape, dtype=host["x"].dtype).pin_memory(),
+                       "grads": {g: torch.empty(host[p].shape).pin_memory() for g, p in zip(GRADS, PARAMS)}})
+    h2d = sum(p["x"].numel() * p["x"].element_size() * 2 for p in pinned)
+    d2h = sum(p["y"].numel() * p["y"].element_size() * 2 + sum(v.numel() * 4 for v in p["grads"].values())
+              for p in pinned)
+
+    def e2e_step():
+        for (s, _, d, ws, out), hp in zip(layers, pinned):
+            d["x"].copy_(hp["x"], non_blocking=True)
+            d["dy"].copy_(hp["dy"], non_blocking=True)
+            p = [d[n] for n in PARAMS]
+            W.wtconv_forward(d["x"], *p, y=out["y"], stream=stream)
+            W.wtconv_backward(d["x"], d["dy"], *p, dx=out["dx"], grads=out["grads"], workspace=ws, stream=stream)
+            hp["y"].copy_(out["y"], non_blocking=True)
+            hp["dx"].copy_(out["dx"], non_blocking=True)
+            for g in GRADS:
+                hp["grads"][g].copy_(out["grads"][g], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(3, min(args.steps, 50))
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    barrier(world)
+
+    # roofline of the dominant kernel (largest share of the step)
+    acc = [algorithmic(s) for s, *_ in layers]
+    fwd_tot, bwd_tot = sum(fwd_ms), sum(bwd_ms)
+    if bwd_tot >= fwd_tot:
+        kname, ms, flop, byt = "wtconv_bwd_kernel", bwd_tot, sum(a["bwd_flop"] for a in acc), sum(a["bwd_bytes"] for a in acc)
+    else:
+        kname, ms, flop, byt = "wtconv_fwd_kernel", fwd_tot, sum(a["fwd_flop"] for a in acc), sum(a["fwd_bytes"] for a in acc)
+    launches = len(layers)
+    achieved_tflops = flop / (ms / 1e3) / 1e12
+    peaks = measured_peaks()
+    hbm_peak = peaks.get("hbm_gbs", HBM_FALLBACK_GBS)
+    hbm_gbs = byt / (ms / 1e3) / 1e9
+    traffic = profiled_traffic(kname, args.workload)
+    roofline = {
+        "bound": "alu", "achieved": round(achieved_tflops, 3), "peak": round(FP32_PEAK_TFLOPS, 2),
+        "unit": "TFLOP/s", "frac": round(achieved_tflops / FP32_PEAK_TFLOPS, 4),
+        "traffic": None if traffic is None else traffic,
+        "kernel": kname, "launch_ms": round(ms / launches, 5),
+        "hbm_achieved_gbs": round(hbm_gbs, 1), "hbm_peak_gbs": hbm_peak,
+        "hbm_frac": round(hbm_gbs / hbm_peak, 4),
+        "peak_note": "FP32 FMA peak = 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz; HBM peak of measured copy",
+    }
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": shapes[0].dtype, "data": "synthetic",
+        "config": {"workload": args.workload, "layers": [s.as_dict() for s in shapes],
+                   "l2": "flushed before every timed step (256 MiB write, outside the event bracket)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "fwd_ms": round(fwd_tot, 5), "bwd_ms": round(bwd_tot, 5),
+        "roofline": roofline,
+        "e2e": {"value": round(whole_job_throughput(elements, world, e2e_ms / 1e3), 3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 3 * len(layers) * args.steps,
+        "clocks": clk.summary(),
+    }
+    return line
+
+
+# -------------------------------------------------------------------------- oracle arm
+
+def oracle_layers(workload: str):
+    return [(s, make_inputs(s, seed=i)) for i, s in enumerate(WORKLOADS[workload])]
+
+
+def oracle_run(layers, b: int, threads: int):
+    """One fwd+bwd of the CPU oracle on the first b batch entries of every layer: (elements, s)."""
+    import oracle
+    elements, secs = 0, 0.0
+    for s, inp in layers:
+        bb = min(s.B, b)
+        sub = dict(inp, x=inp["x"][:bb].contiguous(), dy=inp["dy"][:bb].contiguous())
+        t0 = time.perf_counter()
+        oracle.forward(sub["x"], sub, nthreads=threads)
+        oracle.backward(sub["x"], sub["dy"], sub, nthreads=threads)
+        secs += time.perf_counter() - t0
+        elements += bb * s.C * s.H * s.W
+    return elements, secs
+
+
+def oracle_sample_size(layers, budget_s: float, threads: int) -> int:
+    """Batch entries per layer whose fwd+bwd takes about budget_s (at least 1)."""
+    bmax = max(s.B for s, _ in layers)
+    _, t1 = oracle_run(layers, 1, threads)
+    return int(max(1, min(bmax, budget_s / max(t1, 1e-6))))
+
+
+def cpu_baseline(workload: str, budget_s: float) -> dict:
+    import oracle
+    threads = oracle.default_threads()
+    layers = oracle_layers(workload)
+    b = oracle_sample_size(layers, budget_s, threads)
+    elements, secs = oracle_run(layers, b, threads)
+    return {"value": round(elements / secs / 1e9, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {b} batch entries of every layer of {workload}, one fwd+bwd, fp64, "
+                      f"{threads} threads, {secs:.2f} s"}
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands on the host cores; each step is a bounded sample of the workload
+    sized so that warm-up + timed steps take about two minutes in all."""
+    if rank != 0:
+        return None
+    import oracle
+    threads = oracle.default_threads()
+    layers = oracle_layers(args.workload)
+    per_step = min(5.0, 120.0 / (args.steps + args.warmup))
+    b = oracle_sample_size(layers, per_step, threads)
+    for _ in range(args.warmup):
+        oracle_run(layers, b, threads)
+    elements, secs = 0, 0.0
+    for _ in range(args.steps):
+        e, t = oracle_run(layers, b, threads)
+        elements += e
+        secs += t
+    value = elements / secs / 1e9
+    shapes = WORKLOADS[args.workload]
+    desc = f"first {b} batch entries of every layer of {args.workload} per step, fwd+bwd, fp64, {threads} threads"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": [s.as_dict() for s in shapes]},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------------- main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("cuda", "reference"), default="cuda")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stage1_f32")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "cuda" else "gloo"
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            line = run_reference(args, world, rank)
+        else:
+            W.load()
+            line = run_gpu(args, world, rank, local)
+            if rank == 0 and not args.no_cpu_baseline:
+                line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=8.0)
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

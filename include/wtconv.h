@@ -1,0 +1,128 @@
+/*
+ * wtconv.h -- C ABI of the GB300 (sm_103a) WTConv layer library (libwtconv.so).
+ *
+ * The layer (paper: "Fast and Memory-Efficient Wavelet Convolutions via I/O-Aware
+ * Reformulation", arXiv 2608.10805; its technical summary "Resumo Tecnico", sections Problema
+ * and Metodologia) maps an input x of shape (B, C, H, W) to
+ *
+ *     y = s_b * (conv_k(x, w_b) + b_b)                                      base path
+ *       + sum_{l=1..L} Synth_l( s_l * conv_k(Analysis_l(x), w_l) )           wavelet path
+ *
+ * where Analysis_l is the l-level orthonormal 2-D Haar decomposition (LL, LH, HL, HH subbands of
+ * the low band of level l-1), conv_k is a depthwise k x k cross-correlation with zero 'same'
+ * padding at each level's resolution, s_l a learned scale per subband channel, and Synth_l the
+ * inverse cascade.  The library evaluates it the paper's I/O-aware way: the Haar butterflies are
+ * recomputed on chip from one read of x, scales are folded into the conv weights, and the
+ * synthesis is the closed form in which output pixel (h, w) gathers its level-l terms at
+ * (h >> l, w >> l) with signs set by bit l-1 of h and w.  The backward applies the same
+ * reformulation in transpose.
+ *
+ * Conventions shared by every entry point:
+ *   - B, C, H, W > 0; 1 <= L <= WTCONV_MAX_LEVELS; k odd, 1 <= k <= 7 (k in {3, 5, 7} run;
+ *     other odd k return WTCONV_ERR_UNSUPPORTED); H and W divisible by 2^L.
+ *   - dtype (WTCONV_F32 / WTCONV_BF16 / WTCONV_F16) is the type of the activations x, y, dy,
+ *     dx.  Parameters and parameter gradients are always fp32; all arithmetic is fp32 with
+ *     round-to-nearest-even on the final store of a bf16 / fp16 activation.
+ *   - Layouts are contiguous row-major: x, y, dy, dx [B][C][H][W]; base_w [C][k][k];
+ *     base_bias, base_scale [C]; wavelet_w [L][4C][k][k]; wavelet_scale [L][4C], where subband
+ *     channel 4c+s holds subband s (0 LL, 1 LH, 2 HL, 3 HH) of input channel c at that level.
+ *   - Every pointer is caller-owned DEVICE memory (cudaMalloc or an allocator on top of it).
+ *     Activation pointers and the workspace must be 16-byte aligned, parameter and gradient
+ *     pointers 4-byte aligned.  The library allocates no device memory; scratch is the
+ *     caller's `workspace` of at least wtconv_workspace_size(...) bytes (may be NULL when that
+ *     size is 0).  Inputs are never written.  Outputs are fully overwritten (gradients are
+ *     not accumulated into).
+ *   - Calls are asynchronous on `stream` (NULL: the legacy default stream) and never
+ *     synchronise.  Arguments are validated on the host before anything is launched: on any
+ *     error no kernel runs and no output is touched.  Faults in a launched kernel surface at
+ *     the caller's next synchronisation, as with any CUDA launch.
+ *   - The library keeps no state between calls; concurrent calls on different streams with
+ *     distinct workspaces are safe.
+ *   - Setting the environment variable WTCONV_INJECT_FAULT=1 makes every compute entry point
+ *     return WTCONV_ERR_INJECTED before launching anything (host-side fault injection).
+ */
+#ifndef WTCONV_H
+#define WTCONV_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object type as cudaStream_t / CUstream; declared here so this header needs no CUDA
+ * header. */
+typedef struct CUstream_st *wtconv_stream_t;
+
+enum wtconv_dtype { WTCONV_F32 = 0, WTCONV_BF16 = 1, WTCONV_F16 = 2 };
+
+enum wtconv_status {
+    WTCONV_OK = 0,
+    WTCONV_ERR_INVALID_ARG = 1, /* bad shape, null or misaligned pointer */
+    WTCONV_ERR_UNSUPPORTED = 2, /* valid but not built: dtype, k, or a plane too large */
+    WTCONV_ERR_WORKSPACE = 3,   /* workspace smaller than wtconv_workspace_size() */
+    WTCONV_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+    WTCONV_ERR_INJECTED = 5     /* WTCONV_INJECT_FAULT is set */
+};
+
+/* Operation selector for wtconv_workspace_size. */
+enum wtconv_op {
+    WTCONV_OP_FORWARD = 0,
+    WTCONV_OP_BACKWARD_INPUT = 1,
+    WTCONV_OP_BACKWARD_WEIGHTS = 2,
+    WTCONV_OP_BACKWARD = 3
+};
+
+#define WTCONV_MAX_LEVELS 5
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int wtconv_version(void);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char *wtconv_strerror(int status);
+
+/* Bytes of device workspace `op` needs for this shape on the current device (0 if none).
+ * Returns 0 for an invalid shape as well; the compute call then reports the error. */
+size_t wtconv_workspace_size(int op, int B, int C, int H, int W, int L, int k, int dtype);
+
+/* Forward pass (Metodologia: fused on-chip Haar analysis, folded scales, closed-form
+ * synthesis).  Writes y [B][C][H][W]. */
+int wtconv_forward(int B, int C, int H, int W, int L, int k, int dtype, const void *x,
+                   const float *base_w, const float *base_bias, const float *base_scale,
+                   const float *wavelet_w, const float *wavelet_scale, void *y, void *workspace,
+                   size_t workspace_bytes, wtconv_stream_t stream);
+
+/* Gradient with respect to the input: dx = sum_l Synth_l(s_l * corr(Analysis_l(dy), flip(w_l)))
+ * + s_b * corr(dy, flip(w_b)), the transpose of the forward's linear part (the bias drops out).
+ * Reads dy, writes dx, both [B][C][H][W]. */
+int wtconv_backward_input(int B, int C, int H, int W, int L, int k, int dtype,
+                          const float *base_w, const float *base_bias, const float *base_scale,
+                          const float *wavelet_w, const float *wavelet_scale, const void *dy,
+                          void *dx, void *workspace, size_t workspace_bytes,
+                          wtconv_stream_t stream);
+
+/* Gradients of every parameter (Contribuicoes: "all parameter gradients") from x and dy.
+ * Writes d_base_w [C][k][k], d_base_bias [C], d_base_scale [C], d_wavelet_w [L][4C][k][k],
+ * d_wavelet_scale [L][4C].  Deterministic: the reduction order is fixed for a given device and
+ * shape. */
+int wtconv_backward_weights(int B, int C, int H, int W, int L, int k, int dtype, const void *x,
+                            const void *dy, const float *base_w, const float *base_bias,
+                            const float *base_scale, const float *wavelet_w,
+                            const float *wavelet_scale, float *d_base_w, float *d_base_bias,
+                            float *d_base_scale, float *d_wavelet_w, float *d_wavelet_scale,
+                            void *workspace, size_t workspace_bytes, wtconv_stream_t stream);
+
+/* Fused backward: dx and every parameter gradient in one pass that reads x and dy once.
+ * Same results as wtconv_backward_input followed by wtconv_backward_weights. */
+int wtconv_backward(int B, int C, int H, int W, int L, int k, int dtype, const void *x,
+                    const void *dy, const float *base_w, const float *base_bias,
+                    const float *base_scale, const float *wavelet_w, const float *wavelet_scale,
+                    void *dx, float *d_base_w, float *d_base_bias, float *d_base_scale,
+                    float *d_wavelet_w, float *d_wavelet_scale, void *workspace,
+                    size_t workspace_bytes, wtconv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WTCONV_H */

@@ -1,0 +1,150 @@
+"""CUDA path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Bar: max|gpu - oracle| <= 1e-5 max|oracle| for fp32 activations, <= 2e-2 max|oracle| for bf16 /
+fp16, for every output tensor (y, dx and each parameter gradient)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from memory_bound_cnn_gb300 import wtconv as W
+from memory_bound_cnn_gb300.inputs import WORKLOAD_ORDER, LayerShape, make_inputs, workload_inputs
+from parity import GRADS, PARAMS, TOL, assert_close, gpu_backward, gpu_backward_split, gpu_forward, np64, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def check_layer(shape: LayerShape, inputs: dict, split: bool = True):
+    tol = TOL[shape.dtype]
+    d = to_device(inputs)
+    y = gpu_forward(d)
+    dx, g = gpu_backward(d)
+    torch.cuda.synchronize()
+    y_ref = oracle.forward(inputs["x"], inputs)
+    g_ref = oracle.backward(inputs["x"], inputs["dy"], inputs)
+    assert_close("y", np64(y), y_ref, tol)
+    assert_close("dx", np64(dx), g_ref["dx"], tol)
+    for n in GRADS:
+        assert_close(n, np64(g[n]), g_ref[n], tol)
+    if split:
+        dx2, g2 = gpu_backward_split(d)
+        torch.cuda.synchronize()
+        assert_close("dx (backward_input)", np64(dx2), g_ref["dx"], tol)
+        for n in GRADS:
+            assert_close(n + " (backward_weights)", np64(g2[n]), g_ref[n], tol)
+
+
+@pytest.mark.parametrize("name", WORKLOAD_ORDER)
+def test_workload_parity(name):
+    """Every layer of every named workload, at full size."""
+    for shape, inputs in workload_inputs(name):
+        check_layer(shape, inputs, split=(shape.numel <= 20_000_000))
+
+
+SWEEP = [
+    # (B, C, H, W, L, k, dtype): ragged tiles, one-pixel deepest levels, non-square, packing
+    (1, 1, 2, 2, 1, 3, "f32"),
+    (1, 1, 4, 4, 2, 5, "f32"),
+    (2, 3, 6, 10, 1, 5, "f32"),
+    (3, 2, 8, 24, 3, 3, "f32"),
+    (2, 5, 12, 20, 2, 7, "f32"),
+    (4, 3, 32, 32, 5, 5, "f32"),
+    (1, 2, 64, 32, 4, 7, "f32"),
+    (5, 7, 16, 8, 3, 5, "bf16"),
+    (3, 4, 40, 24, 3, 5, "bf16"),
+    (2, 3, 28, 28, 2, 3, "f16"),
+    (17, 3, 8, 8, 1, 5, "bf16"),
+    (33, 2, 4, 4, 2, 5, "f32"),
+    (2, 2, 96, 64, 5, 5, "bf16"),
+]
+
+
+@pytest.mark.parametrize("case", SWEEP, ids=lambda c: "x".join(map(str, c)))
+def test_shape_sweep(case):
+    shape = LayerShape(*case)
+    check_layer(shape, make_inputs(shape, seed=11))
+
+
+def test_backward_is_deterministic():
+    shape = LayerShape(8, 16, 28, 28, 2, 5, "bf16")
+    d = to_device(make_inputs(shape, seed=3))
+    dx1, g1 = gpu_backward(d)
+    dx2, g2 = gpu_backward(d)
+    torch.cuda.synchronize()
+    assert torch.equal(dx1, dx2)
+    for n in GRADS:
+        assert torch.equal(g1[n], g2[n]), n
+
+
+def test_input_gradient_is_forward_with_rotated_kernels():
+    """dx = forward(dy) with every kernel rotated 180 degrees and no bias (transpose identity)."""
+    shape = LayerShape(2, 4, 32, 32, 3, 5, "f32")
+    d = to_device(make_inputs(shape, seed=5))
+    dx = W.wtconv_backward_input(d["dy"], *[d[p] for p in PARAMS])
+    flipped = dict(d)
+    flipped["base_w"] = torch.flip(d["base_w"], dims=(-2, -1)).contiguous()
+    flipped["wavelet_w"] = torch.flip(d["wavelet_w"], dims=(-2, -1)).contiguous()
+    flipped["base_bias"] = torch.zeros_like(d["base_bias"])
+    y = W.wtconv_forward(d["dy"], *[flipped[p] for p in PARAMS])
+    torch.cuda.synchronize()
+    assert_close("dx vs rotated forward", np64(dx), np64(y), 1e-6)
+
+
+def test_outputs_stay_in_bounds_and_inputs_untouched():
+    """Canary words around every output; inputs byte-identical after the calls."""
+    shape = LayerShape(3, 5, 24, 16, 3, 5, "bf16")
+    inputs = make_inputs(shape, seed=9)
+    d = to_device(inputs)
+    before = {k: v.clone() for k, v in d.items()}
+    pad = 4096
+    n = shape.numel
+    ybuf = torch.full((n + 2 * pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+    dxbuf = torch.full((n + 2 * pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+    y = ybuf[pad:pad + n].view(shape.B, shape.C, shape.H, shape.W)
+    dx = dxbuf[pad:pad + n].view(shape.B, shape.C, shape.H, shape.W)
+    W.wtconv_forward(d["x"], *[d[p] for p in PARAMS], y=y)
+    gbufs = {}
+    grads = {}
+    for gname, p in zip(GRADS, PARAMS):
+        m = d[p].numel()
+        buf = torch.full((m + 2 * 64,), 7.0, device="cuda")
+        gbufs[gname] = buf
+        grads[gname] = buf[64:64 + m].view_as(d[p])
+    W.wtconv_backward(d["x"], d["dy"], *[d[p] for p in PARAMS], dx=dx, grads=grads)
+    torch.cuda.synchronize()
+    for buf in (ybuf, dxbuf):
+        assert torch.all(buf[:pad] == 7.0) and torch.all(buf[pad + n:] == 7.0)
+    for gname, buf in gbufs.items():
+        assert torch.all(buf[:64] == 7.0) and torch.all(buf[-64:] == 7.0), gname
+    for k in d:
+        assert torch.equal(d[k], before[k]), k
+
+
+def test_autograd_function_matches_oracle():
+    shape = LayerShape(2, 3, 16, 16, 2, 5, "f32")
+    inputs = make_inputs(shape, seed=2)
+    d = to_device(inputs)
+    leaves = {k: d[k].clone().requires_grad_(True) for k in ("x",) + PARAMS}
+    y = W.WTConvFunction.apply(leaves["x"], *[leaves[p] for p in PARAMS])
+    y.backward(d["dy"])
+    g_ref = oracle.backward(inputs["x"], inputs["dy"], inputs)
+    assert_close("autograd dx", np64(leaves["x"].grad), g_ref["dx"], 1e-5)
+    for gname, p in zip(GRADS, PARAMS):
+        assert_close("autograd " + gname, np64(leaves[p].grad), g_ref[gname], 1e-5)
+
+
+def test_invalid_call_raises_and_writes_nothing(monkeypatch):
+    shape = LayerShape(2, 3, 16, 16, 2, 5, "f32")
+    d = to_device(make_inputs(shape, seed=1))
+    x_bad = d["x"][:, :, :, :14].contiguous()       # W = 14 is not divisible by 2^L = 4
+    y = torch.full_like(x_bad, 3.0)
+    with pytest.raises(W.WTConvError) as e:
+        W.wtconv_forward(x_bad, *[d[p] for p in PARAMS], y=y)
+    assert e.value.status == W.ERR_INVALID_ARG
+    y2 = torch.full_like(d["x"], 3.0)
+    monkeypatch.setenv("WTCONV_INJECT_FAULT", "1")
+    with pytest.raises(W.WTConvError) as e:
+        W.wtconv_forward(d["x"], *[d[p] for p in PARAMS], y=y2)
+    assert e.value.status == W.ERR_INJECTED
+    torch.cuda.synchronize()
+    assert torch.all(y == 3.0) and torch.all(y2 == 3.0)
