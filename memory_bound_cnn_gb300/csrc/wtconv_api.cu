@@ -4,7 +4,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdlib.h>
+#include <stdio.h>
 #include <string.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "wtconv.h"
 #include "wtconv_internal.h"
@@ -14,7 +19,6 @@ using namespace wtconv;
 namespace {
 
 constexpr int kStaticSmemMargin = 1024;  // static shared memory of the kernels (the Geo copy)
-constexpr int kTargetSlotPixels = 1024;  // gather small planes until a CTA holds this many pixels
 
 bool fault_injected() {
     const char *v = getenv("WTCONV_INJECT_FAULT");
@@ -49,51 +53,198 @@ int device_sms() {
     return sms;
 }
 
-// Forward and input-gradient kernels: one plane group per CTA.
-Plan plan_forward(int B, int C, int H, int W, int L, int k) {
-    Plan p;
-    LayerArgs &a = p.a;
-    a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
-    a.geo = make_geo(H, W, L, k, /*with_dy=*/false, /*with_z=*/true);
-    int G = kTargetSlotPixels / (H * W);
-    if (G < 1) G = 1;
-    if (G > B) G = B;
-    while (G > 1 && fwd_smem_bytes(a.geo, G, L, k) + kStaticSmemMargin > (size_t)kMaxSmem) --G;
-    p.smem = fwd_smem_bytes(a.geo, G, L, k);
-    if (p.smem + kStaticSmemMargin > (size_t)kMaxSmem) { p.status = WTCONV_ERR_UNSUPPORTED; return p; }
-    a.G = G;
-    a.groups_per_cta = 1;
-    a.nb = (B + G - 1) / G;
-    return p;
+// Conv items (kRows x kCols outputs) of one plane over all 1+4L images.
+int items_per_plane(const Geo &g) {
+    int n = 0;
+    for (int l = 0; l <= g.L; ++l) n += (l == 0 ? 1 : 4) * g.rseg[l] * g.cstr[l];
+    return n;
 }
 
-// Backward kernel: CTAs walk several plane groups of one channel so that the weight-gradient
-// partials stay small; about eight waves of resident CTAs keep the tail short.
-Plan plan_backward(int B, int C, int H, int W, int L, int k, int dtype, bool want_dx) {
+// Item balance of the forward's round-robin conv phase on T threads.
+double fwd_balance(const Geo &g, int G, int T) {
+    const int items = G * items_per_plane(g);
+    const int rounds = (items + T - 1) / T;
+    return (double)items / ((double)rounds * T);
+}
+
+// Balance of the weight-gradient schedule (mirrors the kernel's: each thread takes d items of a
+// single correlation; d is the smallest count for which all correlations fit on T threads).
+double dw_balance(const Geo &g, int G, int T) {
+    int tot = 0;
+    const int nsig = 1 + 4 * g.L;
+    for (int s = 0; s < nsig; ++s) {
+        const int l = s == 0 ? 0 : (s - 1) / 4 + 1;
+        tot += G * g.rseg[l] * g.cstr[l];
+    }
+    int d = (tot + T - 1) / T;
+    if (d < 1) d = 1;
+    for (;; ++d) {
+        int need = 0;
+        for (int s = 0; s < nsig; ++s) {
+            const int l = s == 0 ? 0 : (s - 1) / 4 + 1;
+            need += (G * g.rseg[l] * g.cstr[l] + d - 1) / d;
+        }
+        if (need <= T) break;
+    }
+    return (double)tot / ((double)d * T);
+}
+
+int elem_bytes(int dtype) { return dtype == WTCONV_F32 ? 4 : 2; }
+
+void set_io_modes(LayerArgs &a, int dtype) {
+    a.vec_ld = (a.W % 4) == 0;
+    if (dtype == WTCONV_F32) a.st_mode = (a.W % 4) == 0 ? 2 : 0;
+    else a.st_mode = (a.W % 8) == 0 ? 2 : ((a.W % 4) == 0 ? 1 : 0);
+    // staged copies move whole planes in 16-byte pieces
+    a.stage = ((size_t)a.H * a.W * elem_bytes(dtype)) % 16 == 0;
+}
+
+// Fast-division magic numbers of every runtime divisor the kernels use.
+void set_divs(LayerArgs &a, int dtype) {
+    const Geo &g = a.geo;
+    Divs &d = a.dv;
+    d = Divs{};
+    // analysis pass 1 (levels 1-2 from 4x4 blocks, or level 1 from 2x2 blocks when L == 1)
+    if (g.L >= 2) { d.a_w[1] = make_fastdiv(g.W >> 2); d.a_n[1] = make_fastdiv((g.H >> 2) * (g.W >> 2)); }
+    else { d.a_w[1] = make_fastdiv(g.W >> 1); d.a_n[1] = make_fastdiv((g.H >> 1) * (g.W >> 1)); }
+    for (int l = 3; l <= g.L; l += 2) {  // deeper passes from the level l-1 low band
+        const int hs = g.h[l - 1], ws = g.w[l - 1];
+        if (l + 1 <= g.L) { d.a_w[l] = make_fastdiv(ws >> 2); d.a_n[l] = make_fastdiv((hs >> 2) * (ws >> 2)); }
+        else { d.a_w[l] = make_fastdiv(ws >> 1); d.a_n[l] = make_fastdiv((hs >> 1) * (ws >> 1)); }
+    }
+    d.stage_chunks = make_fastdiv((uint32_t)((size_t)g.H * g.W * elem_bytes(dtype) / 16));
+    for (int l = 0; l <= g.L; ++l) {
+        d.item_plane[l] = make_fastdiv(g.rseg[l] * g.cstr[l]);
+        d.item_cols[l] = make_fastdiv(g.cstr[l]);
+    }
+    const int nws = (g.W + 7) / 8;
+    d.out_w = make_fastdiv(nws);
+    d.out_n = make_fastdiv(g.H * nws);
+}
+
+typedef size_t (*SmemFn)(const Geo &, int, int, int, int, bool, int *);
+typedef double (*BalFn)(const Geo &, int, int);
+typedef int (*OccFn)(int, int, int, size_t);
+
+// Planes per CTA (G) and CTA size (T): score = item balance x resident warps per SM (capped at
+// 16, enough to hide latency), over G whose shared memory fits; ties go to the smaller G.
+bool choose_launch(LayerArgs &a, int dtype, SmemFn smem_fn, BalFn bal_fn, OccFn occ_fn, size_t *smem_out) {
+    const int eb = elem_bytes(dtype);
+    double best = -1.0;
+    int bestG = 0, bestT = 0;
+    size_t best_smem = 0;
+    for (int T : {256, 128}) {
+        for (int G = 1; G <= a.B && G <= 64; ++G) {
+            const size_t smem = smem_fn(a.geo, G, a.L, a.K, eb, a.stage != 0, nullptr);
+            if (smem + kStaticSmemMargin > (size_t)kMaxSmem) break;
+            const int occ = occ_fn(dtype, a.K, T, smem);
+            if (occ <= 0) continue;
+            int warps = occ * T / 32;
+            if (warps > 16) warps = 16;
+            const double score = bal_fn(a.geo, G, T) * warps;
+            if (score > best + 1e-9) { best = score; bestG = G; bestT = T; best_smem = smem; }
+        }
+    }
+    if (bestG == 0) return false;
+    a.G = bestG;
+    a.threads = bestT;
+    int off = 0;
+    *smem_out = smem_fn(a.geo, bestG, a.L, a.K, eb, a.stage != 0, &off);
+    a.stage_off = off;
+    (void)best_smem;
+    return true;
+}
+
+// Forward and input-gradient kernel.
+Plan plan_forward_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
     Plan p;
     LayerArgs &a = p.a;
     a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
-    a.want_dx = want_dx ? 1 : 0;
-    a.geo = make_geo(H, W, L, k, /*with_dy=*/true, /*with_z=*/want_dx);
-    int G = kTargetSlotPixels / (H * W);
-    if (G < 1) G = 1;
-    if (G > B) G = B;
-    while (G > 1 && bwd_smem_bytes(a.geo, G, L, k) + kStaticSmemMargin > (size_t)kMaxSmem) --G;
-    p.smem = bwd_smem_bytes(a.geo, G, L, k);
-    if (p.smem + kStaticSmemMargin > (size_t)kMaxSmem) { p.status = WTCONV_ERR_UNSUPPORTED; return p; }
-    a.G = G;
+    a.geo = make_geo(H, W, L, k, 0);
+    set_io_modes(a, dtype);
     const int sms = device_sms();
-    const int occ = occupancy_backward(dtype, k, p.smem);
-    if (sms <= 0 || occ <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
-    const int ngroups = (B + G - 1) / G;
-    const long long target = 8LL * sms * occ;
+    if (sms <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
+    if (!choose_launch(a, dtype, fwd_smem_bytes, fwd_balance, occupancy_forward, &p.smem)) {
+        p.status = WTCONV_ERR_UNSUPPORTED;
+        return p;
+    }
+    set_divs(a, dtype);
+    const int occ = occupancy_forward(dtype, k, a.threads, p.smem);
+    const int ngroups = (B + a.G - 1) / a.G;
+    const long long target = 4LL * sms * occ;  // about four waves of resident CTAs
     long long nb = (target + C - 1) / C;
     if (nb < 1) nb = 1;
     if (nb > ngroups) nb = ngroups;
     a.groups_per_cta = (int)((ngroups + nb - 1) / nb);
     a.nb = (ngroups + a.groups_per_cta - 1) / a.groups_per_cta;
-    p.workspace = (size_t)a.nb * C * (1 + 4 * L) * dw_na(k) * sizeof(float);
     return p;
+}
+
+// Weight-gradient kernel: fewer, longer-lived CTAs keep the per-CTA partials small.
+Plan plan_dw_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
+    Plan p;
+    LayerArgs &a = p.a;
+    a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
+    a.geo = make_geo(H, W, L, k, 1);
+    set_io_modes(a, dtype);
+    const int sms = device_sms();
+    if (sms <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
+    if (!choose_launch(a, dtype, dw_smem_bytes, dw_balance, occupancy_dw, &p.smem)) {
+        p.status = WTCONV_ERR_UNSUPPORTED;
+        return p;
+    }
+    set_divs(a, dtype);
+    const int occ = occupancy_dw(dtype, k, a.threads, p.smem);
+    const int ngroups = (B + a.G - 1) / a.G;
+    const long long target = 4LL * sms * occ;
+    long long nb = (target + C - 1) / C;
+    if (nb < 1) nb = 1;
+    if (nb > ngroups) nb = ngroups;
+    a.groups_per_cta = (int)((ngroups + nb - 1) / nb);
+    a.nb = (ngroups + a.groups_per_cta - 1) / a.groups_per_cta;
+    p.workspace = (size_t)a.nb * C * (1 + 4 * L) * (k * k + 1) * sizeof(float);
+    return p;
+}
+
+// Plans depend only on the shape, dtype and device; they are computed once and reused (the
+// occupancy queries behind them cost far more than a launch).
+typedef std::tuple<int, int, int, int, int, int, int, int, int> PlanKey;
+
+Plan cached_plan(int kind, int B, int C, int H, int W, int L, int k, int dtype) {
+    static std::mutex mu;
+    static std::map<PlanKey, Plan> cache;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        Plan p;
+        p.status = WTCONV_ERR_CUDA;
+        return p;
+    }
+    const PlanKey key(kind, B, C, H, W, L, k, dtype, dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    Plan p = kind == 0 ? plan_forward_uncached(B, C, H, W, L, k, dtype) : plan_dw_uncached(B, C, H, W, L, k, dtype);
+    const char *verbose = getenv("WTCONV_VERBOSE");
+    if (verbose && verbose[0] == '1')
+        fprintf(stderr, "wtconv plan %s B=%d C=%d H=%d W=%d L=%d k=%d dtype=%d: status %d G=%d threads=%d nb=%d "
+                        "groups/cta=%d smem=%zu stage=%d workspace=%zu\n",
+                kind == 0 ? "fwd" : "dw", B, C, H, W, L, k, dtype, p.status, p.a.G, p.a.threads, p.a.nb,
+                p.a.groups_per_cta, p.smem, p.a.stage, p.workspace);
+    if (p.status == WTCONV_OK) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache.emplace(key, p);
+    }
+    return p;
+}
+
+Plan plan_forward(int B, int C, int H, int W, int L, int k, int dtype) {
+    return cached_plan(0, B, C, H, W, L, k, dtype);
+}
+
+Plan plan_dw(int B, int C, int H, int W, int L, int k, int dtype) {
+    return cached_plan(1, B, C, H, W, L, k, dtype);
 }
 
 void set_params(LayerArgs &a, const float *base_w, const float *base_bias, const float *base_scale,
@@ -131,7 +282,7 @@ const char *wtconv_strerror(int status) {
 size_t wtconv_workspace_size(int op, int B, int C, int H, int W, int L, int k, int dtype) {
     if (validate_shape(B, C, H, W, L, k, dtype) != WTCONV_OK) return 0;
     if (op == WTCONV_OP_BACKWARD_WEIGHTS || op == WTCONV_OP_BACKWARD) {
-        Plan p = plan_backward(B, C, H, W, L, k, dtype, op == WTCONV_OP_BACKWARD);
+        Plan p = plan_dw(B, C, H, W, L, k, dtype);
         return p.status == WTCONV_OK ? p.workspace : 0;
     }
     return 0;
@@ -147,7 +298,7 @@ int wtconv_forward(int B, int C, int H, int W, int L, int k, int dtype, const vo
     if (!aligned16(x) || !aligned16(y) || !params_ok(base_w, base_bias, base_scale, wavelet_w, wavelet_scale))
         return WTCONV_ERR_INVALID_ARG;
     if (fault_injected()) return WTCONV_ERR_INJECTED;
-    Plan p = plan_forward(B, C, H, W, L, k);
+    Plan p = plan_forward(B, C, H, W, L, k, dtype);
     if (p.status != WTCONV_OK) return p.status;
     p.a.x = x; p.a.out = y;
     set_params(p.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
@@ -165,7 +316,7 @@ int wtconv_backward_input(int B, int C, int H, int W, int L, int k, int dtype, c
     if (!aligned16(dy) || !aligned16(dx) || !params_ok(base_w, base_bias, base_scale, wavelet_w, wavelet_scale))
         return WTCONV_ERR_INVALID_ARG;
     if (fault_injected()) return WTCONV_ERR_INJECTED;
-    Plan p = plan_forward(B, C, H, W, L, k);
+    Plan p = plan_forward(B, C, H, W, L, k, dtype);
     if (p.status != WTCONV_OK) return p.status;
     p.a.x = dy; p.a.out = dx;
     set_params(p.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
@@ -185,17 +336,26 @@ static int backward_common(bool want_dx, int B, int C, int H, int W, int L, int 
         !params_ok(d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale))
         return WTCONV_ERR_INVALID_ARG;
     if (fault_injected()) return WTCONV_ERR_INJECTED;
-    Plan p = plan_backward(B, C, H, W, L, k, dtype, want_dx);
-    if (p.status != WTCONV_OK) return p.status;
-    if (workspace_bytes < p.workspace || (p.workspace > 0 && !aligned16(workspace))) return WTCONV_ERR_WORKSPACE;
-    p.a.x = x; p.a.dy = dy; p.a.out = want_dx ? dx : nullptr;
-    set_params(p.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
-    p.a.flip = 1; p.a.with_bias = 0;
-    p.a.partials = static_cast<float *>(workspace);
+    Plan pw = plan_dw(B, C, H, W, L, k, dtype);
+    if (pw.status != WTCONV_OK) return pw.status;
+    Plan pf;
+    if (want_dx) {
+        pf = plan_forward(B, C, H, W, L, k, dtype);
+        if (pf.status != WTCONV_OK) return pf.status;
+    }
+    if (workspace_bytes < pw.workspace || (pw.workspace > 0 && !aligned16(workspace))) return WTCONV_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_backward(p.a, dtype, p.smem, s);
-    if (e != cudaSuccess) return WTCONV_ERR_CUDA;
-    return cuda_status(launch_dw_finalize(p.a, d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale, s));
+    if (want_dx) {
+        pf.a.x = dy; pf.a.out = dx;
+        set_params(pf.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
+        pf.a.flip = 1; pf.a.with_bias = 0;
+        if (launch_forward(pf.a, dtype, pf.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+    }
+    pw.a.x = x; pw.a.dy = dy;
+    set_params(pw.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
+    pw.a.partials = static_cast<float *>(workspace);
+    if (launch_dw(pw.a, dtype, pw.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+    return cuda_status(launch_dw_finalize(pw.a, d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale, s));
 }
 
 int wtconv_backward_weights(int B, int C, int H, int W, int L, int k, int dtype, const void *x, const void *dy,

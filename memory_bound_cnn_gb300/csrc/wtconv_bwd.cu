@@ -1,173 +1,170 @@
-// Backward kernels of the WTConv layer.
+// Weight-gradient kernels of the WTConv layer.
 //
-// wtconv_bwd_kernel: one CTA owns channel c and a run of batch entries.  Per plane group it reads
-// x and dy once, builds both Haar pyramids on chip (Yhat from x, Ghat from dy) and
-//   * (input gradient) convolves Ghat with the 180-degree-rotated folded kernels and writes dx
-//     through the same closed-form synthesis as the forward: dx = sum_l A_l^T K_l^T A_l dy + K_b^T dy;
-//   * (weight gradients) correlates Ghat^l_s with Yhat^l_s for every tap:
-//     dW'^l_s[u,v] = 4^-l sum_{i,j} Ghat[i,j] Yhat[i+u-P, j+v-P], and dy with x for the base kernel,
-//     accumulating in registers per lane, reducing across the warp with shuffles (fixed-order
-//     butterfly) and across warps and plane groups in shared memory.  Each CTA writes one
-//     partial per (channel, tap); no atomics, so the result is deterministic.
-// wtconv_dw_finalize_kernel sums the partials over the CTAs of a channel in a fixed order and
-// unfolds the scales by the chain rule: dw = s dW', ds = sum_t w dW' (+ b db' for the base), db = s_b db'.
-#include "wtconv_device.cuh"
+// wtconv_dw_kernel: each CTA owns channel c and a run of batch entries, walked in groups of G
+// planes.  Per group it reads x and dy once, builds both Haar pyramids on chip (Yhat from x,
+// Ghat from dy) and correlates them tap by tap:
+//     dW'^l_s[u, v] = 4^-l sum_{i,j} Ghat^l_s[i, j] Yhat^l_s[i+u-P, j+v-P]      (level l, subband s)
+//     dw'_b[u, v]   =      sum_{h,w} dy[h, w] x[h+u-P, w+v-P],   db' = sum dy  (base path)
+// Every thread is pinned to one of these 1+4L correlations for the whole CTA and owns a fixed
+// share of its sliding-window items, so its k*k tap sums stay in registers (packed f32x2 pairs)
+// across all planes; they are reduced once, at the end, in a fixed order -- no atomics, so the
+// result is deterministic.  Each CTA writes one partial per (channel, subband, tap).
+// wtconv_dw_finalize_kernel sums the partials of a channel in CTA order and unfolds the scales
+// by the chain rule through the folding W' = s w, b' = s_b b: dw = s dW', ds = sum_t w dW'
+// (+ b db' for the base path), db = s_b db'.
+#include "wtconv_analysis.cuh"
 
 namespace wtconv {
 
 static inline int n_sig(int L) { return 1 + 4 * L; }
 
-size_t bwd_smem_bytes(const Geo &geo, int G, int L, int K) {
-    size_t floats = (size_t)G * geo.slot_floats + (size_t)n_sig(L) * wslot_stride(K) + 4 +
-                    (size_t)n_sig(L) * kWarps * dw_na(K) + round_up(n_sig(L) + 1, 4);
-    return floats * sizeof(float);
-}
-
-// Tiles (4x4) of subband sig in one slot, and their column count.
-__device__ __forceinline__ void dw_sig_tiles(const Geo &geo, int sig, int &nt, int &tcols, int &lvl) {
-    lvl = sig == 0 ? 0 : (sig - 1) / 4 + 1;
-    const int h = geo.H >> lvl, w = geo.W >> lvl;
-    tcols = round_up(w, 4) / 4;
-    nt = (round_up(h, 4) / 4) * tcols;
-}
-
-template <int K>
-__device__ __forceinline__ void dw_phase(const Geo &geo, const float *slots, int G, const int *cstart,
-                                         int nsig, float *dwacc) {
-    constexpr int NA = dw_na(K), NA32 = dw_na32(K);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nchunks = cstart[nsig];
-    const int c_begin = (warp * nchunks) / kWarps, c_end = ((warp + 1) * nchunks) / kWarps;
-    float acc[NA32];
-#pragma unroll
-    for (int i = 0; i < NA32; ++i) acc[i] = 0.f;
-    int cur = -1;
-    for (int ch = c_begin; ch < c_end; ++ch) {
-        int sig = 0;
-        while (ch >= cstart[sig + 1]) ++sig;
-        if (sig != cur && cur >= 0) {
-            float res[NA32 / 32];
-            warp_reduce_scatter<NA32>(acc, res);
-#pragma unroll
-            for (int blk = 0; blk < NA32 / 32; ++blk) {
-                const int t = blk * 32 + lane;
-                if (t < NA) dwacc[(cur * kWarps + warp) * NA + t] += res[blk];
-            }
-#pragma unroll
-            for (int i = 0; i < NA32; ++i) acc[i] = 0.f;
-        }
-        cur = sig;
-        int nt, tcols, lvl;
-        dw_sig_tiles(geo, sig, nt, tcols, lvl);
-        const int item = (ch - cstart[sig]) * 32 + lane;
-        if (item < G * nt) {
-            const int g = item / nt, e = item - g * nt;
-            const int ti = e / tcols, tj = e - ti * tcols;
-            const float *slot = slots + (size_t)g * geo.slot_floats;
-            const float *ysrc, *gsrc;
-            if (lvl == 0) {
-                ysrc = slot + geo.off_x;
-                gsrc = slot + geo.off_dy;
-            } else {
-                const int s = (sig - 1) & 3, sub = s * geo.rows[lvl] * geo.pitch[lvl];
-                ysrc = slot + geo.off_y[lvl] + sub;
-                gsrc = slot + geo.off_g[lvl] + sub;
-            }
-            dw_tile_4x4<K>(ysrc, gsrc, geo.pitch[lvl], 4 * ti, 4 * tj, acc);
-        }
-    }
-    if (cur >= 0) {
-        float res[NA32 / 32];
-        warp_reduce_scatter<NA32>(acc, res);
-#pragma unroll
-        for (int blk = 0; blk < NA32 / 32; ++blk) {
-            const int t = blk * 32 + lane;
-            if (t < NA) dwacc[(cur * kWarps + warp) * NA + t] += res[blk];
-        }
-    }
+size_t dw_smem_bytes(const Geo &geo, int G, int L, int K, int elem_bytes, bool stage, int *stage_off) {
+    (void)L;
+    size_t slots = (size_t)G * geo.slot_floats * sizeof(float);
+    if (stage_off) *stage_off = (int)slots;
+    if (stage) slots += 2 * (size_t)G * geo.H * geo.W * elem_bytes;
+    const size_t red = (size_t)kMaxThreads * (K * K + 1) * sizeof(float);
+    const size_t bytes = slots > red ? slots : red;
+    return (bytes + 15) / 16 * 16;
 }
 
 template <int K, typename T>
-__global__ void __launch_bounds__(kThreads) wtconv_bwd_kernel(const LayerArgs a) {
+__global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_dw_kernel(const LayerArgs a) {
+    constexpr int P = K / 2, KK = K * K, NA = KK + 1;
     extern __shared__ __align__(16) float smem[];
     __shared__ Geo geo;
-    if (threadIdx.x == 0) geo = a.geo;
-    constexpr int NA = dw_na(K);
+    __shared__ int tstart[kMaxSig + 1];
+    __shared__ int per_thread;
     const int c = blockIdx.x % a.C;
     const int nbi = blockIdx.x / a.C;
-    const int G = a.G;
-    const int nsig = 1 + 4 * a.L;
+    const int G = a.G, nsig = 1 + 4 * a.L;
     float *slots = smem;
-    float *wts = smem + (size_t)G * a.geo.slot_floats;
-    float *bias_s = wts + nsig * wslot_stride(K);
-    float *dwacc = bias_s + 4;
-    int *cstart = reinterpret_cast<int *>(dwacc + nsig * kWarps * NA);
 
+    if (threadIdx.x == 0) {
+        geo = a.geo;
+        // items per thread d: the smallest d for which every subband's items fit on whole threads
+        int tot = 0;
+        for (int sig = 0; sig < nsig; ++sig) {
+            const int l = sig == 0 ? 0 : (sig - 1) / 4 + 1;
+            tot += G * a.geo.rseg[l] * a.geo.cstr[l];
+        }
+        int d = (tot + (int)blockDim.x - 1) / (int)blockDim.x;
+        if (d < 1) d = 1;
+        for (;; ++d) {
+            int need = 0;
+            for (int sig = 0; sig < nsig; ++sig) {
+                const int l = sig == 0 ? 0 : (sig - 1) / 4 + 1;
+                need += (G * a.geo.rseg[l] * a.geo.cstr[l] + d - 1) / d;
+            }
+            if (need <= (int)blockDim.x) break;
+        }
+        int t0 = 0;
+        for (int sig = 0; sig < nsig; ++sig) {
+            const int l = sig == 0 ? 0 : (sig - 1) / 4 + 1;
+            tstart[sig] = t0;
+            t0 += (G * a.geo.rseg[l] * a.geo.cstr[l] + d - 1) / d;
+        }
+        tstart[nsig] = t0;
+        per_thread = d;
+    }
     {
         float4 *s4 = reinterpret_cast<float4 *>(slots);
         const int n4 = G * a.geo.slot_floats / 4;
         for (int i = threadIdx.x; i < n4; i += blockDim.x) s4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = threadIdx.x; i < nsig * kWarps * NA; i += blockDim.x) dwacc[i] = 0.f;
-    }
-    if (a.want_dx) stage_weights<K>(a, c, wts, bias_s);
-    __syncthreads();
-    if (threadIdx.x == 0) {  // chunk table: 32 tiles per chunk, subband-major
-        int tot = 0;
-        for (int sig = 0; sig < nsig; ++sig) {
-            int nt, tcols, lvl;
-            dw_sig_tiles(geo, sig, nt, tcols, lvl);
-            cstart[sig] = tot;
-            tot += (G * nt + 31) / 32;
-        }
-        cstart[nsig] = tot;
     }
     __syncthreads();
 
+    // this thread's correlation and item range
+    int my_sig = -1, item_begin = 0, item_end = 0;
+    for (int sig = 0; sig < nsig; ++sig)
+        if ((int)threadIdx.x >= tstart[sig] && (int)threadIdx.x < tstart[sig + 1]) my_sig = sig;
+    int lvl = 0, sub_off = 0, per_plane = 1, ncols = 1;
+    if (my_sig >= 0) {
+        lvl = my_sig == 0 ? 0 : (my_sig - 1) / 4 + 1;
+        per_plane = geo.rseg[lvl] * geo.cstr[lvl];
+        ncols = geo.cstr[lvl];
+        const int items = G * per_plane;
+        item_begin = (threadIdx.x - tstart[my_sig]) * per_thread;
+        item_end = min(items, item_begin + per_thread);
+        sub_off = my_sig == 0 ? 0 : ((my_sig - 1) & 3) * geo.rows[lvl] * geo.pitch[lvl];
+    }
+    const int pitch = geo.pitch[lvl];
+    const int y_off = my_sig <= 0 ? geo.off_x : geo.off_y[lvl] + sub_off;
+    const int g_off = my_sig <= 0 ? geo.off_dy : geo.off_g[lvl] + sub_off;
+
+    f2_t acc[KK];
+#pragma unroll
+    for (int i = 0; i < KK; ++i) acc[i] = 0ull;
+    float dysum = 0.f;
+
     const T *x = static_cast<const T *>(a.x);
     const T *dy = static_cast<const T *>(a.dy);
-    T *dx = static_cast<T *>(a.out);
     const size_t HW = (size_t)a.H * a.W;
+    T *stg_x = a.stage ? reinterpret_cast<T *>(reinterpret_cast<char *>(smem) + a.stage_off) : nullptr;
+    T *stg_dy = a.stage ? stg_x + (size_t)G * HW : nullptr;
+    if (stg_x) {  // stage the first group
+        stage_planes<T>(x, stg_x, a.B, a.C, c, nbi * a.groups_per_cta * G, G, HW, a.dv.stage_chunks);
+        stage_planes<T>(dy, stg_dy, a.B, a.C, c, nbi * a.groups_per_cta * G, G, HW, a.dv.stage_chunks);
+        cp_async_commit();
+    }
 
     for (int grp = 0; grp < a.groups_per_cta; ++grp) {
         const int b0 = (nbi * a.groups_per_cta + grp) * G;
         if (b0 >= a.B) break;
-        for (int g = 0; g < G; ++g) {
-            const int b = b0 + g;
-            const bool valid = b < a.B;
-            const size_t off = ((size_t)(valid ? b : 0) * a.C + c) * HW;
-            float *slot = slots + (size_t)g * geo.slot_floats;
-            load_plane<T, K / 2>(x + off, valid, slot + geo.off_x, a.H, a.W, geo.pitch[0]);
-            load_plane<T, K / 2>(dy + off, valid, slot + geo.off_dy, a.H, a.W, geo.pitch[0]);
-        }
-        __syncthreads();
-        for (int l = 1; l <= a.L; ++l) {
-            analysis_level<K / 2>(geo, slots, G, l, geo.off_x, geo.off_y);
-            analysis_level<K / 2>(geo, slots, G, l, geo.off_dy, geo.off_g);
+        if (stg_x) {
+            cp_async_wait_all();
             __syncthreads();
         }
-        if (a.want_dx) conv_levels<K>(geo, slots, G, geo.off_g, wts);
-        dw_phase<K>(geo, slots, G, cstart, nsig, dwacc);
+        // A. both planes -> padded fp32 copies + both Haar pyramids; then the next group streams in
+        analysis_from_global<T, P>(a, geo, x, stg_x, c, b0, slots, geo.off_x, geo.off_y);
+        dysum += analysis_from_global<T, P>(a, geo, dy, stg_dy, c, b0, slots, geo.off_dy, geo.off_g);
         __syncthreads();
-        if (a.want_dx) {
-            output_phase<K, T>(a, geo, slots, G, geo.off_dy, wts, 0.f, dx, c, b0);
+        if (stg_x && grp + 1 < a.groups_per_cta && b0 + G < a.B) {
+            stage_planes<T>(x, stg_x, a.B, a.C, c, b0 + G, G, HW, a.dv.stage_chunks);
+            stage_planes<T>(dy, stg_dy, a.B, a.C, c, b0 + G, G, HW, a.dv.stage_chunks);
+            cp_async_commit();
+        }
+        for (int l = 3; l <= geo.L; l += 2) {
+            analysis_from_shared<P>(a, geo, slots, G, geo.off_y, l);
+            analysis_from_shared<P>(a, geo, slots, G, geo.off_g, l);
             __syncthreads();
         }
+        // C. this thread's share of its correlation
+        for (int it = item_begin; it < item_end; ++it) {
+            const int g = fdiv(a.dv.item_plane[lvl], it), e = it - g * per_plane;
+            const int rs = fdiv(a.dv.item_cols[lvl], e), cs = e - rs * ncols;
+            const float *slot = slots + (size_t)g * geo.slot_floats;
+            const float *yw = slot + y_off + (rs * kRows) * pitch + cs * kCols;
+            const float *gw = slot + g_off + (rs * kRows + P) * pitch + cs * kCols + P;
+            dw_item<K>(yw, gw, pitch, acc);
+        }
+        __syncthreads();
     }
 
-    // one partial per (channel, subband, tap) for this CTA: sum over warps in a fixed order
+    // reduce: per-thread tap sums -> one partial per (subband, tap), in thread order
+    cp_async_wait_all();
+    __syncthreads();
+    float *red = smem;
+#pragma unroll
+    for (int i = 0; i < KK; ++i) red[threadIdx.x * NA + i] = lo2(acc[i]) + hi2(acc[i]);
+    red[threadIdx.x * NA + KK] = dysum;
+    __syncthreads();
     float *part = a.partials + ((size_t)nbi * a.C + c) * nsig * NA;
     for (int i = threadIdx.x; i < nsig * NA; i += blockDim.x) {
         const int sig = i / NA, t = i - sig * NA;
         float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += dwacc[(sig * kWarps + w) * NA + t];
+        if (t < KK) {
+            for (int th = tstart[sig]; th < tstart[sig + 1]; ++th) s += red[th * NA + t];
+        } else if (sig == 0) {
+            for (int th = 0; th < (int)blockDim.x; ++th) s += red[th * NA + KK];
+        }
         part[i] = s;
     }
 }
 
 // Sum the per-CTA partials of each (channel, subband) in order of CTA index and unfold the
-// scales (chain rule through the folding W' = s w, b' = s_b b).  One 64-thread block per
-// (channel, subband); thread t owns tap t (thread K*K: the gradient sum of the base bias).
+// scales.  One 64-thread block per (channel, subband); thread t owns tap t (thread K*K: the
+// gradient sum of the base bias).
 __global__ void __launch_bounds__(64) wtconv_dw_finalize_kernel(const LayerArgs a, float *d_base_w,
                                                                 float *d_base_bias, float *d_base_scale,
                                                                 float *d_wavelet_w, float *d_wavelet_scale) {
@@ -210,21 +207,21 @@ __global__ void __launch_bounds__(64) wtconv_dw_finalize_kernel(const LayerArgs 
 }
 
 template <int K, typename T>
-static cudaError_t launch_bwd_t(const LayerArgs &a, size_t smem, cudaStream_t st) {
-    auto kern = wtconv_bwd_kernel<K, T>;
+static cudaError_t launch_dw_t(const LayerArgs &a, size_t smem, cudaStream_t st) {
+    auto kern = wtconv_dw_kernel<K, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3((unsigned)(a.nb * a.C)), kThreads, smem, st>>>(a);
+    kern<<<dim3((unsigned)(a.nb * a.C)), a.threads, smem, st>>>(a);
     return cudaGetLastError();
 }
 
 template <int K, typename T>
-static int occ_bwd_t(size_t smem) {
-    auto kern = wtconv_bwd_kernel<K, T>;
+static int occ_dw_t(int threads, size_t smem) {
+    auto kern = wtconv_dw_kernel<K, T>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) return 0;
     return n;
 }
 
@@ -242,19 +239,19 @@ static int occ_bwd_t(size_t smem) {
     default: break;                                                                       \
     }
 
-cudaError_t launch_backward(const LayerArgs &a, int dtype, size_t smem, cudaStream_t st) {
-    WTCONV_DISPATCH(a.K, dtype, launch_bwd_t, a, smem, st);
+cudaError_t launch_dw(const LayerArgs &a, int dtype, size_t smem, cudaStream_t st) {
+    WTCONV_DISPATCH(a.K, dtype, launch_dw_t, a, smem, st);
     return cudaErrorInvalidValue;
 }
 
-int occupancy_backward(int dtype, int K, size_t smem) {
-    WTCONV_DISPATCH(K, dtype, occ_bwd_t, smem);
+int occupancy_dw(int dtype, int K, int threads, size_t smem) {
+    WTCONV_DISPATCH(K, dtype, occ_dw_t, threads, smem);
     return 0;
 }
 
 cudaError_t launch_dw_finalize(const LayerArgs &a, float *d_base_w, float *d_base_bias, float *d_base_scale,
                                float *d_wavelet_w, float *d_wavelet_scale, cudaStream_t st) {
-    const int n = a.C * (1 + 4 * a.L);
+    const int n = a.C * n_sig(a.L);
     wtconv_dw_finalize_kernel<<<n, 64, 0, st>>>(a, d_base_w, d_base_bias, d_base_scale, d_wavelet_w,
                                                 d_wavelet_scale);
     return cudaGetLastError();
