@@ -1,23 +1,28 @@
-// On-chip Haar analysis passes: one read of each input plane from global memory builds the
-// padded fp32 copy of the plane and the first Haar levels; later passes build deeper levels from
-// the low band in shared memory.  Each pass computes two levels per item where it can (a 4x4
-// block of the finer low band gives four level-l positions and one level-(l+1) position), so an
-// L-level pyramid needs ceil(L/2) passes (and barriers).
+// On-chip Haar analysis passes: one read of each input plane (from the shared staging area or
+// from global memory) builds the padded fp32 copy of the plane and the first Haar levels; later
+// passes build deeper levels from the low band in shared memory.  Each pass computes two levels
+// per item where it can (a 4x4 block of the finer low band gives four level-l positions and one
+// level-(l+1) position), so an L-level pyramid needs ceil(L/2) passes (and barriers).
+// Levels are written as subband-pair images: pair 0 = (LL, LH), pair 1 = (HL, HH).
 #pragma once
 
 #include "wtconv_device.cuh"
 
 namespace wtconv {
 
-// Level-l subband images of one slot: padded, interior origin (P, P).
-struct LevelView {
-    float *base;  // subband 0
-    int sub;      // floats between subbands
-    int pitch;
-};
+// Write the quad of level l at interior position (i, j) of the slot's pair images.
+__device__ __forceinline__ void put_quad_pairs(float *slot, const Geo &geo, const int *off, int l, int i, int j,
+                                               const Quad &q) {
+    const int P = geo.P;
+    float *p0 = slot + off[l] + 2 * ((i + P) * geo.pitch[l] + j + P);
+    *reinterpret_cast<float2 *>(p0) = make_float2(q.ll, q.lh);
+    *reinterpret_cast<float2 *>(p0 + geo.pimg[l]) = make_float2(q.hl, q.hh);
+}
 
-__device__ __forceinline__ LevelView level_view(float *slot, const Geo &geo, const int *off, int l) {
-    return {slot + off[l], geo.rows[l] * geo.pitch[l], geo.pitch[l]};
+// LL value of level l at interior position (i, j).
+__device__ __forceinline__ float get_ll(const float *slot, const Geo &geo, const int *off, int l, int i, int j) {
+    const int P = geo.P;
+    return slot[off[l] + 2 * ((i + P) * geo.pitch[l] + j + P)];
 }
 
 // Pass 1: read G planes of x (type T; from the shared staging area when `stg` is not null, else
@@ -26,12 +31,13 @@ __device__ __forceinline__ LevelView level_view(float *slot, const Geo &geo, con
 template <typename T, int P>
 __device__ __forceinline__ float analysis_from_global(const LayerArgs &a, const Geo &geo, const T *x, const T *stg,
                                                       int c, int b0, float *slots, int x_off, const int *pyr_off) {
-    const int G = a.G, H = geo.H, W = geo.W;
-    const size_t HW = (size_t)H * W;
+    const int G = a.G, W = geo.W;
+    const size_t HW = (size_t)geo.H * W;
     float sum = 0.f;
+    const FastDiv &dn = a.dv.a_n[1], &dw = a.dv.a_w[1];
+    const int bw = (int)dw.d, n = (int)dn.d;
+    const int xp = geo.pitch[0];
     if (geo.L >= 2) {
-        const FastDiv &dn = a.dv.a_n[1], &dw = a.dv.a_w[1];
-        const int bw = (int)dw.d, n = (int)dn.d;
         for (int it = threadIdx.x; it < G * n; it += blockDim.x) {
             const int g = fdiv(dn, it), e = it - g * n;
             const int bi = fdiv(dw, e), bj = e - bi * bw;
@@ -43,7 +49,7 @@ __device__ __forceinline__ float analysis_from_global(const LayerArgs &a, const 
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     if (a.vec_ld) {
-                        float4 t = Act<T>::ld4(src + r * W);
+                        const float4 t = Act<T>::ld4(src + r * W);
                         v[r][0] = t.x; v[r][1] = t.y; v[r][2] = t.z; v[r][3] = t.w;
                     } else {
 #pragma unroll
@@ -57,15 +63,14 @@ __device__ __forceinline__ float analysis_from_global(const LayerArgs &a, const 
                     for (int cc = 0; cc < 4; ++cc) v[r][cc] = 0.f;
             }
             float *slot = slots + (size_t)g * geo.slot_floats;
-            float *X = slot + x_off + (4 * bi + P) * geo.pitch[0] + 4 * bj + P;
+            float *X = slot + x_off + (4 * bi + P) * xp + 4 * bj + P;
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    X[r * geo.pitch[0] + cc] = v[r][cc];
+                    X[r * xp + cc] = v[r][cc];
                     sum += v[r][cc];
                 }
-            const LevelView l1 = level_view(slot, geo, pyr_off, 1);
             Quad q[2][2];
 #pragma unroll
             for (int a2 = 0; a2 < 2; ++a2)
@@ -73,15 +78,11 @@ __device__ __forceinline__ float analysis_from_global(const LayerArgs &a, const 
                 for (int b2 = 0; b2 < 2; ++b2) {
                     q[a2][b2] = butterfly(v[2 * a2][2 * b2], v[2 * a2][2 * b2 + 1], v[2 * a2 + 1][2 * b2],
                                           v[2 * a2 + 1][2 * b2 + 1]);
-                    put_quad(l1.base, l1.sub, (2 * bi + a2 + P) * l1.pitch + 2 * bj + b2 + P, q[a2][b2]);
+                    put_quad_pairs(slot, geo, pyr_off, 1, 2 * bi + a2, 2 * bj + b2, q[a2][b2]);
                 }
-            const LevelView l2 = level_view(slot, geo, pyr_off, 2);
-            put_quad(l2.base, l2.sub, (bi + P) * l2.pitch + bj + P,
-                     butterfly(q[0][0].ll, q[0][1].ll, q[1][0].ll, q[1][1].ll));
+            put_quad_pairs(slot, geo, pyr_off, 2, bi, bj, butterfly(q[0][0].ll, q[0][1].ll, q[1][0].ll, q[1][1].ll));
         }
     } else {
-        const FastDiv &dn = a.dv.a_n[1], &dw = a.dv.a_w[1];
-        const int bw = (int)dw.d, n = (int)dn.d;
         for (int it = threadIdx.x; it < G * n; it += blockDim.x) {
             const int g = fdiv(dn, it), e = it - g * n;
             const int bi = fdiv(dw, e), bj = e - bi * bw;
@@ -94,11 +95,10 @@ __device__ __forceinline__ float analysis_from_global(const LayerArgs &a, const 
                 v10 = Act<T>::ld(src + W); v11 = Act<T>::ld(src + W + 1);
             }
             float *slot = slots + (size_t)g * geo.slot_floats;
-            float *X = slot + x_off + (2 * bi + P) * geo.pitch[0] + 2 * bj + P;
-            X[0] = v00; X[1] = v01; X[geo.pitch[0]] = v10; X[geo.pitch[0] + 1] = v11;
+            float *X = slot + x_off + (2 * bi + P) * xp + 2 * bj + P;
+            X[0] = v00; X[1] = v01; X[xp] = v10; X[xp + 1] = v11;
             sum += (v00 + v01) + (v10 + v11);
-            const LevelView l1 = level_view(slot, geo, pyr_off, 1);
-            put_quad(l1.base, l1.sub, (bi + P) * l1.pitch + bj + P, butterfly(v00, v01, v10, v11));
+            put_quad_pairs(slot, geo, pyr_off, 1, bi, bj, butterfly(v00, v01, v10, v11));
         }
     }
     return sum;
@@ -108,22 +108,19 @@ __device__ __forceinline__ float analysis_from_global(const LayerArgs &a, const 
 template <int P>
 __device__ __forceinline__ void analysis_from_shared(const LayerArgs &a, const Geo &geo, float *slots, int G,
                                                      const int *pyr_off, int l) {
-    const int two = (l + 1 <= geo.L);
+    const bool two = (l + 1 <= geo.L);
     const FastDiv &dn = a.dv.a_n[l], &dw = a.dv.a_w[l];
     const int bw = (int)dw.d, n = (int)dn.d;
-    if (two) {
-        for (int it = threadIdx.x; it < G * n; it += blockDim.x) {
-            const int g = fdiv(dn, it), e = it - g * n;
-            const int bi = fdiv(dw, e), bj = e - bi * bw;
-            float *slot = slots + (size_t)g * geo.slot_floats;
-            const LevelView s = level_view(slot, geo, pyr_off, l - 1);
-            const float *ll = s.base + (4 * bi + P) * s.pitch + 4 * bj + P;
+    for (int it = threadIdx.x; it < G * n; it += blockDim.x) {
+        const int g = fdiv(dn, it), e = it - g * n;
+        const int bi = fdiv(dw, e), bj = e - bi * bw;
+        float *slot = slots + (size_t)g * geo.slot_floats;
+        if (two) {
             float v[4][4];
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) v[r][cc] = ll[r * s.pitch + cc];
-            const LevelView d1 = level_view(slot, geo, pyr_off, l);
+                for (int cc = 0; cc < 4; ++cc) v[r][cc] = get_ll(slot, geo, pyr_off, l - 1, 4 * bi + r, 4 * bj + cc);
             Quad q[2][2];
 #pragma unroll
             for (int a2 = 0; a2 < 2; ++a2)
@@ -131,22 +128,16 @@ __device__ __forceinline__ void analysis_from_shared(const LayerArgs &a, const G
                 for (int b2 = 0; b2 < 2; ++b2) {
                     q[a2][b2] = butterfly(v[2 * a2][2 * b2], v[2 * a2][2 * b2 + 1], v[2 * a2 + 1][2 * b2],
                                           v[2 * a2 + 1][2 * b2 + 1]);
-                    put_quad(d1.base, d1.sub, (2 * bi + a2 + P) * d1.pitch + 2 * bj + b2 + P, q[a2][b2]);
+                    put_quad_pairs(slot, geo, pyr_off, l, 2 * bi + a2, 2 * bj + b2, q[a2][b2]);
                 }
-            const LevelView d2 = level_view(slot, geo, pyr_off, l + 1);
-            put_quad(d2.base, d2.sub, (bi + P) * d2.pitch + bj + P,
-                     butterfly(q[0][0].ll, q[0][1].ll, q[1][0].ll, q[1][1].ll));
-        }
-    } else {
-        for (int it = threadIdx.x; it < G * n; it += blockDim.x) {
-            const int g = fdiv(dn, it), e = it - g * n;
-            const int bi = fdiv(dw, e), bj = e - bi * bw;
-            float *slot = slots + (size_t)g * geo.slot_floats;
-            const LevelView s = level_view(slot, geo, pyr_off, l - 1);
-            const float *ll = s.base + (2 * bi + P) * s.pitch + 2 * bj + P;
-            const LevelView d1 = level_view(slot, geo, pyr_off, l);
-            put_quad(d1.base, d1.sub, (bi + P) * d1.pitch + bj + P,
-                     butterfly(ll[0], ll[1], ll[s.pitch], ll[s.pitch + 1]));
+            put_quad_pairs(slot, geo, pyr_off, l + 1, bi, bj,
+                           butterfly(q[0][0].ll, q[0][1].ll, q[1][0].ll, q[1][1].ll));
+        } else {
+            const float v00 = get_ll(slot, geo, pyr_off, l - 1, 2 * bi, 2 * bj);
+            const float v01 = get_ll(slot, geo, pyr_off, l - 1, 2 * bi, 2 * bj + 1);
+            const float v10 = get_ll(slot, geo, pyr_off, l - 1, 2 * bi + 1, 2 * bj);
+            const float v11 = get_ll(slot, geo, pyr_off, l - 1, 2 * bi + 1, 2 * bj + 1);
+            put_quad_pairs(slot, geo, pyr_off, l, bi, bj, butterfly(v00, v01, v10, v11));
         }
     }
 }

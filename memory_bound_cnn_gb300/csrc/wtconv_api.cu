@@ -53,10 +53,10 @@ int device_sms() {
     return sms;
 }
 
-// Conv items (kRows x kCols outputs) of one plane over all 1+4L images.
+// Conv items of one plane: the base image plus two subband-pair images per level.
 int items_per_plane(const Geo &g) {
     int n = 0;
-    for (int l = 0; l <= g.L; ++l) n += (l == 0 ? 1 : 4) * g.rseg[l] * g.cstr[l];
+    for (int l = 0; l <= g.L; ++l) n += (l == 0 ? 1 : 2) * g.rseg[l] * g.cstr[l];
     return n;
 }
 
@@ -71,17 +71,17 @@ double fwd_balance(const Geo &g, int G, int T) {
 // single correlation; d is the smallest count for which all correlations fit on T threads).
 double dw_balance(const Geo &g, int G, int T) {
     int tot = 0;
-    const int nsig = 1 + 4 * g.L;
-    for (int s = 0; s < nsig; ++s) {
-        const int l = s == 0 ? 0 : (s - 1) / 4 + 1;
+    const int nimg = 1 + 2 * g.L;
+    for (int s = 0; s < nimg; ++s) {
+        const int l = s == 0 ? 0 : (s - 1) / 2 + 1;
         tot += G * g.rseg[l] * g.cstr[l];
     }
     int d = (tot + T - 1) / T;
     if (d < 1) d = 1;
     for (;; ++d) {
         int need = 0;
-        for (int s = 0; s < nsig; ++s) {
-            const int l = s == 0 ? 0 : (s - 1) / 4 + 1;
+        for (int s = 0; s < nimg; ++s) {
+            const int l = s == 0 ? 0 : (s - 1) / 2 + 1;
             need += (G * g.rseg[l] * g.cstr[l] + d - 1) / d;
         }
         if (need <= T) break;
@@ -126,32 +126,40 @@ typedef size_t (*SmemFn)(const Geo &, int, int, int, int, bool, int *);
 typedef double (*BalFn)(const Geo &, int, int);
 typedef int (*OccFn)(int, int, int, size_t);
 
-// Planes per CTA (G) and CTA size (T): score = item balance x resident warps per SM (capped at
-// 16, enough to hide latency), over G whose shared memory fits; ties go to the smaller G.
+// Planes per CTA (G), CTA size (T) and staging: score = item balance x resident warps per SM
+// (capped at 32), over G whose shared memory fits; ties go to staging, then to the smaller G.
+// Staging through shared memory hides the next planes' load latency but costs shared memory;
+// without it the next planes are only prefetched into L2.  WTCONV_STAGE=0/1 forces the choice.
 bool choose_launch(LayerArgs &a, int dtype, SmemFn smem_fn, BalFn bal_fn, OccFn occ_fn, size_t *smem_out) {
     const int eb = elem_bytes(dtype);
+    const bool can_stage = a.stage != 0;
+    const char *force = getenv("WTCONV_STAGE");
     double best = -1.0;
-    int bestG = 0, bestT = 0;
-    size_t best_smem = 0;
-    for (int T : {256, 128}) {
-        for (int G = 1; G <= a.B && G <= 64; ++G) {
-            const size_t smem = smem_fn(a.geo, G, a.L, a.K, eb, a.stage != 0, nullptr);
-            if (smem + kStaticSmemMargin > (size_t)kMaxSmem) break;
-            const int occ = occ_fn(dtype, a.K, T, smem);
-            if (occ <= 0) continue;
-            int warps = occ * T / 32;
-            if (warps > 16) warps = 16;
-            const double score = bal_fn(a.geo, G, T) * warps;
-            if (score > best + 1e-9) { best = score; bestG = G; bestT = T; best_smem = smem; }
+    int bestG = 0, bestT = 0, bestS = 0;
+    for (int stage : {1, 0}) {
+        if (stage && !can_stage) continue;
+        if (force && force[0] == '0' && stage) continue;
+        if (force && force[0] == '1' && !stage && can_stage) continue;
+        for (int T : {256, 128}) {
+            for (int G = 1; G <= a.B && G <= 64; ++G) {
+                const size_t smem = smem_fn(a.geo, G, a.L, a.K, eb, stage != 0, nullptr);
+                if (smem + kStaticSmemMargin > (size_t)kMaxSmem) break;
+                const int occ = occ_fn(dtype, a.K, T, smem);
+                if (occ <= 0) continue;
+                int warps = occ * T / 32;
+                if (warps > 32) warps = 32;
+                const double score = bal_fn(a.geo, G, T) * warps;
+                if (score > best + 1e-9) { best = score; bestG = G; bestT = T; bestS = stage; }
+            }
         }
     }
     if (bestG == 0) return false;
     a.G = bestG;
     a.threads = bestT;
+    a.stage = bestS;
     int off = 0;
-    *smem_out = smem_fn(a.geo, bestG, a.L, a.K, eb, a.stage != 0, &off);
+    *smem_out = smem_fn(a.geo, bestG, a.L, a.K, eb, bestS != 0, &off);
     a.stage_off = off;
-    (void)best_smem;
     return true;
 }
 

@@ -23,48 +23,53 @@ size_t dw_smem_bytes(const Geo &geo, int G, int L, int K, int elem_bytes, bool s
     size_t slots = (size_t)G * geo.slot_floats * sizeof(float);
     if (stage_off) *stage_off = (int)slots;
     if (stage) slots += 2 * (size_t)G * geo.H * geo.W * elem_bytes;
-    const size_t red = (size_t)kMaxThreads * (K * K + 1) * sizeof(float);
+    const size_t red = (size_t)kMaxThreads * (2 * K * K + 1) * sizeof(float);
     const size_t bytes = slots > red ? slots : red;
     return (bytes + 15) / 16 * 16;
 }
 
+// Correlation images: ci = 0 the base path (dy with the padded x, column-pair items of kRows x
+// kCols pixels, the two halves of each accumulator pair are partial sums of the same tap);
+// ci = 1 + 2(l-1) + pp the level-l subband pair pp (Ghat with Yhat, items of kRows x kColsL
+// positions, the halves are the two subbands).
 template <int K, typename T>
 __global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_dw_kernel(const LayerArgs a) {
-    constexpr int P = K / 2, KK = K * K, NA = KK + 1;
+    constexpr int P = K / 2, KK = K * K, NA = KK + 1, NR = 2 * KK + 1;
+    constexpr int kMaxImg = 1 + 2 * kMaxLevels;
     extern __shared__ __align__(16) float smem[];
     __shared__ Geo geo;
-    __shared__ int tstart[kMaxSig + 1];
+    __shared__ int tstart[kMaxImg + 1];
     __shared__ int per_thread;
     const int c = blockIdx.x % a.C;
     const int nbi = blockIdx.x / a.C;
-    const int G = a.G, nsig = 1 + 4 * a.L;
+    const int G = a.G, nimg = 1 + 2 * a.L, nsig = 1 + 4 * a.L;
     float *slots = smem;
 
     if (threadIdx.x == 0) {
         geo = a.geo;
-        // items per thread d: the smallest d for which every subband's items fit on whole threads
+        // items per thread d: the smallest d for which every image's items fit on whole threads
         int tot = 0;
-        for (int sig = 0; sig < nsig; ++sig) {
-            const int l = sig == 0 ? 0 : (sig - 1) / 4 + 1;
+        for (int ci = 0; ci < nimg; ++ci) {
+            const int l = ci == 0 ? 0 : (ci - 1) / 2 + 1;
             tot += G * a.geo.rseg[l] * a.geo.cstr[l];
         }
         int d = (tot + (int)blockDim.x - 1) / (int)blockDim.x;
         if (d < 1) d = 1;
         for (;; ++d) {
             int need = 0;
-            for (int sig = 0; sig < nsig; ++sig) {
-                const int l = sig == 0 ? 0 : (sig - 1) / 4 + 1;
+            for (int ci = 0; ci < nimg; ++ci) {
+                const int l = ci == 0 ? 0 : (ci - 1) / 2 + 1;
                 need += (G * a.geo.rseg[l] * a.geo.cstr[l] + d - 1) / d;
             }
             if (need <= (int)blockDim.x) break;
         }
         int t0 = 0;
-        for (int sig = 0; sig < nsig; ++sig) {
-            const int l = sig == 0 ? 0 : (sig - 1) / 4 + 1;
-            tstart[sig] = t0;
+        for (int ci = 0; ci < nimg; ++ci) {
+            const int l = ci == 0 ? 0 : (ci - 1) / 2 + 1;
+            tstart[ci] = t0;
             t0 += (G * a.geo.rseg[l] * a.geo.cstr[l] + d - 1) / d;
         }
-        tstart[nsig] = t0;
+        tstart[nimg] = t0;
         per_thread = d;
     }
     {
@@ -74,23 +79,21 @@ __global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_dw_kerne
     }
     __syncthreads();
 
-    // this thread's correlation and item range
-    int my_sig = -1, item_begin = 0, item_end = 0;
-    for (int sig = 0; sig < nsig; ++sig)
-        if ((int)threadIdx.x >= tstart[sig] && (int)threadIdx.x < tstart[sig + 1]) my_sig = sig;
-    int lvl = 0, sub_off = 0, per_plane = 1, ncols = 1;
-    if (my_sig >= 0) {
-        lvl = my_sig == 0 ? 0 : (my_sig - 1) / 4 + 1;
-        per_plane = geo.rseg[lvl] * geo.cstr[lvl];
-        ncols = geo.cstr[lvl];
-        const int items = G * per_plane;
-        item_begin = (threadIdx.x - tstart[my_sig]) * per_thread;
+    // this thread's image and item range
+    int my = -1, item_begin = 0, item_end = 0;
+    for (int ci = 0; ci < nimg; ++ci)
+        if ((int)threadIdx.x >= tstart[ci] && (int)threadIdx.x < tstart[ci + 1]) my = ci;
+    const int lvl = my <= 0 ? 0 : (my - 1) / 2 + 1;
+    const int pp = my <= 0 ? 0 : (my - 1) & 1;
+    if (my >= 0) {
+        const int items = G * geo.rseg[lvl] * geo.cstr[lvl];
+        item_begin = (threadIdx.x - tstart[my]) * per_thread;
         item_end = min(items, item_begin + per_thread);
-        sub_off = my_sig == 0 ? 0 : ((my_sig - 1) & 3) * geo.rows[lvl] * geo.pitch[lvl];
     }
     const int pitch = geo.pitch[lvl];
-    const int y_off = my_sig <= 0 ? geo.off_x : geo.off_y[lvl] + sub_off;
-    const int g_off = my_sig <= 0 ? geo.off_dy : geo.off_g[lvl] + sub_off;
+    const int y_off = lvl == 0 ? geo.off_x : geo.off_y[lvl] + pp * geo.pimg[lvl];
+    const int g_off = lvl == 0 ? geo.off_dy : geo.off_g[lvl] + pp * geo.pimg[lvl];
+    const int ncols = geo.cstr[lvl], per_plane = geo.rseg[lvl] * ncols;
 
     f2_t acc[KK];
 #pragma unroll
@@ -102,16 +105,18 @@ __global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_dw_kerne
     const size_t HW = (size_t)a.H * a.W;
     T *stg_x = a.stage ? reinterpret_cast<T *>(reinterpret_cast<char *>(smem) + a.stage_off) : nullptr;
     T *stg_dy = a.stage ? stg_x + (size_t)G * HW : nullptr;
-    if (stg_x) {  // stage the first group
-        stage_planes<T>(x, stg_x, a.B, a.C, c, nbi * a.groups_per_cta * G, G, HW, a.dv.stage_chunks);
-        stage_planes<T>(dy, stg_dy, a.B, a.C, c, nbi * a.groups_per_cta * G, G, HW, a.dv.stage_chunks);
-        cp_async_commit();
-    }
+    const int first = nbi * a.groups_per_cta * G;
+    int ngrp = 0;
+    while (ngrp < a.groups_per_cta && first + ngrp * G < a.B) ++ngrp;
 
-    for (int grp = 0; grp < a.groups_per_cta; ++grp) {
-        const int b0 = (nbi * a.groups_per_cta + grp) * G;
-        if (b0 >= a.B) break;
+    for (int grp = 0; grp < ngrp; ++grp) {
+        const int b0 = first + grp * G;
         if (stg_x) {
+            if (grp == 0) {
+                stage_planes<T>(x, stg_x, a.B, a.C, c, b0, G, HW, a.dv.stage_chunks);
+                stage_planes<T>(dy, stg_dy, a.B, a.C, c, b0, G, HW, a.dv.stage_chunks);
+                cp_async_commit();
+            }
             cp_async_wait_all();
             __syncthreads();
         }
@@ -119,7 +124,7 @@ __global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_dw_kerne
         analysis_from_global<T, P>(a, geo, x, stg_x, c, b0, slots, geo.off_x, geo.off_y);
         dysum += analysis_from_global<T, P>(a, geo, dy, stg_dy, c, b0, slots, geo.off_dy, geo.off_g);
         __syncthreads();
-        if (stg_x && grp + 1 < a.groups_per_cta && b0 + G < a.B) {
+        if (stg_x && grp + 1 < ngrp) {
             stage_planes<T>(x, stg_x, a.B, a.C, c, b0 + G, G, HW, a.dv.stage_chunks);
             stage_planes<T>(dy, stg_dy, a.B, a.C, c, b0 + G, G, HW, a.dv.stage_chunks);
             cp_async_commit();
@@ -129,14 +134,22 @@ __global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_dw_kerne
             analysis_from_shared<P>(a, geo, slots, G, geo.off_g, l);
             __syncthreads();
         }
+        if (!stg_x && grp + 1 < ngrp && ((HW * sizeof(T)) & 15) == 0 && (int)threadIdx.x < 2 * G) {
+            const int bn = b0 + G + (threadIdx.x >> 1);
+            if (bn < a.B) prefetch_l2(((threadIdx.x & 1) ? dy : x) + ((size_t)bn * a.C + c) * HW, (uint32_t)(HW * sizeof(T)));
+        }
         // C. this thread's share of its correlation
         for (int it = item_begin; it < item_end; ++it) {
             const int g = fdiv(a.dv.item_plane[lvl], it), e = it - g * per_plane;
             const int rs = fdiv(a.dv.item_cols[lvl], e), cs = e - rs * ncols;
             const float *slot = slots + (size_t)g * geo.slot_floats;
-            const float *yw = slot + y_off + (rs * kRows) * pitch + cs * kCols;
-            const float *gw = slot + g_off + (rs * kRows + P) * pitch + cs * kCols + P;
-            dw_item<K>(yw, gw, pitch, acc);
+            if (lvl == 0) {
+                dw_item<K>(slot + y_off + (rs * kRows) * pitch + cs * kCols,
+                           slot + g_off + (rs * kRows + P) * pitch + cs * kCols + P, pitch, acc);
+            } else {
+                dw_item_pair<K>(slot + y_off + 2 * ((rs * kRows) * pitch + cs * kColsL),
+                                slot + g_off + 2 * ((rs * kRows + P) * pitch + cs * kColsL + P), pitch, acc);
+            }
         }
         __syncthreads();
     }
@@ -146,17 +159,27 @@ __global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_dw_kerne
     __syncthreads();
     float *red = smem;
 #pragma unroll
-    for (int i = 0; i < KK; ++i) red[threadIdx.x * NA + i] = lo2(acc[i]) + hi2(acc[i]);
-    red[threadIdx.x * NA + KK] = dysum;
+    for (int i = 0; i < KK; ++i) {
+        const float lo = lo2(acc[i]), hi = hi2(acc[i]);
+        red[threadIdx.x * NR + i] = lvl == 0 ? lo + hi : lo;
+        red[threadIdx.x * NR + KK + i] = lvl == 0 ? 0.f : hi;
+    }
+    red[threadIdx.x * NR + 2 * KK] = dysum;
     __syncthreads();
     float *part = a.partials + ((size_t)nbi * a.C + c) * nsig * NA;
     for (int i = threadIdx.x; i < nsig * NA; i += blockDim.x) {
         const int sig = i / NA, t = i - sig * NA;
         float s = 0.f;
         if (t < KK) {
-            for (int th = tstart[sig]; th < tstart[sig + 1]; ++th) s += red[th * NA + t];
+            int ci = 0, half = 0;
+            if (sig > 0) {
+                const int l = (sig - 1) / 4 + 1, sb = (sig - 1) & 3;
+                ci = 1 + 2 * (l - 1) + (sb >> 1);
+                half = sb & 1;
+            }
+            for (int th = tstart[ci]; th < tstart[ci + 1]; ++th) s += red[th * NR + half * KK + t];
         } else if (sig == 0) {
-            for (int th = 0; th < (int)blockDim.x; ++th) s += red[th * NA + KK];
+            for (int th = 0; th < (int)blockDim.x; ++th) s += red[th * NR + 2 * KK];
         }
         part[i] = s;
     }

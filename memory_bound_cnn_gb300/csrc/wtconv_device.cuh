@@ -161,27 +161,31 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
 
 // ------------------------------------------------------------------------ weight staging
 
-// Stage channel c's kernels into shared memory as duplicated pairs {w, w}, scales folded in:
-//   sig 0            : s_b[c] * w_b[c]
-//   sig 1 + 4(l-1)+s : 4^-l * s_l[4c+s] * w_l[4c+s]      (4^-l: unnormalised pyramid)
+// Stage channel c's kernels into shared memory as packed pairs, scales folded in.  Conv image
+// ci = 0 is the base kernel, stored duplicated {w, w} (it pairs two output columns); conv image
+// ci = 1 + 2(l-1) + pp holds level l's subbands 2pp and 2pp+1 side by side {w_2pp, w_2pp+1}
+// (it pairs the two subbands of a pair image):
+//   base            : s_b[c] * w_b[c]
+//   level l, subband s: 4^-l * s_l[4c+s] * w_l[4c+s]      (4^-l: unnormalised pyramid)
 // `flip` rotates every kernel by 180 degrees (the transposed conv of the input gradient).
 template <int K>
 __device__ __forceinline__ void stage_weights(const LayerArgs &a, int c, f2_t *wts) {
     constexpr int KK = K * K, WP = wpairs(K);
-    const int nsig = 1 + 4 * a.L;
-    for (int it = threadIdx.x; it < nsig * KK; it += blockDim.x) {
-        const int sig = it / KK, t = it - sig * KK;
+    const int nimg = 1 + 2 * a.L;
+    for (int it = threadIdx.x; it < nimg * KK; it += blockDim.x) {
+        const int ci = it / KK, t = it - ci * KK;
         const int tu = t / K, tv = t - tu * K;
         const int src_t = a.flip ? (K - 1 - tu) * K + (K - 1 - tv) : t;
-        float v;
-        if (sig == 0) {
-            v = a.base_scale[c] * a.base_w[(size_t)c * KK + src_t];
+        float v0, v1;
+        if (ci == 0) {
+            v0 = v1 = a.base_scale[c] * a.base_w[(size_t)c * KK + src_t];
         } else {
-            const int l = (sig - 1) / 4 + 1, s = (sig - 1) & 3;
-            const size_t ch = (size_t)(l - 1) * 4 * a.C + 4 * c + s;
-            v = ldexpf(a.wavelet_scale[ch] * a.wavelet_w[ch * KK + src_t], -2 * l);
+            const int l = (ci - 1) / 2 + 1, pp = (ci - 1) & 1;
+            const size_t ch = (size_t)(l - 1) * 4 * a.C + 4 * c + 2 * pp;
+            v0 = ldexpf(a.wavelet_scale[ch] * a.wavelet_w[ch * KK + src_t], -2 * l);
+            v1 = ldexpf(a.wavelet_scale[ch + 1] * a.wavelet_w[(ch + 1) * KK + src_t], -2 * l);
         }
-        wts[sig * WP + t] = pk2(v, v);
+        wts[ci * WP + t] = pk2(v0, v1);
     }
 }
 
@@ -214,13 +218,13 @@ __device__ __forceinline__ void load_row(const float *p, f2_t (&e)[2 * NV], f2_t
     for (int i = 0; i < 2 * NV - 1; ++i) o[i] = shift1(e[i], e[i + 1]);
 }
 
-// One conv item: out[r][c] = sum_{u,v} w[u][v] * in[r + u][c + v] for r < kRows, c < kCols, where
+// One base conv item: out[r][c] = init + sum_{u,v} w[u][v] * in[r + u][c + v] for r < kRows, c < kCols, where
 // `in` points at the padded window origin (= output interior origin) and `out` at the compact
 // output.  Weights w are duplicated pairs in registers.  The tap loop runs v-major so that
 // consecutive FMAs update different accumulators (rows in flight x column pairs).
 template <int K>
 __device__ __forceinline__ void conv_item(const float *__restrict__ in, int pitch, const f2_t (&w)[K * K],
-                                          float *__restrict__ out, int opitch) {
+                                          float *__restrict__ out, int opitch, f2_t init) {
     constexpr int NV = (kCols + K - 1 + 3) / 4;  // 16-byte loads per window row
     f2_t acc[kRows][2];
 #pragma unroll
@@ -236,7 +240,7 @@ __device__ __forceinline__ void conv_item(const float *__restrict__ in, int pitc
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
                         const f2_t xv = (v & 1) ? o[q + v / 2] : e[q + v / 2];
-                        if (u == 0 && v == 0) acc[j][q] = fmul2(w[0], xv);
+                        if (u == 0 && v == 0) acc[j][q] = ffma2(w[0], xv, init);
                         else ffma2_acc(acc[j][q], w[u * K + v], xv);
                     }
                 }
@@ -287,6 +291,87 @@ __device__ __forceinline__ void dw_item(const float *__restrict__ y, const float
                         const f2_t xv = (v & 1) ? o[q + v / 2] : e[q + v / 2];
                         ffma2_acc(acc[u * K + v], gr[j][q], xv);
                     }
+                }
+            }
+        }
+    }
+}
+
+// -------------------------------------------------------- subband-pair items (levels >= 1)
+
+// Window row of a pair image: positions 0 .. 2*NV-1 (each a packed pair of subbands).
+template <int NV>
+__device__ __forceinline__ void load_pair_row(const float *p, f2_t (&x)[2 * NV]) {
+    const ulonglong2 *q = reinterpret_cast<const ulonglong2 *>(p);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const ulonglong2 t = q[i];
+        x[2 * i] = t.x;
+        x[2 * i + 1] = t.y;
+    }
+}
+
+// Conv item on a subband-pair image: for kRows x kColsL output positions,
+// out[r][c] = sum_{u,v} w[u][v] * in[r + u][c + v] elementwise on the two subbands; `in` points at
+// the padded window origin, `out` at the compact pair output; pitches in positions.
+template <int K>
+__device__ __forceinline__ void conv_item_pair(const float *__restrict__ in, int pitch, const f2_t (&w)[K * K],
+                                               float *__restrict__ out, int opitch) {
+    constexpr int NV = (kColsL + K - 1 + 1) / 2;  // 16-byte loads (two positions each) per window row
+    f2_t acc[kRows][kColsL];
+#pragma unroll
+    for (int i = 0; i < kRows + K - 1; ++i) {
+        f2_t x[2 * NV];
+        load_pair_row<NV>(in + 2 * i * pitch, x);
+#pragma unroll
+        for (int v = 0; v < K; ++v) {
+#pragma unroll
+            for (int u = 0; u < K; ++u) {
+                const int j = i - u;
+                if (j >= 0 && j < kRows) {
+#pragma unroll
+                    for (int q = 0; q < kColsL; ++q) {
+                        if (u == 0 && v == 0) acc[j][q] = fmul2(w[0], x[q]);
+                        else ffma2_acc(acc[j][q], w[u * K + v], x[q + v]);
+                    }
+                }
+            }
+        }
+        const int jd = i - (K - 1);
+        if (jd >= 0) {
+            ulonglong2 t;
+            t.x = acc[jd][0];
+            t.y = acc[jd][1];
+            *reinterpret_cast<ulonglong2 *>(out + 2 * jd * opitch) = t;
+        }
+    }
+}
+
+// Weight-gradient item on subband-pair images: acc[u*K+v] = (dW_s0[u][v], dW_s1[u][v]) +=
+// sum over the kRows x kColsL interior tile of G[r][c] * Ypad[r + u][c + v] (elementwise on the
+// pair); `y` points at the padded window origin, `g` at the tile's interior origin (same pitch).
+template <int K>
+__device__ __forceinline__ void dw_item_pair(const float *__restrict__ y, const float *__restrict__ g, int pitch,
+                                             f2_t (&acc)[K * K]) {
+    constexpr int NV = (kColsL + K - 1 + 1) / 2;
+    f2_t gr[kRows][kColsL];
+#pragma unroll
+    for (int i = 0; i < kRows + K - 1; ++i) {
+        if (i < kRows) {
+            const f2_t *gp = reinterpret_cast<const f2_t *>(g + 2 * i * pitch);
+            gr[i][0] = gp[0];
+            gr[i][1] = gp[1];
+        }
+        f2_t x[2 * NV];
+        load_pair_row<NV>(y + 2 * i * pitch, x);
+#pragma unroll
+        for (int q = 0; q < kColsL; ++q) {
+#pragma unroll
+            for (int u = 0; u < K; ++u) {
+                const int j = i - u;
+                if (j >= 0 && j < kRows) {
+#pragma unroll
+                    for (int v = 0; v < K; ++v) ffma2_acc(acc[u * K + v], gr[j][q], x[q + v]);
                 }
             }
         }

@@ -19,20 +19,26 @@ __host__ __device__ constexpr int round_up(int a, int m) { return (a + m - 1) / 
 __host__ __device__ constexpr int ceil_div(int a, int m) { return (a + m - 1) / m; }
 // packed weight pairs per staged kernel (16-byte aligned)
 __host__ __device__ constexpr int wpairs(int K) { return round_up(K * K, 2); }
+constexpr int kColsL = 2;       // output positions (subband pairs) of one level conv item
 
-// Shared-memory geometry of one plane slot, in floats.  Image 0 is the full-resolution plane;
-// image l >= 1 is one subband of Haar level l (H >> l by W >> l).  Every conv input is held
-// zero-padded: interior origin (P, P), P = K/2, extents rounded up to whole conv items
-// (kRows x kCols) plus the K-1 halo, rows 16-byte aligned.  Conv outputs Z (levels >= 1) and the
-// base-conv buffer are compact.
+// Shared-memory geometry of one plane slot, in floats.
+//
+// Level 0 is the full-resolution plane, one fp32 image.  Each Haar level l >= 1 is stored as two
+// "pair images": pair 0 interleaves subbands (LL, LH), pair 1 interleaves (HL, HH), so every
+// position holds two floats that a packed f32x2 instruction consumes together.
+//
+// Conv inputs are zero-padded: interior origin (P, P), P = K/2 (in pixels, or in positions for
+// pair images), extents rounded up to whole conv items plus the K-1 halo, rows 16-byte aligned.
+// Conv outputs (the base buffer, and Z^l as pair images) are compact.
 struct Geo {
     int H, W, L, K, P;
     int h[kMaxLevels + 1], w[kMaxLevels + 1];          // interior size per level
     int rseg[kMaxLevels + 1], cstr[kMaxLevels + 1];    // conv items per image: row segments x col strips
-    int pitch[kMaxLevels + 1], rows[kMaxLevels + 1];   // padded input buffers
-    int zpitch[kMaxLevels + 1], zrows[kMaxLevels + 1]; // compact outputs (level 0: base buffer)
+    int pitch[kMaxLevels + 1], rows[kMaxLevels + 1];   // padded inputs (level 0: floats, l >= 1: positions)
+    int zpitch[kMaxLevels + 1], zrows[kMaxLevels + 1]; // compact outputs (level 0: floats, l >= 1: positions)
     int off_x, off_dy, off_base;
-    int off_y[kMaxLevels + 1], off_g[kMaxLevels + 1], off_z[kMaxLevels + 1];
+    int off_y[kMaxLevels + 1], off_g[kMaxLevels + 1], off_z[kMaxLevels + 1];  // pair 0 of level l
+    int pimg[kMaxLevels + 1], zimg[kMaxLevels + 1];    // floats per padded / compact pair image
     int slot_floats;
 };
 
@@ -41,30 +47,37 @@ struct Geo {
 __host__ __device__ inline Geo make_geo(int H, int W, int L, int K, int kind) {
     Geo g = {};
     g.H = H; g.W = W; g.L = L; g.K = K; g.P = K / 2;
-    const int halo_c = round_up(K - 1, 4);
     for (int l = 0; l <= L; ++l) {
         g.h[l] = H >> l;
         g.w[l] = W >> l;
         g.rseg[l] = ceil_div(g.h[l], kRows);
-        g.cstr[l] = ceil_div(g.w[l], kCols);
         g.rows[l] = g.rseg[l] * kRows + K - 1;
-        g.pitch[l] = g.cstr[l] * kCols + halo_c;
         g.zrows[l] = g.rseg[l] * kRows;
-        g.zpitch[l] = l == 0 ? round_up(W, 8) : g.cstr[l] * kCols;
+        if (l == 0) {
+            g.cstr[l] = ceil_div(g.w[l], kCols);
+            g.pitch[l] = g.cstr[l] * kCols + round_up(K - 1, 4);
+            g.zpitch[l] = round_up(W, 8);
+        } else {
+            g.cstr[l] = ceil_div(g.w[l], kColsL);
+            g.pitch[l] = g.cstr[l] * kColsL + round_up(K - 1, 2);
+            g.zpitch[l] = round_up(g.w[l], 4);
+            g.pimg[l] = 2 * g.rows[l] * g.pitch[l];
+            g.zimg[l] = 2 * g.zrows[l] * g.zpitch[l];
+        }
     }
     int off = 0;
     g.off_x = off; off += g.rows[0] * g.pitch[0];
     g.off_dy = -1;
     g.off_base = -1;
     if (kind == 1) { g.off_dy = off; off += g.rows[0] * g.pitch[0]; }
-    for (int l = 1; l <= L; ++l) { g.off_y[l] = off; off += 4 * g.rows[l] * g.pitch[l]; }
+    for (int l = 1; l <= L; ++l) { g.off_y[l] = off; off += 2 * g.pimg[l]; }
     for (int l = 1; l <= L; ++l) {
         g.off_g[l] = -1;
-        if (kind == 1) { g.off_g[l] = off; off += 4 * g.rows[l] * g.pitch[l]; }
+        if (kind == 1) { g.off_g[l] = off; off += 2 * g.pimg[l]; }
     }
     for (int l = 1; l <= L; ++l) {
         g.off_z[l] = -1;
-        if (kind == 0) { g.off_z[l] = off; off += 4 * g.zrows[l] * g.zpitch[l]; }
+        if (kind == 0) { g.off_z[l] = off; off += 2 * g.zimg[l]; }
     }
     if (kind == 0) { g.off_base = off; off += g.zrows[0] * g.zpitch[0]; }
     g.slot_floats = round_up(off, 4);
