@@ -82,6 +82,10 @@ int wtconv_version(void);
 const char *wtconv_strerror(int status);
 
 /* Bytes of device workspace `op` needs for this shape on the current device (0 if none).
+ * FORWARD and BACKWARD_INPUT need, for L >= 2, one fp32 per level-1 position
+ * (B*C*(H/2)*(W/2)*4 bytes, rounded up to 256): the contribution of the Haar levels >= 2, which a
+ * first kernel computes per plane and the second kernel adds to every output pixel.  The weight
+ * gradients need one fp32 partial per (CTA, channel, subband, tap); BACKWARD needs both.
  * Returns 0 for an invalid shape as well; the compute call then reports the error. */
 size_t wtconv_workspace_size(int op, int B, int C, int H, int W, int L, int k, int dtype);
 

@@ -44,6 +44,7 @@ struct Plan {
     LayerArgs a{};
     size_t smem = 0;
     size_t workspace = 0;
+    int dw_pyramid = 0;  // weight gradient: 1 = pyramids in the workspace + tiled correlations
 };
 
 int device_sms() {
@@ -163,7 +164,7 @@ bool choose_launch(LayerArgs &a, int dtype, SmemFn smem_fn, BalFn bal_fn, OccFn 
     return true;
 }
 
-// Forward and input-gradient kernel.
+// Whole-plane forward / input-gradient kernel; UNSUPPORTED when a plane's pyramid does not fit.
 Plan plan_forward_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
     Plan p;
     LayerArgs &a = p.a;
@@ -198,7 +199,15 @@ Plan plan_dw_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
     const int sms = device_sms();
     if (sms <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
     if (!choose_launch(a, dtype, dw_smem_bytes, dw_balance, occupancy_dw, &p.smem)) {
-        p.status = WTCONV_ERR_UNSUPPORTED;
+        // planes too large for shared memory: pyramids in the workspace, tiled correlations
+        p.dw_pyramid = 1;
+        const long long units0 = (long long)B * ((H + 15) / 16) * ((W + 63) / 64);
+        long long nb = (8LL * sms + C - 1) / C;
+        if (nb > units0) nb = units0;
+        if (nb < 1) nb = 1;
+        a.nb = (int)nb;
+        p.workspace = dw_pyramid_bytes(B, C, H, W, L) +
+                      ((size_t)a.nb * C * (1 + 4 * L) * (k * k + 1) * sizeof(float) + 255) / 256 * 256;
         return p;
     }
     set_divs(a, dtype);
@@ -212,6 +221,121 @@ Plan plan_dw_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
     a.nb = (ngroups + a.groups_per_cta - 1) / a.groups_per_cta;
     p.workspace = (size_t)a.nb * C * (1 + 4 * L) * (k * k + 1) * sizeof(float);
     return p;
+}
+
+// Deep kernel (levels >= 2; only when L >= 2): like the forward planner, on a levels>=2 slot.
+double deep_balance(const Geo &g, int G, int T) {
+    int items = 0;
+    for (int l = 2; l <= g.L; ++l) items += 2 * g.rseg[l] * g.cstr[l];
+    items *= G;
+    const int rounds = (items + T - 1) / T;
+    return rounds > 0 ? (double)items / ((double)rounds * T) : 0.0;
+}
+
+Plan plan_deep_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
+    Plan p;
+    LayerArgs &a = p.a;
+    a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
+    a.geo = make_geo(H, W, L, k, 2);
+    set_io_modes(a, dtype);
+    const int sms = device_sms();
+    if (sms <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
+    if (!choose_launch(a, dtype, deep_smem_bytes, deep_balance, occupancy_deep, &p.smem)) {
+        p.status = WTCONV_ERR_UNSUPPORTED;
+        return p;
+    }
+    set_divs(a, dtype);
+    // pass 1 reads 4 x 4 pixel blocks; the output is D at level-1 resolution in segments of 8
+    a.dv.a_w[1] = make_fastdiv(W >> 2);
+    a.dv.a_n[1] = make_fastdiv((H >> 2) * (W >> 2));
+    const int nws = ((W >> 1) + 7) / 8;
+    a.dv.out_w = make_fastdiv(nws);
+    a.dv.out_n = make_fastdiv((H >> 1) * nws);
+    const int occ = occupancy_deep(dtype, k, a.threads, p.smem);
+    const int ngroups = (B + a.G - 1) / a.G;
+    const long long target = 4LL * sms * occ;
+    long long nb = (target + C - 1) / C;
+    if (nb < 1) nb = 1;
+    if (nb > ngroups) nb = ngroups;
+    a.groups_per_cta = (int)((ngroups + nb - 1) / nb);
+    a.nb = (ngroups + a.groups_per_cta - 1) / a.groups_per_cta;
+    return p;
+}
+
+struct SPlan {
+    int status = WTCONV_OK;
+    ShallowArgs a{};
+    size_t smem = 0;
+};
+
+// Shallow kernel tiles: full-width tiles up to 64 columns, at most 32 fused 8x4 items per tile
+// (one per lane); small planes are packed G to a warp.
+SPlan plan_shallow_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
+    SPlan p;
+    ShallowArgs &a = p.a;
+    a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
+    a.vec_ld = (W % 4) == 0;
+    a.st_mode = (W % 4) == 0 ? 1 : 0;
+    const int W4 = round_up(W, 4);
+    const int TW = W4 <= 64 ? W4 : 64;
+    const int items_c = TW / kCols;
+    int rows_of_items = 32 / items_c;
+    if (rows_of_items < 1) rows_of_items = 1;
+    int TH = kRows * rows_of_items;
+    if (TH > round_up(H, kRows)) TH = round_up(H, kRows);
+    int G = 1;
+    if (TH >= H && TW >= W) {
+        G = 32 / (items_c * (TH / kRows));
+        if (G < 1) G = 1;
+        if (G > B) G = B;
+    }
+    const int eb = elem_bytes(dtype);
+    const int P = k / 2;
+    // staged tiles move 8-byte chunks: each must lie wholly inside or outside the plane, and its
+    // shared destination must be 8-byte aligned (an fp32 tile is staged straight into the X
+    // layout, whose interior starts pad_l = (4 - P % 4) % 4 floats in: even only for even P)
+    const int E = 8 / eb;
+    const int pad_l = (4 - P % 4) % 4;
+    const int dst_off_bytes = eb == 4 ? pad_l * 4 : 0;
+    a.stage = ((2 * P) % E == 0 && W % E == 0 && dst_off_bytes % 8 == 0 && (L < 2 || W % 4 == 0)) ? 1 : 0;
+    const bool convert = eb != 4;
+    a.sg = make_shallow_geo(H, W, k, TH, TW, G, eb);
+    p.smem = shallow_smem_bytes(a.sg, k, a.stage != 0, convert);
+    while (G > 1 && p.smem + kStaticSmemMargin > (size_t)kMaxSmem) {
+        --G;
+        a.sg = make_shallow_geo(H, W, k, TH, TW, G, eb);
+        p.smem = shallow_smem_bytes(a.sg, k, a.stage != 0, convert);
+    }
+    if (p.smem + kStaticSmemMargin > (size_t)kMaxSmem) { p.status = WTCONV_ERR_UNSUPPORTED; return p; }
+    const int sms = device_sms();
+    const int occ = occupancy_shallow(dtype, k, p.smem);
+    if (sms <= 0 || occ <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
+    const int tiles = a.sg.tiles_r * a.sg.tiles_c;
+    a.units = ((B + G - 1) / G) * tiles;
+    const long long target = 4LL * sms * occ;  // about four waves of resident CTAs
+    long long nb = (target + C - 1) / C;
+    if (nb < 1) nb = 1;
+    if (nb > a.units) nb = a.units;
+    a.units_per_cta = (int)((a.units + nb - 1) / nb);
+    a.nb = (a.units + a.units_per_cta - 1) / a.units_per_cta;
+    const int nchunk = (TW + 4 * P) / 4;
+    a.tiles = make_fastdiv(tiles);
+    a.tiles_c = make_fastdiv(a.sg.tiles_c);
+    a.xchunk = make_fastdiv(nchunk);
+    a.xload = make_fastdiv(a.sg.xrows * nchunk);
+    a.ycols = make_fastdiv(a.sg.ycols);
+    a.ypos = make_fastdiv(a.sg.yrows * a.sg.ycols);
+    a.rchunk_row = make_fastdiv((TW + 4 * P) / E);
+    a.rchunks = make_fastdiv(a.sg.xrows * ((TW + 4 * P) / E));
+    a.dchunk_row = make_fastdiv(TW / 4);
+    a.dchunks = make_fastdiv((TH / 2) * (TW / 4));
+    return p;
+}
+
+// Bytes of the deep contribution (level-1 resolution, fp32, 16-byte rounded); 0 when L == 1.
+size_t deep_bytes(int B, int C, int H, int W, int L) {
+    if (L < 2) return 0;
+    return ((size_t)B * C * (H >> 1) * (W >> 1) * sizeof(float) + 255) / 256 * 256;
 }
 
 // Plans depend only on the shape, dtype and device; they are computed once and reused (the
@@ -233,12 +357,14 @@ Plan cached_plan(int kind, int B, int C, int H, int W, int L, int k, int dtype) 
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    Plan p = kind == 0 ? plan_forward_uncached(B, C, H, W, L, k, dtype) : plan_dw_uncached(B, C, H, W, L, k, dtype);
+    Plan p = kind == 0   ? plan_forward_uncached(B, C, H, W, L, k, dtype)
+             : kind == 1 ? plan_dw_uncached(B, C, H, W, L, k, dtype)
+                         : plan_deep_uncached(B, C, H, W, L, k, dtype);
     const char *verbose = getenv("WTCONV_VERBOSE");
     if (verbose && verbose[0] == '1')
         fprintf(stderr, "wtconv plan %s B=%d C=%d H=%d W=%d L=%d k=%d dtype=%d: status %d G=%d threads=%d nb=%d "
                         "groups/cta=%d smem=%zu stage=%d workspace=%zu\n",
-                kind == 0 ? "fwd" : "dw", B, C, H, W, L, k, dtype, p.status, p.a.G, p.a.threads, p.a.nb,
+                kind == 0 ? "fwd" : kind == 1 ? "dw" : "deep", B, C, H, W, L, k, dtype, p.status, p.a.G, p.a.threads, p.a.nb,
                 p.a.groups_per_cta, p.smem, p.a.stage, p.workspace);
     if (p.status == WTCONV_OK) {
         std::lock_guard<std::mutex> lock(mu);
@@ -249,6 +375,39 @@ Plan cached_plan(int kind, int B, int C, int H, int W, int L, int k, int dtype) 
 
 Plan plan_forward(int B, int C, int H, int W, int L, int k, int dtype) {
     return cached_plan(0, B, C, H, W, L, k, dtype);
+}
+
+Plan plan_deep(int B, int C, int H, int W, int L, int k, int dtype) {
+    return cached_plan(2, B, C, H, W, L, k, dtype);
+}
+
+SPlan plan_shallow(int B, int C, int H, int W, int L, int k, int dtype) {
+    static std::mutex mu;
+    static std::map<PlanKey, SPlan> cache;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        SPlan p;
+        p.status = WTCONV_ERR_CUDA;
+        return p;
+    }
+    const PlanKey key(3, B, C, H, W, L, k, dtype, dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    SPlan p = plan_shallow_uncached(B, C, H, W, L, k, dtype);
+    const char *verbose = getenv("WTCONV_VERBOSE");
+    if (verbose && verbose[0] == '1')
+        fprintf(stderr, "wtconv plan shallow B=%d C=%d H=%d W=%d L=%d k=%d dtype=%d: status %d TH=%d TW=%d G=%d "
+                        "units=%d units/cta=%d nb=%d smem=%zu\n",
+                B, C, H, W, L, k, dtype, p.status, p.a.sg.TH, p.a.sg.TW, p.a.sg.G, p.a.units, p.a.units_per_cta,
+                p.a.nb, p.smem);
+    if (p.status == WTCONV_OK) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache.emplace(key, p);
+    }
+    return p;
 }
 
 Plan plan_dw(int B, int C, int H, int W, int L, int k, int dtype) {
@@ -289,47 +448,87 @@ const char *wtconv_strerror(int status) {
 
 size_t wtconv_workspace_size(int op, int B, int C, int H, int W, int L, int k, int dtype) {
     if (validate_shape(B, C, H, W, L, k, dtype) != WTCONV_OK) return 0;
+    size_t bytes = 0;
+    if (op == WTCONV_OP_FORWARD || op == WTCONV_OP_BACKWARD_INPUT || op == WTCONV_OP_BACKWARD)
+        bytes += deep_bytes(B, C, H, W, L);
     if (op == WTCONV_OP_BACKWARD_WEIGHTS || op == WTCONV_OP_BACKWARD) {
         Plan p = plan_dw(B, C, H, W, L, k, dtype);
-        return p.status == WTCONV_OK ? p.workspace : 0;
+        if (p.status != WTCONV_OK) return 0;
+        bytes += p.workspace;
     }
-    return 0;
+    return bytes;
+}
+
+// The layer's linear operator on `src` (x -> y, or dy -> dx with rotated kernels and no bias):
+// deep kernel (levels >= 2 -> contribution at level-1 resolution, in the workspace), then the
+// shallow kernel (base conv + level 1 + synthesis, final outputs).
+static int run_operator(int B, int C, int H, int W, int L, int k, int dtype, const void *src, const float *base_w,
+                        const float *base_bias, const float *base_scale, const float *wavelet_w,
+                        const float *wavelet_scale, void *dst, bool flip, void *workspace, size_t workspace_bytes,
+                        cudaStream_t s) {
+    // planes whose whole pyramid fits in shared memory: one kernel, no workspace
+    Plan pf = plan_forward(B, C, H, W, L, k, dtype);
+    if (pf.status == WTCONV_OK) {
+        pf.a.x = src;
+        pf.a.out = dst;
+        set_params(pf.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
+        pf.a.flip = flip ? 1 : 0;
+        pf.a.with_bias = flip ? 0 : 1;
+        return cuda_status(launch_forward(pf.a, dtype, pf.smem, s));
+    }
+    if (pf.status != WTCONV_ERR_UNSUPPORTED) return pf.status;
+    const size_t dbytes = deep_bytes(B, C, H, W, L);
+    Plan pd;
+    if (L >= 2) {
+        pd = plan_deep(B, C, H, W, L, k, dtype);
+        if (pd.status != WTCONV_OK) return pd.status;
+    }
+    SPlan ps = plan_shallow(B, C, H, W, L, k, dtype);
+    if (ps.status != WTCONV_OK) return ps.status;
+    if (workspace_bytes < dbytes || (dbytes > 0 && !aligned16(workspace))) return WTCONV_ERR_WORKSPACE;
+    float *deep = L >= 2 ? static_cast<float *>(workspace) : nullptr;
+    if (L >= 2) {
+        pd.a.x = src;
+        set_params(pd.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
+        pd.a.flip = flip ? 1 : 0;
+        pd.a.with_bias = 0;
+        if (launch_deep(pd.a, deep, dtype, pd.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+    }
+    ShallowArgs &a = ps.a;
+    a.x = src;
+    a.deep = deep;
+    a.out = dst;
+    a.base_w = base_w; a.base_bias = base_bias; a.base_scale = base_scale;
+    a.wavelet_w = wavelet_w; a.wavelet_scale = wavelet_scale;
+    a.flip = flip ? 1 : 0;
+    a.with_bias = flip ? 0 : 1;
+    return cuda_status(launch_shallow(a, dtype, ps.smem, s));
 }
 
 int wtconv_forward(int B, int C, int H, int W, int L, int k, int dtype, const void *x, const float *base_w,
                    const float *base_bias, const float *base_scale, const float *wavelet_w,
                    const float *wavelet_scale, void *y, void *workspace, size_t workspace_bytes,
                    wtconv_stream_t stream) {
-    (void)workspace; (void)workspace_bytes;
     int st = validate_shape(B, C, H, W, L, k, dtype);
     if (st != WTCONV_OK) return st;
     if (!aligned16(x) || !aligned16(y) || !params_ok(base_w, base_bias, base_scale, wavelet_w, wavelet_scale))
         return WTCONV_ERR_INVALID_ARG;
     if (fault_injected()) return WTCONV_ERR_INJECTED;
-    Plan p = plan_forward(B, C, H, W, L, k, dtype);
-    if (p.status != WTCONV_OK) return p.status;
-    p.a.x = x; p.a.out = y;
-    set_params(p.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
-    p.a.flip = 0; p.a.with_bias = 1;
-    return cuda_status(launch_forward(p.a, dtype, p.smem, reinterpret_cast<cudaStream_t>(stream)));
+    return run_operator(B, C, H, W, L, k, dtype, x, base_w, base_bias, base_scale, wavelet_w, wavelet_scale, y,
+                        false, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int wtconv_backward_input(int B, int C, int H, int W, int L, int k, int dtype, const float *base_w,
                           const float *base_bias, const float *base_scale, const float *wavelet_w,
                           const float *wavelet_scale, const void *dy, void *dx, void *workspace,
                           size_t workspace_bytes, wtconv_stream_t stream) {
-    (void)workspace; (void)workspace_bytes;
     int st = validate_shape(B, C, H, W, L, k, dtype);
     if (st != WTCONV_OK) return st;
     if (!aligned16(dy) || !aligned16(dx) || !params_ok(base_w, base_bias, base_scale, wavelet_w, wavelet_scale))
         return WTCONV_ERR_INVALID_ARG;
     if (fault_injected()) return WTCONV_ERR_INJECTED;
-    Plan p = plan_forward(B, C, H, W, L, k, dtype);
-    if (p.status != WTCONV_OK) return p.status;
-    p.a.x = dy; p.a.out = dx;
-    set_params(p.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
-    p.a.flip = 1; p.a.with_bias = 0;
-    return cuda_status(launch_forward(p.a, dtype, p.smem, reinterpret_cast<cudaStream_t>(stream)));
+    return run_operator(B, C, H, W, L, k, dtype, dy, base_w, base_bias, base_scale, wavelet_w, wavelet_scale, dx,
+                        true, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 static int backward_common(bool want_dx, int B, int C, int H, int W, int L, int k, int dtype, const void *x,
@@ -346,23 +545,36 @@ static int backward_common(bool want_dx, int B, int C, int H, int W, int L, int 
     if (fault_injected()) return WTCONV_ERR_INJECTED;
     Plan pw = plan_dw(B, C, H, W, L, k, dtype);
     if (pw.status != WTCONV_OK) return pw.status;
-    Plan pf;
-    if (want_dx) {
-        pf = plan_forward(B, C, H, W, L, k, dtype);
-        if (pf.status != WTCONV_OK) return pf.status;
-    }
-    if (workspace_bytes < pw.workspace || (pw.workspace > 0 && !aligned16(workspace))) return WTCONV_ERR_WORKSPACE;
+    const size_t dbytes = want_dx ? deep_bytes(B, C, H, W, L) : 0;
+    if (workspace_bytes < dbytes + pw.workspace || (dbytes + pw.workspace > 0 && !aligned16(workspace)))
+        return WTCONV_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (want_dx) {
-        pf.a.x = dy; pf.a.out = dx;
-        set_params(pf.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
-        pf.a.flip = 1; pf.a.with_bias = 0;
-        if (launch_forward(pf.a, dtype, pf.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+        st = run_operator(B, C, H, W, L, k, dtype, dy, base_w, base_bias, base_scale, wavelet_w, wavelet_scale, dx,
+                          true, workspace, dbytes, s);
+        if (st != WTCONV_OK) return st;
     }
     pw.a.x = x; pw.a.dy = dy;
     set_params(pw.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
-    pw.a.partials = static_cast<float *>(workspace);
-    if (launch_dw(pw.a, dtype, pw.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+    char *wsp = static_cast<char *>(workspace) + dbytes;
+    if (pw.dw_pyramid) {
+        DwPyramidArgs d{};
+        d.B = B; d.C = C; d.H = H; d.W = W; d.L = L; d.K = k;
+        d.nb = pw.a.nb;
+        d.x = x; d.dy = dy;
+        for (int l = 1; l <= L; ++l) {
+            const size_t lb = ((size_t)B * C * (H >> l) * (W >> l) * sizeof(float4) + 255) / 256 * 256;
+            d.pyr_x[l] = reinterpret_cast<float4 *>(wsp);
+            d.pyr_dy[l] = reinterpret_cast<float4 *>(wsp + lb);
+            wsp += 2 * lb;
+        }
+        d.partials = reinterpret_cast<float *>(wsp);
+        pw.a.partials = d.partials;
+        if (launch_dw_pyramid(d, dtype, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+    } else {
+        pw.a.partials = reinterpret_cast<float *>(wsp);
+        if (launch_dw(pw.a, dtype, pw.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+    }
     return cuda_status(launch_dw_finalize(pw.a, d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale, s));
 }
 

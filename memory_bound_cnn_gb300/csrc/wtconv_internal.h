@@ -44,6 +44,7 @@ struct Geo {
 
 // kind 0: forward / input-gradient slot (x, pyramid, conv outputs, base buffer)
 // kind 1: weight-gradient slot (x, dy and both pyramids)
+// kind 2: deep slot (levels >= 2 only: pyramid and conv outputs; no full-resolution plane)
 __host__ __device__ inline Geo make_geo(int H, int W, int L, int K, int kind) {
     Geo g = {};
     g.H = H; g.W = W; g.L = L; g.K = K; g.P = K / 2;
@@ -66,18 +67,23 @@ __host__ __device__ inline Geo make_geo(int H, int W, int L, int K, int kind) {
         }
     }
     int off = 0;
-    g.off_x = off; off += g.rows[0] * g.pitch[0];
+    const int l0 = kind == 2 ? 2 : 1;  // first stored level
+    g.off_x = -1;
+    if (kind != 2) { g.off_x = off; off += g.rows[0] * g.pitch[0]; }
     g.off_dy = -1;
     g.off_base = -1;
     if (kind == 1) { g.off_dy = off; off += g.rows[0] * g.pitch[0]; }
-    for (int l = 1; l <= L; ++l) { g.off_y[l] = off; off += 2 * g.pimg[l]; }
+    for (int l = 1; l <= L; ++l) {
+        g.off_y[l] = -1;
+        if (l >= l0) { g.off_y[l] = off; off += 2 * g.pimg[l]; }
+    }
     for (int l = 1; l <= L; ++l) {
         g.off_g[l] = -1;
         if (kind == 1) { g.off_g[l] = off; off += 2 * g.pimg[l]; }
     }
     for (int l = 1; l <= L; ++l) {
         g.off_z[l] = -1;
-        if (kind == 0) { g.off_z[l] = off; off += 2 * g.zimg[l]; }
+        if ((kind == 0 && l >= 1) || (kind == 2 && l >= 2)) { g.off_z[l] = off; off += 2 * g.zimg[l]; }
     }
     if (kind == 0) { g.off_base = off; off += g.zrows[0] * g.zpitch[0]; }
     g.slot_floats = round_up(off, 4);
@@ -130,16 +136,109 @@ struct LayerArgs {
 
 // Dynamic shared memory of the kernels for G planes per slot group; *stage_off receives the
 // byte offset of the staging area (staging holds n_in * G raw planes of elem_bytes elements).
+// Geometry of one shallow tile slot: the zero-padded fp32 input tile X (the output tile plus a
+// halo of 2P pixels: P for the base conv, P level-1 coefficients for the level-1 conv) and the
+// tile's Haar level 1 as two subband-pair images (LL|LH, HL|HH) with a halo of P coefficients.
+struct ShallowGeo {
+    int TH, TW;            // output tile (TH % 8 == 0, TW % 4 == 0)
+    int G;                 // planes per slot group (whole-plane tiles of small planes), else 1
+    int tiles_r, tiles_c;  // tiles per plane
+    int pad_l;             // left padding of X so every base window starts 16-byte aligned
+    int xrows, xpitch;     // X tile (floats)
+    int yrows, ypitch;     // level-1 pair images (positions)
+    int ycols;             // level-1 positions computed per row (TW/2 + 2P)
+    int off_y, yimg;       // start of pair image 0 (floats from the slot start); floats per image
+    int slot_floats;
+    int items_r, items_c;  // fused output items per tile (8 x 4 pixels each)
+    // staged path: raw input tiles (type T, two buffers) and deep-contribution tiles (fp32, two
+    // buffers) arrive by cp.async while the previous tile computes
+    int rpitch, roff;      // raw tile pitch and interior column offset (elements)
+    int raw_bytes;         // one raw tile buffer (all G planes), 16-byte rounded
+    int dtile;             // floats of one deep tile per plane: (TH/2) x (TW/2)
+};
+
+__host__ __device__ inline ShallowGeo make_shallow_geo(int H, int W, int K, int TH, int TW, int G, int elem_bytes) {
+    ShallowGeo s = {};
+    const int P = K / 2;
+    const int NV = (kCols + K - 1 + 3) / 4, NVP = (kColsL + K - 1 + 1) / 2;
+    s.TH = TH; s.TW = TW; s.G = G;
+    s.tiles_r = ceil_div(H, TH);
+    s.tiles_c = ceil_div(W, TW);
+    s.pad_l = (4 - P % 4) % 4;
+    s.xrows = TH + 4 * P;
+    const int xneed = (TW + 4 * P) > (TW - 4 + P + 4 * NV) ? (TW + 4 * P) : (TW - 4 + P + 4 * NV);
+    s.xpitch = round_up(xneed + s.pad_l, 4);
+    s.yrows = TH / 2 + 2 * P;
+    s.ycols = TW / 2 + 2 * P;
+    const int yneed = s.ycols > (TW / 2 - 3 + 2 * NVP) ? s.ycols : (TW / 2 - 3 + 2 * NVP);
+    s.ypitch = round_up(yneed, 2);
+    s.off_y = round_up(s.xrows * s.xpitch, 4);
+    s.yimg = 2 * s.yrows * s.ypitch;
+    s.slot_floats = round_up(s.off_y + 2 * s.yimg, 4);
+    s.items_r = TH / kRows;
+    s.items_c = TW / kCols;
+    // fp32 input: the raw tile has the X layout itself; narrower types are converted into X
+    s.rpitch = elem_bytes == 4 ? s.xpitch : round_up(TW + 4 * P, 8);
+    s.roff = elem_bytes == 4 ? s.pad_l : 0;
+    s.raw_bytes = round_up(G * s.xrows * s.rpitch * elem_bytes, 16);
+    s.dtile = (TH / 2) * (TW / 2);
+    return s;
+}
+
+struct ShallowArgs {
+    int B, C, H, W, L, K;
+    int units;            // work units per channel: slot groups x tiles
+    int units_per_cta;    // contiguous units each CTA walks through
+    int nb;               // CTAs per channel; grid = nb * C
+    int vec_ld, st_mode;
+    int stage;            // 1: cp.async double-buffered tiles (8-byte chunks that never straddle the plane edge)
+    const void *x;        // forward: x; input gradient: dy
+    const float *deep;    // deep contribution at level-1 resolution [B][C][H/2][W/2] (L >= 2)
+    void *out;            // y or dx
+    const float *base_w, *base_bias, *base_scale, *wavelet_w, *wavelet_scale;
+    int flip, with_bias;
+    ShallowGeo sg;
+    // units per slot group (tiles), tile columns, X-tile 4-pixel chunks per plane and per row,
+    // level-1 positions per plane and per row
+    FastDiv tiles, tiles_c, xload, xchunk, ypos, ycols;
+    FastDiv rchunks, rchunk_row;    // staged raw tile: 8-byte chunks per plane / per row
+    FastDiv dchunks, dchunk_row;    // staged deep tile: 8-byte chunks per plane / per row
+};
+
+size_t shallow_smem_bytes(const ShallowGeo &sg, int K, bool stage, bool convert);
+cudaError_t launch_shallow(const ShallowArgs &a, int dtype, size_t smem, cudaStream_t st);
+int occupancy_shallow(int dtype, int K, size_t smem);
+
+// Deep kernel: levels >= 2 of every plane and their closed-form contribution at level-1 resolution.
+size_t deep_smem_bytes(const Geo &geo, int G, int L, int K, int elem_bytes, bool stage, int *stage_off);
+cudaError_t launch_deep(const LayerArgs &a, float *deep_out, int dtype, size_t smem, cudaStream_t st);
+int occupancy_deep(int dtype, int K, int threads, size_t smem);
+
+// Whole-plane kernel (planes whose pyramid fits in shared memory): forward / input gradient in one pass.
 size_t fwd_smem_bytes(const Geo &geo, int G, int L, int K, int elem_bytes, bool stage, int *stage_off);
+cudaError_t launch_forward(const LayerArgs &a, int dtype, size_t smem, cudaStream_t st);
+int occupancy_forward(int dtype, int K, int threads, size_t smem);
+
 size_t dw_smem_bytes(const Geo &geo, int G, int L, int K, int elem_bytes, bool stage, int *stage_off);
 
+// Weight gradient of planes too large for the whole-plane kernel: Haar pyramids of x and dy in
+// the workspace (float4 (LL, LH, HL, HH) per position, level l at pyr_*[l]), then tiled
+// correlations writing nb partials per (channel, signal, tap) for the finalize kernel.
+struct DwPyramidArgs {
+    int B, C, H, W, L, K;
+    int nb;                    // partials per (channel, signal, tap): CTAs per channel of each correlation
+    const void *x, *dy;
+    float4 *pyr_x[kMaxLevels + 1], *pyr_dy[kMaxLevels + 1];
+    float *partials;           // [nb][C][1+4L][K*K+1]
+};
+size_t dw_pyramid_bytes(int B, int C, int H, int W, int L);
+cudaError_t launch_dw_pyramid(const DwPyramidArgs &a, int dtype, cudaStream_t st);
+
 // Launchers (host side, in the kernel translation units).  dtype: 0 f32, 1 bf16, 2 f16.
-cudaError_t launch_forward(const LayerArgs &a, int dtype, size_t smem, cudaStream_t st);
 cudaError_t launch_dw(const LayerArgs &a, int dtype, size_t smem, cudaStream_t st);
 cudaError_t launch_dw_finalize(const LayerArgs &a, float *d_base_w, float *d_base_bias,
                                float *d_base_scale, float *d_wavelet_w, float *d_wavelet_scale,
                                cudaStream_t st);
-int occupancy_forward(int dtype, int K, int threads, size_t smem);
 int occupancy_dw(int dtype, int K, int threads, size_t smem);
 
 }  // namespace wtconv

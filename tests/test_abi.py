@@ -67,7 +67,15 @@ def test_backward_entry_points_reject_invalid_arguments():
 
 def test_workspace_size_of_invalid_shape_is_zero():
     assert W.wtconv_workspace_size(W.OP_BACKWARD, 2, 3, 12, 16, 3, 5, 0) == 0
-    assert W.wtconv_workspace_size(W.OP_FORWARD, 2, 3, 16, 16, 2, 5, 0) == 0
+    assert W.wtconv_workspace_size(W.OP_FORWARD, 2, 3, 16, 16, 0, 5, 0) == 0
+
+
+def test_forward_workspace_holds_the_deep_contribution():
+    # levels >= 2 leave one fp32 value per level-1 position (B*C*(H/2)*(W/2)), rounded to 256 bytes
+    n = 2 * 3 * 8 * 8 * 4
+    assert W.wtconv_workspace_size(W.OP_FORWARD, 2, 3, 16, 16, 2, 5, 0) == (n + 255) // 256 * 256
+    assert W.wtconv_workspace_size(W.OP_BACKWARD_INPUT, 2, 3, 16, 16, 2, 5, 1) == (n + 255) // 256 * 256
+    assert W.wtconv_workspace_size(W.OP_FORWARD, 2, 3, 16, 16, 1, 5, 0) == 0
 
 
 def test_fault_injection_returns_before_launch(monkeypatch):
