@@ -62,7 +62,8 @@ enum wtconv_status {
     WTCONV_ERR_UNSUPPORTED = 2, /* valid but not built: dtype, k, or a plane too large */
     WTCONV_ERR_WORKSPACE = 3,   /* workspace smaller than wtconv_workspace_size() */
     WTCONV_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
-    WTCONV_ERR_INJECTED = 5     /* WTCONV_INJECT_FAULT is set */
+    WTCONV_ERR_INJECTED = 5,    /* WTCONV_INJECT_FAULT is set */
+    WTCONV_ERR_SCRATCH_LIMIT = 6 /* shape needs more than WTCONV_NOALLOC_SCRATCH_BYTES of scratch */
 };
 
 /* Operation selector for wtconv_workspace_size. */
@@ -124,6 +125,40 @@ int wtconv_backward(int B, int C, int H, int W, int L, int k, int dtype, const v
                     void *dx, float *d_base_w, float *d_base_bias, float *d_base_scale,
                     float *d_wavelet_w, float *d_wavelet_scale, void *workspace,
                     size_t workspace_bytes, wtconv_stream_t stream);
+
+/* Size of the fixed device scratch behind wtconv_backward_weights_noalloc: 4 MiB per device. */
+#define WTCONV_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* wtconv_backward_weights without a workspace argument.  The pages describe no such call: it is
+ * an addition of this library, for callers that cannot hand it device memory.  Examples are a
+ * plain C host program that has no device allocator of its own, a plug-in whose host framework
+ * owns all device memory and lends none, and a training step whose memory was budgeted in full
+ * beforehand, where a late allocation could fail or stall on the allocator.
+ *
+ * The per-CTA partial sums of the weight-gradient reduction go to a scratch array that is
+ * compiled into the library (WTCONV_NOALLOC_SCRATCH_BYTES bytes of device memory per device,
+ * reserved when the library's device code is loaded).  This call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *   - Set-up: the first call on a device, with that device current, looks up the scratch
+ *     address (cudaGetSymbolAddress) and plans the shape; later calls reuse both.  Make that
+ *     first call for each device and shape before any stream capture begins.
+ *   - Limit: if this shape needs more scratch than WTCONV_NOALLOC_SCRATCH_BYTES (many channels
+ *     and levels, or planes too large for the whole-plane kernel, which need their Haar
+ *     pyramids in scratch), the call returns WTCONV_ERR_SCRATCH_LIMIT and launches nothing;
+ *     use wtconv_backward_weights with a workspace then.
+ *   - Nothing in the scratch has to start at zero: every partial is written before it is read.
+ *   - The scratch is shared by every call on the device.  Calls whose execution overlaps (on
+ *     different streams, or issued from different host threads without ordering) race on it
+ *     and give wrong gradients; calls ordered on one stream are safe.
+ * Arguments, outputs and the other status codes are those of wtconv_backward_weights, whose
+ * kernels this call runs; the results equal that call's for the same device and shape. */
+int wtconv_backward_weights_noalloc(int B, int C, int H, int W, int L, int k, int dtype,
+                                    const void *x, const void *dy, const float *base_w,
+                                    const float *base_bias, const float *base_scale,
+                                    const float *wavelet_w, const float *wavelet_scale,
+                                    float *d_base_w, float *d_base_bias, float *d_base_scale,
+                                    float *d_wavelet_w, float *d_wavelet_scale,
+                                    wtconv_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -428,6 +428,26 @@ bool params_ok(const float *base_w, const float *base_bias, const float *base_sc
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? WTCONV_OK : WTCONV_ERR_CUDA; }
 
+// Scratch of wtconv_backward_weights_noalloc: the weight-gradient partials of one call, in device
+// memory that comes with the library's module instead of from an allocator.
+__device__ __align__(256) unsigned char g_noalloc_scratch[WTCONV_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device (with
+// that device current) and cached; nullptr if the lookup fails.
+void *noalloc_scratch() {
+    static std::mutex mu;
+    static std::map<int, void *> addr;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = addr.find(dev);
+    if (it != addr.end()) return it->second;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    addr.emplace(dev, p);
+    return p;
+}
+
 }  // namespace
 
 extern "C" {
@@ -442,6 +462,7 @@ const char *wtconv_strerror(int status) {
     case WTCONV_ERR_WORKSPACE: return "workspace too small";
     case WTCONV_ERR_CUDA: return "CUDA runtime error";
     case WTCONV_ERR_INJECTED: return "fault injected (WTCONV_INJECT_FAULT)";
+    case WTCONV_ERR_SCRATCH_LIMIT: return "shape needs more scratch than the no-alloc entry point's fixed array";
     default: return "unknown status";
     }
 }
@@ -586,6 +607,30 @@ int wtconv_backward_weights(int B, int C, int H, int W, int L, int k, int dtype,
     return backward_common(false, B, C, H, W, L, k, dtype, x, dy, base_w, base_bias, base_scale, wavelet_w,
                            wavelet_scale, nullptr, d_base_w, d_base_bias, d_base_scale, d_wavelet_w,
                            d_wavelet_scale, workspace, workspace_bytes, stream);
+}
+
+int wtconv_backward_weights_noalloc(int B, int C, int H, int W, int L, int k, int dtype, const void *x,
+                                    const void *dy, const float *base_w, const float *base_bias,
+                                    const float *base_scale, const float *wavelet_w, const float *wavelet_scale,
+                                    float *d_base_w, float *d_base_bias, float *d_base_scale, float *d_wavelet_w,
+                                    float *d_wavelet_scale, wtconv_stream_t stream) {
+    int st = validate_shape(B, C, H, W, L, k, dtype);
+    if (st != WTCONV_OK) return st;
+    if (!aligned16(x) || !aligned16(dy) || !params_ok(base_w, base_bias, base_scale, wavelet_w, wavelet_scale) ||
+        !params_ok(d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale))
+        return WTCONV_ERR_INVALID_ARG;
+    if (fault_injected()) return WTCONV_ERR_INJECTED;
+    Plan pw = plan_dw(B, C, H, W, L, k, dtype);
+    if (pw.status != WTCONV_OK) return pw.status;
+    if (pw.dw_pyramid || pw.workspace > sizeof(g_noalloc_scratch)) return WTCONV_ERR_SCRATCH_LIMIT;
+    void *scratch = noalloc_scratch();
+    if (scratch == nullptr) return WTCONV_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    pw.a.x = x; pw.a.dy = dy;
+    set_params(pw.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
+    pw.a.partials = static_cast<float *>(scratch);
+    if (launch_dw(pw.a, dtype, pw.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+    return cuda_status(launch_dw_finalize(pw.a, d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale, s));
 }
 
 int wtconv_backward(int B, int C, int H, int W, int L, int k, int dtype, const void *x, const void *dy,

@@ -6,7 +6,8 @@ caching allocator.  There is no CPU or PyTorch fallback: if the library cannot b
 call raises.
 
 Functions carry the C names: ``wtconv_forward``, ``wtconv_backward_input``,
-``wtconv_backward_weights``, ``wtconv_backward``, ``wtconv_workspace_size``,
+``wtconv_backward_weights``, ``wtconv_backward``, ``wtconv_backward_weights_noalloc``,
+``wtconv_workspace_size``,
 ``wtconv_strerror``, ``wtconv_version``.  ``WTConvFunction`` wraps forward and the fused
 backward as a ``torch.autograd.Function``.
 """
@@ -21,12 +22,14 @@ from . import _build
 
 F32, BF16, F16 = 0, 1, 2
 OP_FORWARD, OP_BACKWARD_INPUT, OP_BACKWARD_WEIGHTS, OP_BACKWARD = 0, 1, 2, 3
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_INJECTED = range(6)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_INJECTED, ERR_SCRATCH_LIMIT = range(7)
+NOALLOC_SCRATCH_BYTES = 4 << 20  # WTCONV_NOALLOC_SCRATCH_BYTES
 TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16, F16: torch.float16}
 DTYPE_CODE = {v: k for k, v in TORCH_DTYPE.items()}
 
 EXPORTED = ("wtconv_version", "wtconv_strerror", "wtconv_workspace_size", "wtconv_forward",
-            "wtconv_backward_input", "wtconv_backward_weights", "wtconv_backward")
+            "wtconv_backward_input", "wtconv_backward_weights", "wtconv_backward",
+            "wtconv_backward_weights_noalloc")
 
 _lib = None
 
@@ -69,6 +72,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.wtconv_backward_input.argtypes = shape + params + [vp, vp, vp, sz, vp]
     lib.wtconv_backward_weights.restype = i
     lib.wtconv_backward_weights.argtypes = shape + [vp, vp] + params + [fp] * 5 + [vp, sz, vp]
+    lib.wtconv_backward_weights_noalloc.restype = i
+    lib.wtconv_backward_weights_noalloc.argtypes = shape + [vp, vp] + params + [fp] * 5 + [vp]
     lib.wtconv_backward.restype = i
     lib.wtconv_backward.argtypes = shape + [vp, vp] + params + [vp] + [fp] * 5 + [vp, sz, vp]
     _lib = lib
@@ -190,6 +195,24 @@ def wtconv_backward_weights(x, dy, base_w, base_bias, base_scale, wavelet_w, wav
     ws, nbytes = _workspace(OP_BACKWARD_WEIGHTS, shape, x.device, workspace)
     rc = load().wtconv_backward_weights(*shape, _ptr(x), _ptr(dy), *p, *gp, _ptr(ws), nbytes, _stream(stream))
     _raise(rc, "wtconv_backward_weights")
+    return grads
+
+
+def wtconv_backward_weights_noalloc(x, dy, base_w, base_bias, base_scale, wavelet_w, wavelet_scale, grads,
+                                    stream=None) -> dict:
+    """wtconv_backward_weights on the library's fixed scratch: no workspace, no allocation.
+
+    ``grads`` (the dict of gradient buffers) must be passed in, so this call allocates nothing
+    either; calls that overlap in time race on the shared scratch."""
+    if grads is None:
+        raise ValueError("wtconv_backward_weights_noalloc needs preallocated gradient buffers")
+    _check_act(x, "x")
+    _check_act(dy, "dy")
+    shape = _shape(x, wavelet_w, base_w)
+    p = _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, x.device)
+    grads, gp = _grad_buffers(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, grads)
+    rc = load().wtconv_backward_weights_noalloc(*shape, _ptr(x), _ptr(dy), *p, *gp, _stream(stream))
+    _raise(rc, "wtconv_backward_weights_noalloc")
     return grads
 
 

@@ -31,7 +31,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_version_and_strerror():
     assert W.wtconv_version() >= 100
-    for s in range(6):
+    for s in range(7):
         assert isinstance(W.wtconv_strerror(s), str) and W.wtconv_strerror(s)
     assert "unknown" in W.wtconv_strerror(99)
 
@@ -63,6 +63,11 @@ def test_backward_entry_points_reject_invalid_arguments():
     assert lib.wtconv_backward(2, 3, 16, 16, 2, 6, 0, FAKE, FAKE, *p5, FAKE, *p5, None, 0, None) == W.ERR_INVALID_ARG
     assert lib.wtconv_backward(2, 3, 16, 16, 2, 5, 0, FAKE, FAKE, *p5, FAKE, FAKE, None, FAKE, FAKE, FAKE,
                                None, 0, None) == W.ERR_INVALID_ARG
+    noalloc = lib.wtconv_backward_weights_noalloc
+    assert noalloc(*shape, FAKE, None, *p5, *p5, None) == W.ERR_INVALID_ARG
+    assert noalloc(2, 3, 12, 16, 3, 5, 0, FAKE, FAKE, *p5, *p5, None) == W.ERR_INVALID_ARG
+    assert noalloc(2, 3, 16, 16, 2, 5, 0, FAKE, FAKE, *p5, FAKE, ctypes.c_void_p(258), FAKE, FAKE, FAKE,
+                   None) == W.ERR_INVALID_ARG
 
 
 def test_workspace_size_of_invalid_shape_is_zero():
@@ -84,5 +89,6 @@ def test_fault_injection_returns_before_launch(monkeypatch):
     assert _fwd(lib) == W.ERR_INJECTED
     p5 = [FAKE] * 5
     assert lib.wtconv_backward(2, 3, 16, 16, 2, 5, 0, FAKE, FAKE, *p5, FAKE, *p5, None, 0, None) == W.ERR_INJECTED
+    assert lib.wtconv_backward_weights_noalloc(2, 3, 16, 16, 2, 5, 0, FAKE, FAKE, *p5, *p5, None) == W.ERR_INJECTED
     monkeypatch.setenv("WTCONV_INJECT_FAULT", "0")
     assert _fwd(lib, k=4) == W.ERR_INVALID_ARG
