@@ -38,6 +38,9 @@
  *     the caller's next synchronisation, as with any CUDA launch.
  *   - The library keeps no state between calls; concurrent calls on different streams with
  *     distinct workspaces are safe.
+ *   - The forward and the input gradient run one whole-plane kernel where a plane's Haar pyramid
+ *     fits in shared memory, else two tiled kernels.  WTCONV_FWD_PATH=tiles selects the tiled
+ *     kernels for every shape (same results within fp32 rounding).
  *   - Setting the environment variable WTCONV_INJECT_FAULT=1 makes every compute entry point
  *     return WTCONV_ERR_INJECTED before launching anything (host-side fault injection).
  */
@@ -89,6 +92,14 @@ const char *wtconv_strerror(int status);
  * gradients need one fp32 partial per (CTA, channel, subband, tap); BACKWARD needs both.
  * Returns 0 for an invalid shape as well; the compute call then reports the error. */
 size_t wtconv_workspace_size(int op, int B, int C, int H, int W, int L, int k, int dtype);
+
+/* Number of kernel launches `op` makes for this shape on the current device (0 for an invalid
+ * or unsupported shape).  Planes whose Haar pyramid fits in shared memory take one launch for
+ * the forward and the input gradient and two for the weight gradients (correlations +
+ * finalize); larger planes take two for the forward / input gradient (levels >= 2, then the
+ * base conv and level 1) and 2L + 2 for the weight gradients (L pyramid levels, L + 1
+ * correlations, finalize).  BACKWARD is the sum of BACKWARD_INPUT and BACKWARD_WEIGHTS. */
+int wtconv_launch_count(int op, int B, int C, int H, int W, int L, int k, int dtype);
 
 /* Forward pass (Metodologia: fused on-chip Haar analysis, folded scales, closed-form
  * synthesis).  Writes y [B][C][H][W]. */

@@ -36,6 +36,13 @@ int validate_shape(int B, int C, int H, int W, int L, int k, int dtype) {
     return WTCONV_OK;
 }
 
+// WTCONV_FWD_PATH=tiles: the forward and input gradient take the tiled kernels even where the
+// whole-plane kernel fits (same results within rounding; for testing and comparison).
+bool tiles_forced() {
+    const char *v = getenv("WTCONV_FWD_PATH");
+    return v && strcmp(v, "tiles") == 0;
+}
+
 bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 bool aligned4(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
 
@@ -269,12 +276,12 @@ struct SPlan {
 };
 
 // Shallow kernel tiles: full-width tiles up to 64 columns, at most 32 fused 8x4 items per tile
-// (one per lane); small planes are packed G to a warp.
+// (one per lane); small planes are packed G to a unit.  Copy chunks are the widest of 16, 8 and
+// 4 bytes for which every chunk lies wholly inside or outside the plane.
 SPlan plan_shallow_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
     SPlan p;
     ShallowArgs &a = p.a;
     a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
-    a.vec_ld = (W % 4) == 0;
     a.st_mode = (W % 4) == 0 ? 1 : 0;
     const int W4 = round_up(W, 4);
     const int TW = W4 <= 64 ? W4 : 64;
@@ -290,21 +297,18 @@ SPlan plan_shallow_uncached(int B, int C, int H, int W, int L, int k, int dtype)
         if (G > B) G = B;
     }
     const int eb = elem_bytes(dtype);
-    const int P = k / 2;
-    // staged tiles move 8-byte chunks: each must lie wholly inside or outside the plane, and its
-    // shared destination must be 8-byte aligned (an fp32 tile is staged straight into the X
-    // layout, whose interior starts pad_l = (4 - P % 4) % 4 floats in: even only for even P)
-    const int E = 8 / eb;
-    const int pad_l = (4 - P % 4) % 4;
-    const int dst_off_bytes = eb == 4 ? pad_l * 4 : 0;
-    a.stage = ((2 * P) % E == 0 && W % E == 0 && dst_off_bytes % 8 == 0 && (L < 2 || W % 4 == 0)) ? 1 : 0;
-    const bool convert = eb != 4;
-    a.sg = make_shallow_geo(H, W, k, TH, TW, G, eb);
-    p.smem = shallow_smem_bytes(a.sg, k, a.stage != 0, convert);
+    int chunk_e = 16 / eb;
+    while (chunk_e > 1 && (W % chunk_e != 0 || TW % chunk_e != 0)) chunk_e /= 2;
+    if (chunk_e * eb < 4) { p.status = WTCONV_ERR_UNSUPPORTED; return p; }
+    const int W1 = W / 2;
+    const int dchunk_e = (W1 % 4 == 0 && (TW / 2) % 4 == 0) ? 4 : 2;
+    const bool convert = eb != 4, deep = L >= 2;
+    a.sg = make_shallow_geo(H, W, k, TH, TW, G, eb, chunk_e, dchunk_e);
+    p.smem = shallow_smem_bytes(a.sg, k, convert, deep);
     while (G > 1 && p.smem + kStaticSmemMargin > (size_t)kMaxSmem) {
         --G;
-        a.sg = make_shallow_geo(H, W, k, TH, TW, G, eb);
-        p.smem = shallow_smem_bytes(a.sg, k, a.stage != 0, convert);
+        a.sg = make_shallow_geo(H, W, k, TH, TW, G, eb, chunk_e, dchunk_e);
+        p.smem = shallow_smem_bytes(a.sg, k, convert, deep);
     }
     if (p.smem + kStaticSmemMargin > (size_t)kMaxSmem) { p.status = WTCONV_ERR_UNSUPPORTED; return p; }
     const int sms = device_sms();
@@ -318,17 +322,14 @@ SPlan plan_shallow_uncached(int B, int C, int H, int W, int L, int k, int dtype)
     if (nb > a.units) nb = a.units;
     a.units_per_cta = (int)((a.units + nb - 1) / nb);
     a.nb = (a.units + a.units_per_cta - 1) / a.units_per_cta;
-    const int nchunk = (TW + 4 * P) / 4;
     a.tiles = make_fastdiv(tiles);
     a.tiles_c = make_fastdiv(a.sg.tiles_c);
-    a.xchunk = make_fastdiv(nchunk);
-    a.xload = make_fastdiv(a.sg.xrows * nchunk);
+    a.rchunks_row = make_fastdiv(a.sg.xw / chunk_e);
+    a.xrows = make_fastdiv(a.sg.xrows);
+    a.dchunks_row = make_fastdiv((TW / 2) / dchunk_e);
+    a.drows = make_fastdiv(TH / 2);
     a.ycols = make_fastdiv(a.sg.ycols);
-    a.ypos = make_fastdiv(a.sg.yrows * a.sg.ycols);
-    a.rchunk_row = make_fastdiv((TW + 4 * P) / E);
-    a.rchunks = make_fastdiv(a.sg.xrows * ((TW + 4 * P) / E));
-    a.dchunk_row = make_fastdiv(TW / 4);
-    a.dchunks = make_fastdiv((TH / 2) * (TW / 4));
+    a.xw4 = make_fastdiv(a.sg.xw / 4);
     return p;
 }
 
@@ -480,6 +481,24 @@ size_t wtconv_workspace_size(int op, int B, int C, int H, int W, int L, int k, i
     return bytes;
 }
 
+int wtconv_launch_count(int op, int B, int C, int H, int W, int L, int k, int dtype) {
+    if (validate_shape(B, C, H, W, L, k, dtype) != WTCONV_OK) return 0;
+    int n = 0;
+    if (op == WTCONV_OP_FORWARD || op == WTCONV_OP_BACKWARD_INPUT || op == WTCONV_OP_BACKWARD) {
+        const Plan pf = plan_forward(B, C, H, W, L, k, dtype);
+        if (pf.status == WTCONV_OK && !tiles_forced()) n += 1;
+        else if (pf.status == WTCONV_OK) n += L >= 2 ? 2 : 1;
+        else if (pf.status == WTCONV_ERR_UNSUPPORTED) n += L >= 2 ? 2 : 1;
+        else return 0;
+    }
+    if (op == WTCONV_OP_BACKWARD_WEIGHTS || op == WTCONV_OP_BACKWARD) {
+        const Plan pw = plan_dw(B, C, H, W, L, k, dtype);
+        if (pw.status != WTCONV_OK) return 0;
+        n += pw.dw_pyramid ? 2 * L + 2 : 2;
+    }
+    return n;
+}
+
 // The layer's linear operator on `src` (x -> y, or dy -> dx with rotated kernels and no bias):
 // deep kernel (levels >= 2 -> contribution at level-1 resolution, in the workspace), then the
 // shallow kernel (base conv + level 1 + synthesis, final outputs).
@@ -487,9 +506,10 @@ static int run_operator(int B, int C, int H, int W, int L, int k, int dtype, con
                         const float *base_bias, const float *base_scale, const float *wavelet_w,
                         const float *wavelet_scale, void *dst, bool flip, void *workspace, size_t workspace_bytes,
                         cudaStream_t s) {
-    // planes whose whole pyramid fits in shared memory: one kernel, no workspace
+    // planes whose whole pyramid fits in shared memory: one kernel, no workspace (unless
+    // WTCONV_FWD_PATH=tiles asks for the tiled kernels)
     Plan pf = plan_forward(B, C, H, W, L, k, dtype);
-    if (pf.status == WTCONV_OK) {
+    if (pf.status == WTCONV_OK && !tiles_forced()) {
         pf.a.x = src;
         pf.a.out = dst;
         set_params(pf.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
@@ -497,7 +517,7 @@ static int run_operator(int B, int C, int H, int W, int L, int k, int dtype, con
         pf.a.with_bias = flip ? 0 : 1;
         return cuda_status(launch_forward(pf.a, dtype, pf.smem, s));
     }
-    if (pf.status != WTCONV_ERR_UNSUPPORTED) return pf.status;
+    if (pf.status != WTCONV_OK && pf.status != WTCONV_ERR_UNSUPPORTED) return pf.status;
     const size_t dbytes = deep_bytes(B, C, H, W, L);
     Plan pd;
     if (L >= 2) {

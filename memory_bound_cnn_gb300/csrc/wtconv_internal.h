@@ -136,76 +136,74 @@ struct LayerArgs {
 
 // Dynamic shared memory of the kernels for G planes per slot group; *stage_off receives the
 // byte offset of the staging area (staging holds n_in * G raw planes of elem_bytes elements).
-// Geometry of one shallow tile slot: the zero-padded fp32 input tile X (the output tile plus a
-// halo of 2P pixels: P for the base conv, P level-1 coefficients for the level-1 conv) and the
-// tile's Haar level 1 as two subband-pair images (LL|LH, HL|HH) with a halo of P coefficients.
+// Geometry of the shallow kernel's tiles.  A unit is one output tile of TH x TW pixels of G
+// planes (G > 1 only when one tile covers a whole plane).  Its input tile X covers plane rows
+// r0 - 2P .. r0 + TH + 2P - 1 and columns c0 - padx .. c0 + TW + padx - 1 (halo 2P: P for the
+// base conv, P level-1 coefficients for the level-1 conv; padx = 2P rounded up to a multiple of
+// 4 and of the copy chunk, so every chunk lies wholly inside or outside the plane and every base
+// window row starts 16-byte aligned).  Level 1 of the tile (+ P coefficients of halo) is kept as
+// two subband-pair images (LL|LH, HL|HH).
 struct ShallowGeo {
     int TH, TW;            // output tile (TH % 8 == 0, TW % 4 == 0)
-    int G;                 // planes per slot group (whole-plane tiles of small planes), else 1
+    int G;                 // planes per unit
     int tiles_r, tiles_c;  // tiles per plane
-    int pad_l;             // left padding of X so every base window starts 16-byte aligned
-    int xrows, xpitch;     // X tile (floats)
-    int yrows, ypitch;     // level-1 pair images (positions)
-    int ycols;             // level-1 positions computed per row (TW/2 + 2P)
-    int off_y, yimg;       // start of pair image 0 (floats from the slot start); floats per image
-    int slot_floats;
+    int padx;              // left / right halo columns of X (multiple of 4 and of chunk_e)
+    int xrows, xw;         // X tile rows and row length (floats; also the raw tile's row length)
+    int yrows, ycols;      // level-1 positions per pair image (TH/2 + 2P) x (TW/2 + 2P)
+    int ypitch, yimg;      // pair-image row pitch (positions) and floats per image
     int items_r, items_c;  // fused output items per tile (8 x 4 pixels each)
-    // staged path: raw input tiles (type T, two buffers) and deep-contribution tiles (fp32, two
-    // buffers) arrive by cp.async while the previous tile computes
-    int rpitch, roff;      // raw tile pitch and interior column offset (elements)
-    int raw_bytes;         // one raw tile buffer (all G planes), 16-byte rounded
+    int chunk_e;           // elements per cp.async chunk of the raw tile (16, 8 or 4 bytes)
+    int dchunk_e;          // floats per cp.async chunk of the deep tile (4 or 2)
     int dtile;             // floats of one deep tile per plane: (TH/2) x (TW/2)
+    int raw_bytes;         // one raw tile buffer (G planes), 16-byte rounded
+    int xbuf;              // floats of one X buffer (G planes): the raw buffer itself for fp32
+    int pslot;             // floats of the pair images of one plane
 };
 
-__host__ __device__ inline ShallowGeo make_shallow_geo(int H, int W, int K, int TH, int TW, int G, int elem_bytes) {
+__host__ __device__ inline ShallowGeo make_shallow_geo(int H, int W, int K, int TH, int TW, int G, int elem_bytes,
+                                                       int chunk_e, int dchunk_e) {
     ShallowGeo s = {};
     const int P = K / 2;
-    const int NV = (kCols + K - 1 + 3) / 4, NVP = (kColsL + K - 1 + 1) / 2;
     s.TH = TH; s.TW = TW; s.G = G;
     s.tiles_r = ceil_div(H, TH);
     s.tiles_c = ceil_div(W, TW);
-    s.pad_l = (4 - P % 4) % 4;
+    const int pq = chunk_e > 4 ? chunk_e : 4;
+    s.padx = round_up(2 * P, pq);
     s.xrows = TH + 4 * P;
-    const int xneed = (TW + 4 * P) > (TW - 4 + P + 4 * NV) ? (TW + 4 * P) : (TW - 4 + P + 4 * NV);
-    s.xpitch = round_up(xneed + s.pad_l, 4);
+    s.xw = TW + 2 * s.padx;
     s.yrows = TH / 2 + 2 * P;
     s.ycols = TW / 2 + 2 * P;
-    const int yneed = s.ycols > (TW / 2 - 3 + 2 * NVP) ? s.ycols : (TW / 2 - 3 + 2 * NVP);
-    s.ypitch = round_up(yneed, 2);
-    s.off_y = round_up(s.xrows * s.xpitch, 4);
+    s.ypitch = round_up(s.ycols, 2);
     s.yimg = 2 * s.yrows * s.ypitch;
-    s.slot_floats = round_up(s.off_y + 2 * s.yimg, 4);
+    s.pslot = 2 * s.yimg;
     s.items_r = TH / kRows;
     s.items_c = TW / kCols;
-    // fp32 input: the raw tile has the X layout itself; narrower types are converted into X
-    s.rpitch = elem_bytes == 4 ? s.xpitch : round_up(TW + 4 * P, 8);
-    s.roff = elem_bytes == 4 ? s.pad_l : 0;
-    s.raw_bytes = round_up(G * s.xrows * s.rpitch * elem_bytes, 16);
+    s.chunk_e = chunk_e;
+    s.dchunk_e = dchunk_e;
     s.dtile = (TH / 2) * (TW / 2);
+    s.raw_bytes = round_up(G * s.xrows * s.xw * elem_bytes, 16);
+    s.xbuf = G * s.xrows * s.xw;
     return s;
 }
 
 struct ShallowArgs {
     int B, C, H, W, L, K;
-    int units;            // work units per channel: slot groups x tiles
+    int units;            // work units per channel: plane groups x tiles
     int units_per_cta;    // contiguous units each CTA walks through
     int nb;               // CTAs per channel; grid = nb * C
-    int vec_ld, st_mode;
-    int stage;            // 1: cp.async double-buffered tiles (8-byte chunks that never straddle the plane edge)
+    int st_mode;          // output stores: 1 = 4-element vectors where a row allows, 0 = scalar
     const void *x;        // forward: x; input gradient: dy
     const float *deep;    // deep contribution at level-1 resolution [B][C][H/2][W/2] (L >= 2)
     void *out;            // y or dx
     const float *base_w, *base_bias, *base_scale, *wavelet_w, *wavelet_scale;
     int flip, with_bias;
     ShallowGeo sg;
-    // units per slot group (tiles), tile columns, X-tile 4-pixel chunks per plane and per row,
-    // level-1 positions per plane and per row
-    FastDiv tiles, tiles_c, xload, xchunk, ypos, ycols;
-    FastDiv rchunks, rchunk_row;    // staged raw tile: 8-byte chunks per plane / per row
-    FastDiv dchunks, dchunk_row;    // staged deep tile: 8-byte chunks per plane / per row
+    // units per plane group (tiles) and tile columns; raw-tile chunks per row and rows per plane;
+    // deep-tile chunks per row and rows per plane; level-1 positions per row; X 4-float groups per row
+    FastDiv tiles, tiles_c, rchunks_row, xrows, dchunks_row, drows, ycols, xw4;
 };
 
-size_t shallow_smem_bytes(const ShallowGeo &sg, int K, bool stage, bool convert);
+size_t shallow_smem_bytes(const ShallowGeo &sg, int K, bool convert, bool deep);
 cudaError_t launch_shallow(const ShallowArgs &a, int dtype, size_t smem, cudaStream_t st);
 int occupancy_shallow(int dtype, int K, size_t smem);
 

@@ -1,41 +1,48 @@
 // Shallow kernel of the WTConv layer: the base conv and Haar level 1, tile by tile, writing the
 // final outputs (forward y, or the input gradient dx with rotated kernels and no bias).
 //
-// Each CTA is one warp that owns channel c and walks a run of tiles (or, for small planes, of
-// groups of whole planes).  Per tile:
-//   1. the zero-padded input tile X (output tile + 2P halo) is read once and converted to fp32;
-//   2. Haar level 1 of the tile (+ P coefficients of halo) is computed on chip with butterflies
-//      and stored as two subband-pair images (LL|LH, HL|HH);
+// Each CTA is one warp that owns channel c and walks a run of units (a unit is one output tile
+// of G planes; G > 1 only when a tile covers a whole plane).  Per unit:
+//   1. the input tile (output tile + 2P halo, zero outside the plane) arrives by cp.async in
+//      chunks that never straddle the plane edge; fp32 tiles land directly in the conv layout X,
+//      narrower types are converted into X by one elementwise pass (after which the raw buffer
+//      takes the next unit's copy while this unit computes);
+//   2. Haar level 1 of the tile (+ P coefficients of halo) is computed with butterflies and
+//      stored as two subband-pair images (LL|LH, HL|HH);
 //   3. every lane owns an 8 x 4 pixel output block and computes, in registers:
 //        - the level-1 convs of its 4 x 2 coefficients for all four subbands (folded kernels,
 //          packed f32x2 FMAs on subband pairs),
 //        - their closed-form synthesis onto its 8 x 4 pixels, plus the contribution of the
-//          deeper levels (precomputed at level-1 resolution by the deep kernel) and the bias,
+//          deeper levels (precomputed at level-1 resolution by the deep kernel, staged with the
+//          tile) and the bias,
 //        - the base conv of its block (sliding window, packed f32x2 FMAs on column pairs)
 //          accumulated on top of that,
 //      and stores each output pixel once.
-// No intermediate tensor reaches global memory except the deep contribution (N/4 floats).
+// The G planes of a unit are stacked vertically in X and in the pair images, so the per-unit
+// loops index rows of one tall image.
 #include "wtconv_device.cuh"
 
 namespace wtconv {
 
-// Shared memory: G plane slots ([X tile] + level-1 pair images; X lives in the raw buffer when a
-// staged fp32 tile can be used as is), then two raw tile buffers and two deep tiles (staged
-// path), then the kernels.
-size_t shallow_smem_bytes(const ShallowGeo &sg, int K, bool stage, bool convert) {
-    const size_t xfl = (size_t)round_up(sg.xrows * sg.xpitch, 4);
-    const size_t pslot = (stage && !convert ? 0 : xfl) + 2 * (size_t)sg.yimg;
-    size_t bytes = (size_t)sg.G * pslot * sizeof(float);
-    if (stage) bytes += 2 * (size_t)sg.raw_bytes + 2 * (size_t)sg.G * sg.dtile * sizeof(float);
+// Shared memory: the raw tile buffer (type T; for fp32 it is X itself), the X buffer (narrow
+// types only), the pair images, the deep tile (L >= 2), then the kernels.
+size_t shallow_smem_bytes(const ShallowGeo &sg, int K, bool convert, bool deep) {
+    size_t bytes = (size_t)sg.raw_bytes;
+    if (convert) bytes += (size_t)sg.xbuf * sizeof(float);
+    bytes += (size_t)sg.G * sg.pslot * sizeof(float);
+    if (deep) bytes += (size_t)sg.G * sg.dtile * sizeof(float);
     return bytes + (size_t)3 * wpairs(K) * sizeof(f2_t);
 }
 
-// Level-1 pair images start after the X tile in a plane slot, unless X lives in the raw buffer.
-__device__ __forceinline__ int yoff_fixed(bool x_in_raw, int xfl) { return x_in_raw ? 0 : xfl; }
-
-__device__ __forceinline__ void cp_async8(void *smem_dst, const void *gmem_src, int src_bytes) {
+// cp.async of `N` bytes (4, 8 or 16); src_bytes = 0 zero-fills the destination without reading.
+template <int N>
+__device__ __forceinline__ void cp_async_n(void *smem_dst, const void *gmem_src, int src_bytes) {
     const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(d), "l"(gmem_src), "r"(src_bytes) : "memory");
+    if constexpr (N == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gmem_src), "r"(src_bytes) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(d), "l"(gmem_src), "n"(N), "r"(src_bytes)
+                     : "memory");
 }
 
 // Level-1 conv of one subband-pair image for 4 coefficient rows x 2 positions, kept in registers.
@@ -67,19 +74,22 @@ __device__ __forceinline__ void level1_item(const float *__restrict__ in, int pi
 }
 
 // Base conv of one 8 x 4 pixel block on top of `init`, each finished row rounded and stored:
-// out[r][c] = init[r][c] + sum_{u,v} w[u][v] * X[r + u][c + v] (X window origin at `in`).
+// out[r][c] = init[r][c] + sum_{u,v} w[u][v] * X[r + u][c + v - P].  `in` points at the 16-byte
+// aligned X position 4 - P columns left of the window origin (window row r, column 0); three
+// 16-byte loads per window row cover columns 0 .. 11 of that, the window is columns
+// 4 - P .. 4 - P + 3 + K - 1.
 template <int K, typename T>
 __device__ __forceinline__ void base_item_store(const float *__restrict__ in, int pitch, const f2_t *wsm,
                                                 const f2_t (&init)[kRows][2], T *dst, int ld, int nrows,
                                                 int ncols, bool vec) {
-    constexpr int NV = (kCols + K - 1 + 3) / 4;
+    constexpr int P = K / 2, O = 4 - P;
     f2_t w[K * K];
     load_weights<K>(wsm, w);
     f2_t acc[kRows][2];
 #pragma unroll
     for (int i = 0; i < kRows + K - 1; ++i) {
-        f2_t e[2 * NV], o[2 * NV - 1];
-        load_row<NV>(in + i * pitch, e, o);
+        f2_t e[6], o[5];
+        load_row<3>(in + i * pitch, e, o);
 #pragma unroll
         for (int v = 0; v < K; ++v) {
 #pragma unroll
@@ -88,7 +98,8 @@ __device__ __forceinline__ void base_item_store(const float *__restrict__ in, in
                 if (j >= 0 && j < kRows) {
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
-                        const f2_t xv = (v & 1) ? o[q + v / 2] : e[q + v / 2];
+                        const int s0 = O + v + 2 * q;  // first column of the pair
+                        const f2_t xv = (s0 & 1) ? o[(s0 - 1) / 2] : e[s0 / 2];
                         if (u == 0 && v == 0) acc[j][q] = ffma2(w[0], xv, init[j][q]);
                         else ffma2_acc(acc[j][q], w[u * K + v], xv);
                     }
@@ -108,25 +119,28 @@ __device__ __forceinline__ void base_item_store(const float *__restrict__ in, in
     }
 }
 
+// Four narrow activations (8 bytes) to fp32.
+template <typename T>
+__device__ __forceinline__ float4 cvt4(const T *p) {
+    return Act<T>::ld4(p);
+}
+
 template <int K, typename T>
 __global__ void __launch_bounds__(32) wtconv_shallow_kernel(const ShallowArgs a) {
     constexpr int P = K / 2, WP = wpairs(K);
     constexpr bool kConvert = sizeof(T) != 4;  // narrow inputs are converted into an fp32 X tile
-    constexpr int E = 8 / (int)sizeof(T);       // elements per 8-byte staged chunk
     extern __shared__ __align__(16) float smem[];
-    const ShallowGeo &sg = a.sg;
+    const ShallowGeo sg = a.sg;
     const int lane = threadIdx.x;
     const int c = blockIdx.x % a.C;
     const int nbi = blockIdx.x / a.C;
     const int G = sg.G;
-    const bool stage = a.stage != 0;
-    const bool x_in_raw = stage && !kConvert;
-    const int xfl = round_up(sg.xrows * sg.xpitch, 4);
-    const int pslot = (x_in_raw ? 0 : xfl) + 2 * sg.yimg;  // floats per plane slot
-    float *slots = smem;
-    char *raw_base = reinterpret_cast<char *>(smem + (size_t)G * pslot);
-    float *dtile_base = reinterpret_cast<float *>(raw_base + (stage ? 2 * sg.raw_bytes : 0));
-    f2_t *wts = reinterpret_cast<f2_t *>(dtile_base + (stage ? 2 * G * sg.dtile : 0));
+    const bool has_deep = a.deep != nullptr;
+    char *raw_base = reinterpret_cast<char *>(smem);
+    float *xconv = reinterpret_cast<float *>(raw_base + (size_t)sg.raw_bytes);  // narrow types only
+    float *pairs = xconv + (kConvert ? sg.xbuf : 0);
+    float *dtile = pairs + G * sg.pslot;
+    f2_t *wts = reinterpret_cast<f2_t *>(dtile + (has_deep ? G * sg.dtile : 0));
 
     // kernels, scales folded in: 0 base {w, w}; 1, 2 level-1 subband pairs {w_LL, w_LH}, {w_HL, w_HH}
     {
@@ -145,159 +159,157 @@ __global__ void __launch_bounds__(32) wtconv_shallow_kernel(const ShallowArgs a)
             }
             wts[ci * WP + t] = pk2(v0, v1);
         }
-        // zero the slots and the staging buffers once: padding columns that no copy writes stay zero
-        float4 *s4 = reinterpret_cast<float4 *>(slots);
-        const int nz = (int)((reinterpret_cast<char *>(wts) - reinterpret_cast<char *>(slots)) / 16);
-        for (int i = lane; i < nz; i += 32) s4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     const float bias = a.with_bias ? a.base_scale[c] * a.base_bias[c] : 0.f;
     __syncthreads();
 
     const T *x = static_cast<const T *>(a.x);
     T *out = static_cast<T *>(a.out);
-    const int H = a.H, W = a.W, H1 = H >> 1, W1 = W >> 1;
-    const size_t HW = (size_t)H * W;
-    const int nchunk = (sg.TW + 4 * P) / 4;  // 4-pixel chunks per X tile row (unstaged loads)
-    const int per_tile_items = sg.items_r * sg.items_c;
-    const bool vec_st = a.st_mode >= 1;
-    const int dtw = sg.TW / 2;                 // deep tile row length
-
+    const int B = a.B, H = a.H, W = a.W, H1 = H >> 1, W1 = W >> 1;
+    const size_t HW = (size_t)H * W, HW1 = (size_t)H1 * W1;
+    const size_t cstride = (size_t)a.C * HW, cstride1 = (size_t)a.C * HW1;  // between batch entries
+    const T *xc = x + (size_t)c * HW;
+    const float *deepc = has_deep ? a.deep + (size_t)c * HW1 : nullptr;
+    const int dtw = sg.TW / 2, dth = sg.TH / 2;
+    const FastDiv fd_tiles = a.tiles, fd_tiles_c = a.tiles_c, fd_rrow = a.rchunks_row, fd_drow = a.dchunks_row;
     const int u_begin = nbi * a.units_per_cta;
     const int u_end = min(a.units, u_begin + a.units_per_cta);
+    const bool vec_st = a.st_mode >= 1;
 
-    // this lane's output item (at most one per tile by construction): fixed for the whole CTA
+    // this lane's output item (at most one per unit by construction): fixed for the whole CTA
+    const int per_tile_items = sg.items_r * sg.items_c;
     const bool has_item = lane < G * per_tile_items;
     const int ig = has_item ? lane / per_tile_items : 0;
     const int ie = lane - ig * per_tile_items;
     const int irs = has_item ? ie / sg.items_c : 0, ics = has_item ? ie - irs * sg.items_c : 0;
-    const int y_item = ig * pslot + yoff_fixed(x_in_raw, xfl) + 2 * ((4 * irs) * sg.ypitch + 2 * ics);
-    const int x_item = (kRows * irs + P) * sg.xpitch + sg.pad_l + kCols * ics + P;
+    const int x_item = (ig * sg.xrows + kRows * irs + P) * sg.xw + kCols * ics + sg.padx - 4;
+    const int y_item = 2 * ((ig * sg.yrows + 4 * irs) * sg.ypitch + 2 * ics);
     const int d_item = ig * sg.dtile + (4 * irs) * dtw + 2 * ics;
-    const int nrow = (int)a.rchunk_row.d;     // staged 8-byte chunks per raw tile row
-    const int ndrow = (int)a.dchunk_row.d;    // staged 8-byte chunks per deep tile row
 
-    // cp.async of unit u's raw input tiles and deep tiles into buffer `buf`; chunks outside the
-    // plane are zero-filled (source size 0).  Lanes walk (row, chunk) with incremental indices.
-    auto issue_stage = [&](int u, int buf) {
-        const int bg = fdiv(a.tiles, u), t = u - bg * (int)a.tiles.d;
-        const int tr = fdiv(a.tiles_c, t), tc = t - tr * sg.tiles_c;
-        const int rb = tr * sg.TH - 2 * P, cb = tc * sg.TW - 2 * P;
-        T *raw = reinterpret_cast<T *>(raw_base + buf * sg.raw_bytes) + sg.roff;
-        for (int g = 0; g < G; ++g) {
-            const int b = bg * G + g;
-            const bool plane_ok = b < a.B;
-            const T *src_plane = x + ((size_t)(plane_ok ? b : 0) * a.C + c) * HW;
-            T *dst_plane = raw + (size_t)g * sg.xrows * sg.rpitch;
-            int row = 0, m = lane;
-            while (m >= nrow) { m -= nrow; ++row; }
-            for (; row < sg.xrows;) {
-                const int pr = rb + row, pc = cb + E * m;
-                const bool in = plane_ok && (unsigned)pr < (unsigned)H && (unsigned)pc < (unsigned)W;
-                cp_async8(dst_plane + row * sg.rpitch + E * m, in ? src_plane + (size_t)pr * W + pc : x, in ? 8 : 0);
-                m += 32;
-                while (m >= nrow) { m -= nrow; ++row; }
-            }
-        }
-        if (a.deep != nullptr) {
-            float *dt = dtile_base + buf * G * sg.dtile;
-            const int drb = tr * (sg.TH >> 1), dcb = tc * (sg.TW >> 1);
-            for (int g = 0; g < G; ++g) {
-                const int b = bg * G + g;
-                const bool plane_ok = b < a.B;
-                const float *src_plane = a.deep + ((size_t)(plane_ok ? b : 0) * a.C + c) * H1 * W1;
-                int i = 0, m = lane;
-                while (m >= ndrow) { m -= ndrow; ++i; }
-                for (; i < (sg.TH >> 1);) {
-                    const int dr = drb + i, dc = dcb + 2 * m;
-                    const bool in = plane_ok && dr < H1 && dc + 1 < W1;
-                    cp_async8(dt + g * sg.dtile + i * dtw + 2 * m, in ? src_plane + (size_t)dr * W1 + dc : a.deep,
-                              in ? 8 : 0);
-                    m += 32;
-                    while (m >= ndrow) { m -= ndrow; ++i; }
+    // lane layout of the copy and analysis loops: a lane keeps one column (chunk or position) and
+    // walks rows with a fixed stride, so no index is divided per element
+    const int nrow = (int)fd_rrow.d, ndrow = (int)fd_drow.d;
+    const int r_rstep = nrow >= 32 ? 1 : 32 / nrow, r_lanes = nrow >= 32 ? 32 : r_rstep * nrow;
+    const int r_row0 = nrow >= 32 ? 0 : lane / nrow, r_col = (nrow >= 32 ? lane : lane - r_row0 * nrow) * sg.chunk_e;
+    const int n_rrows = G * sg.xrows;
+    const int d_rstep = ndrow >= 32 ? 1 : 32 / ndrow, d_lanes = ndrow >= 32 ? 32 : d_rstep * ndrow;
+    const int d_row0 = ndrow >= 32 ? 0 : lane / ndrow, d_col = (ndrow >= 32 ? lane : lane - d_row0 * ndrow) * sg.dchunk_e;
+    const int n_drows = G * dth;
+    const int ycols = sg.ycols;
+    const int a_rstep = ycols >= 32 ? 1 : 32 / ycols, a_lanes = ycols >= 32 ? 32 : a_rstep * ycols;
+    const int a_row0 = ycols >= 32 ? 0 : lane / ycols, a_col0 = ycols >= 32 ? lane : lane - a_row0 * ycols;
+    const int n_arows = G * sg.yrows;
+
+    // cp.async of unit u's raw input tiles; chunks outside the plane (or past the last batch
+    // entry) are zero-filled without a read.  One commit group.
+    auto issue_raw = [&](int u) {
+        const int bg = (int)fdiv(fd_tiles, (uint32_t)u), t = u - bg * (int)fd_tiles.d;
+        const int tr = (int)fdiv(fd_tiles_c, (uint32_t)t), tc = t - tr * sg.tiles_c;
+        const int b0 = bg * G;
+        const int rb = tr * sg.TH - 2 * P, cb = tc * sg.TW - sg.padx;
+        T *raw = reinterpret_cast<T *>(raw_base);
+        // lane -> fixed chunk column (several columns only for rows of more than 32 chunks); rows
+        // advance by r_rstep (lanes past r_rstep * nrow idle)
+        if (lane < r_lanes) {
+            for (int cc = r_col; cc < sg.xw; cc += 32 * sg.chunk_e) {
+                const int pc = cb + cc;
+                const long long col_off = (long long)b0 * (long long)cstride + pc;  // + g planes + pr rows
+                const bool col_ok = (unsigned)pc < (unsigned)W;
+                T *dst = raw + r_row0 * sg.xw + cc;
+                int g = 0, row = r_row0;  // row within plane g
+#pragma unroll 4
+                for (int rowg = r_row0; rowg < n_rrows; rowg += r_rstep) {
+                    while (row >= sg.xrows) { row -= sg.xrows; ++g; }
+                    const int pr = rb + row;
+                    const bool ok = col_ok && (b0 + g) < B && (unsigned)pr < (unsigned)H;
+                    const T *src = ok ? xc + (col_off + (long long)g * (long long)cstride + (long long)pr * W) : x;
+                    if constexpr (sizeof(T) == 4) {
+                        if (sg.chunk_e == 4) cp_async_n<16>(dst, src, ok ? 16 : 0);
+                        else cp_async_n<8>(dst, src, ok ? 8 : 0);
+                    } else {
+                        if (sg.chunk_e == 8) cp_async_n<16>(dst, src, ok ? 16 : 0);
+                        else if (sg.chunk_e == 4) cp_async_n<8>(dst, src, ok ? 8 : 0);
+                        else cp_async_n<4>(dst, src, ok ? 4 : 0);
+                    }
+                    dst += r_rstep * sg.xw;
+                    row += r_rstep;
                 }
             }
         }
         cp_async_commit();
     };
+    // cp.async of unit u's deep tiles (L >= 2).  One commit group.
+    auto issue_deep = [&](int u) {
+        if (!has_deep) return;
+        const int bg = (int)fdiv(fd_tiles, (uint32_t)u), t = u - bg * (int)fd_tiles.d;
+        const int tr = (int)fdiv(fd_tiles_c, (uint32_t)t), tc = t - tr * sg.tiles_c;
+        const int b0 = bg * G;
+        if (lane < d_lanes) {
+            float *dst = dtile + d_row0 * dtw + d_col;
+            const int drb = tr * dth, dc = tc * dtw + d_col;
+            const float *src_col = deepc + (size_t)b0 * cstride1 + dc;
+            int g = 0, row = d_row0;
+            for (int rowg = d_row0; rowg < n_drows; rowg += d_rstep) {
+                while (row >= dth) { row -= dth; ++g; }
+                const int dr = drb + row;
+                const bool ok = (b0 + g) < B && dr < H1 && dc < W1;
+                const float *src = ok ? src_col + (size_t)g * cstride1 + (size_t)dr * W1 : a.deep;
+                if (sg.dchunk_e == 4) cp_async_n<16>(dst, src, ok ? 16 : 0);
+                else cp_async_n<8>(dst, src, ok ? 8 : 0);
+                dst += d_rstep * dtw;
+                row += d_rstep;
+            }
+        }
+        cp_async_commit();
+    };
 
-    if (stage && u_begin < u_end) issue_stage(u_begin, 0);
-    int buf = 0;
-    for (int u = u_begin; u < u_end; ++u, buf ^= 1) {
-        const int bg = fdiv(a.tiles, u), t = u - bg * (int)a.tiles.d;
-        const int tr = fdiv(a.tiles_c, t), tc = t - tr * sg.tiles_c;
+    // Single-buffered: the next unit's copies start as soon as their buffers are free (raw after
+    // the conversion for narrow types, else after the items); the other warps resident on the SM
+    // cover the copy latency.
+    if (u_begin < u_end) {
+        issue_raw(u_begin);
+        issue_deep(u_begin);
+    }
+    for (int u = u_begin; u < u_end; ++u) {
+        const int bg = (int)fdiv(fd_tiles, (uint32_t)u), t = u - bg * (int)fd_tiles.d;
+        const int tr = (int)fdiv(fd_tiles_c, (uint32_t)t), tc = t - tr * sg.tiles_c;
         const int r0 = tr * sg.TH, c0 = tc * sg.TW;
         const int b0 = bg * G;
 
-        // 1. input tiles (fp32 X, zero outside the plane)
-        if (stage) {
-            cp_async_wait_all();
+        // 1. this unit's tiles have landed
+        cp_async_wait_all();
+        __syncthreads();
+        const float *X;
+        if constexpr (kConvert) {
+            const T *raw = reinterpret_cast<const T *>(raw_base);
+            float4 *x4 = reinterpret_cast<float4 *>(xconv);
+            for (int i = lane; i < sg.xbuf / 4; i += 32) x4[i] = cvt4<T>(raw + 4 * i);
             __syncthreads();
-            if (u + 1 < u_end) issue_stage(u + 1, buf ^ 1);
-            if constexpr (kConvert) {
-                const T *raw = reinterpret_cast<const T *>(raw_base + buf * sg.raw_bytes);
-                const int n = sg.TW + 4 * P;
-                for (int g = 0; g < G; ++g) {
-                    int row = 0, col = lane;
-                    while (col >= n) { col -= n; ++row; }
-                    for (; row < sg.xrows;) {
-                        slots[g * pslot + row * sg.xpitch + sg.pad_l + col] =
-                            Act<T>::ld(raw + ((size_t)g * sg.xrows + row) * sg.rpitch + col);
-                        col += 32;
-                        while (col >= n) { col -= n; ++row; }
-                    }
-                }
-                __syncthreads();
-            }
+            if (u + 1 < u_end) issue_raw(u + 1);
+            X = xconv;
         } else {
-            for (int it = lane; it < G * sg.xrows * nchunk; it += 32) {
-                const int g = fdiv(a.xload, it), e = it - g * (int)a.xload.d;
-                const int row = fdiv(a.xchunk, e), k = e - row * nchunk;
-                const int b = b0 + g;
-                const int pr = r0 - 2 * P + row, pc = c0 - 2 * P + 4 * k;
-                float v[4] = {0.f, 0.f, 0.f, 0.f};
-                if (b < a.B && pr >= 0 && pr < H) {
-                    const T *src = x + ((size_t)b * a.C + c) * HW + (size_t)pr * W;
-                    if (a.vec_ld && pc >= 0 && pc + 3 < W && (pc & 3) == 0) {
-                        const float4 f = Act<T>::ld4(src + pc);
-                        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (pc + q >= 0 && pc + q < W) v[q] = Act<T>::ld(src + pc + q);
-                    }
-                }
-                float *X = slots + g * pslot + row * sg.xpitch + sg.pad_l + 4 * k;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) X[q] = v[q];
-            }
-            __syncthreads();
+            X = reinterpret_cast<const float *>(raw_base);
         }
-        const float *xtiles = x_in_raw ? reinterpret_cast<const float *>(raw_base + buf * sg.raw_bytes) : slots;
-        const int xstride = x_in_raw ? sg.xrows * sg.rpitch : pslot;  // floats between planes' X tiles
-        const int yoff = yoff_fixed(x_in_raw, xfl);                    // Y images within a plane slot
 
-        // 2. Haar level 1 of the tile (unnormalised butterflies) -> pair images
-        for (int g = 0; g < G; ++g) {
-            const float *Xg = xtiles + g * xstride + sg.pad_l;
-            float *Yg = slots + g * pslot + yoff;
-            int ya = 0, yb = lane;
-            while (yb >= sg.ycols) { yb -= sg.ycols; ++ya; }
-            for (; ya < sg.yrows;) {
-                const float *X = Xg + (2 * ya) * sg.xpitch + 2 * yb;
-                float p, q, r, s;
-                if constexpr ((P & 1) == 0) {
-                    const float2 t0 = *reinterpret_cast<const float2 *>(X);
-                    const float2 t1 = *reinterpret_cast<const float2 *>(X + sg.xpitch);
-                    p = t0.x; q = t0.y; r = t1.x; s = t1.y;
-                } else {
-                    p = X[0]; q = X[1]; r = X[sg.xpitch]; s = X[sg.xpitch + 1];
+        // 2. Haar level 1 of the tile (unnormalised butterflies) -> pair images; row ya of the
+        //    stacked images comes from X rows 2 ya and 2 ya + 1
+        if (lane < a_lanes) {
+            for (int col = a_col0; col < ycols; col += 32) {
+                const float *xs = X + sg.padx - 2 * P + 2 * col + (2 * a_row0) * sg.xw;
+                float *y0 = pairs + 2 * (a_row0 * sg.ypitch + col);
+#pragma unroll 4
+                for (int ya = a_row0; ya < n_arows; ya += a_rstep) {
+                    // rows (a, b) and (c, d): s = (a+c, b+d), d = (a-c, b-d); LL = s.x + s.y,
+                    // LH = s.x - s.y, HL = d.x + d.y, HH = d.x - d.y
+                    const f2_t t0 = *reinterpret_cast<const f2_t *>(xs);
+                    const f2_t t1 = *reinterpret_cast<const f2_t *>(xs + sg.xw);
+                    const f2_t sv = fadd2(t0, t1), dv = fsub2(t0, t1);
+                    const float s0 = lo2(sv), s1 = hi2(sv), d0 = lo2(dv), d1 = hi2(dv);
+                    *reinterpret_cast<float2 *>(y0) = make_float2(s0 + s1, s0 - s1);
+                    *reinterpret_cast<float2 *>(y0 + G * sg.yimg) = make_float2(d0 + d1, d0 - d1);
+                    xs += 2 * a_rstep * sg.xw;
+                    y0 += 2 * a_rstep * sg.ypitch;
                 }
-                const Quad qd = butterfly(p, q, r, s);
-                float *y0 = Yg + 2 * (ya * sg.ypitch + yb);
-                *reinterpret_cast<float2 *>(y0) = make_float2(qd.ll, qd.lh);
-                *reinterpret_cast<float2 *>(y0 + sg.yimg) = make_float2(qd.hl, qd.hh);
-                yb += 32;
-                while (yb >= sg.ycols) { yb -= sg.ycols; ++ya; }
             }
         }
         __syncthreads();
@@ -306,7 +318,7 @@ __global__ void __launch_bounds__(32) wtconv_shallow_kernel(const ShallowArgs a)
         if (has_item) {
             const int b = b0 + ig;
             const int pr = r0 + kRows * irs, pc = c0 + kCols * ics;  // block origin in the plane
-            const float *dtiles = dtile_base + buf * G * sg.dtile;
+            const float *dt = dtile + d_item;
             // start values of the base accumulators: deep contribution of levels >= 2 (constant over
             // each 2x2 pixel block) + bias, then the closed-form level-1 synthesis, folded in one
             // subband pair at a time: pixel (2i+a, 2q+b) += (LL + (-1)^b LH) + (-1)^a (HL + (-1)^b HH)
@@ -314,22 +326,10 @@ __global__ void __launch_bounds__(32) wtconv_shallow_kernel(const ShallowArgs a)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 float d0 = 0.f, d1 = 0.f;
-                if (a.deep != nullptr) {
-                    if (stage) {
-                        const float2 t2 = *reinterpret_cast<const float2 *>(dtiles + d_item + i * dtw);
-                        d0 = t2.x;
-                        d1 = t2.y;
-                    } else if (b < a.B) {
-                        const int dr = (pr >> 1) + i, dc = pc >> 1;
-                        const float *dp = a.deep + ((size_t)b * a.C + c) * H1 * W1;
-                        if (dr < H1 && dc + 1 < W1) {
-                            const float2 t2 = *reinterpret_cast<const float2 *>(dp + (size_t)dr * W1 + dc);
-                            d0 = t2.x;
-                            d1 = t2.y;
-                        } else if (dr < H1 && dc < W1) {
-                            d0 = dp[(size_t)dr * W1 + dc];
-                        }
-                    }
+                if (has_deep) {
+                    const float2 t2 = *reinterpret_cast<const float2 *>(dt + i * dtw);
+                    d0 = t2.x;
+                    d1 = t2.y;
                 }
                 init[2 * i][0] = init[2 * i + 1][0] = pk2(d0 + bias, d0 + bias);
                 init[2 * i][1] = init[2 * i + 1][1] = pk2(d1 + bias, d1 + bias);
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(32) wtconv_shallow_kernel(const ShallowArgs a)
 #pragma unroll
             for (int pp = 0; pp < 2; ++pp) {
                 f2_t z[4][kColsL];
-                level1_item<K>(slots + y_item + pp * sg.yimg, sg.ypitch, wts + (1 + pp) * WP, z);
+                level1_item<K>(pairs + y_item + pp * G * sg.yimg, sg.ypitch, wts + (1 + pp) * WP, z);
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -348,13 +348,18 @@ __global__ void __launch_bounds__(32) wtconv_shallow_kernel(const ShallowArgs a)
                         init[2 * i + 1][q] = pp == 0 ? fadd2(init[2 * i + 1][q], sv) : fsub2(init[2 * i + 1][q], sv);
                     }
             }
-            const int nrows = b < a.B ? max(0, min(kRows, H - pr)) : 0;
+            const int nrows = b < B ? max(0, min(kRows, H - pr)) : 0;
             const int ncols = max(0, min(kCols, W - pc));
-            T *dst = out + ((size_t)(b < a.B ? b : 0) * a.C + c) * HW + (size_t)pr * W + pc;
-            base_item_store<K, T>(xtiles + ig * xstride + x_item, sg.xpitch, wts, init, dst, W, nrows, ncols, vec_st);
+            T *dst = out + (size_t)(b < B ? b : 0) * cstride + (size_t)c * HW + (size_t)pr * W + pc;
+            base_item_store<K, T>(X + x_item, sg.xw, wts, init, dst, W, nrows, ncols, vec_st);
         }
         __syncthreads();
+        if (u + 1 < u_end) {
+            if constexpr (!kConvert) issue_raw(u + 1);
+            issue_deep(u + 1);
+        }
     }
+    cp_async_wait_all();
 }
 
 template <int K, typename T>

@@ -7,7 +7,7 @@ call raises.
 
 Functions carry the C names: ``wtconv_forward``, ``wtconv_backward_input``,
 ``wtconv_backward_weights``, ``wtconv_backward``, ``wtconv_backward_weights_noalloc``,
-``wtconv_workspace_size``,
+``wtconv_workspace_size``, ``wtconv_launch_count``,
 ``wtconv_strerror``, ``wtconv_version``.  ``WTConvFunction`` wraps forward and the fused
 backward as a ``torch.autograd.Function``.
 """
@@ -29,7 +29,7 @@ DTYPE_CODE = {v: k for k, v in TORCH_DTYPE.items()}
 
 EXPORTED = ("wtconv_version", "wtconv_strerror", "wtconv_workspace_size", "wtconv_forward",
             "wtconv_backward_input", "wtconv_backward_weights", "wtconv_backward",
-            "wtconv_backward_weights_noalloc")
+            "wtconv_backward_weights_noalloc", "wtconv_launch_count")
 
 _lib = None
 
@@ -64,6 +64,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.wtconv_strerror.argtypes = [i]
     lib.wtconv_workspace_size.restype = sz
     lib.wtconv_workspace_size.argtypes = [i] * 8
+    lib.wtconv_launch_count.restype = i
+    lib.wtconv_launch_count.argtypes = [i] * 8
     shape = [i] * 7
     params = [fp] * 5
     lib.wtconv_forward.restype = i
@@ -90,6 +92,10 @@ def wtconv_strerror(status: int) -> str:
 
 def wtconv_workspace_size(op: int, B: int, C: int, H: int, W: int, L: int, k: int, dtype: int) -> int:
     return load().wtconv_workspace_size(op, B, C, H, W, L, k, dtype)
+
+
+def wtconv_launch_count(op: int, B: int, C: int, H: int, W: int, L: int, k: int, dtype: int) -> int:
+    return load().wtconv_launch_count(op, B, C, H, W, L, k, dtype)
 
 
 # ------------------------------------------------------------------------------- marshalling

@@ -70,6 +70,11 @@ def test_backward_entry_points_reject_invalid_arguments():
                    None) == W.ERR_INVALID_ARG
 
 
+def test_launch_count_of_invalid_shape_is_zero():
+    assert W.wtconv_launch_count(W.OP_BACKWARD, 2, 3, 12, 16, 3, 5, 0) == 0
+    assert W.wtconv_launch_count(W.OP_FORWARD, 2, 3, 16, 16, 2, 4, 0) == 0
+
+
 def test_workspace_size_of_invalid_shape_is_zero():
     assert W.wtconv_workspace_size(W.OP_BACKWARD, 2, 3, 12, 16, 3, 5, 0) == 0
     assert W.wtconv_workspace_size(W.OP_FORWARD, 2, 3, 16, 16, 0, 5, 0) == 0

@@ -2,6 +2,9 @@
 
 Bar: max|gpu - oracle| <= 1e-5 max|oracle| for fp32 activations, <= 2e-2 max|oracle| for bf16 /
 fp16, for every output tensor (y, dx and each parameter gradient)."""
+import contextlib
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -14,18 +17,38 @@ from parity import GRADS, PARAMS, TOL, assert_close, gpu_backward, gpu_backward_
 pytestmark = pytest.mark.gpu
 
 
+@contextlib.contextmanager
+def fwd_path(path: str):
+    """WTCONV_FWD_PATH for the calls inside (the library reads it at every call)."""
+    old = os.environ.get("WTCONV_FWD_PATH")
+    os.environ["WTCONV_FWD_PATH"] = path
+    try:
+        yield
+    finally:
+        if old is None:
+            del os.environ["WTCONV_FWD_PATH"]
+        else:
+            os.environ["WTCONV_FWD_PATH"] = old
+
+
 def check_layer(shape: LayerShape, inputs: dict, split: bool = True):
+    """Forward, fused backward and (if `split`) the separate backward entry points against the
+    oracle, on the default kernels and again with the tiled forward / input-gradient kernels
+    forced (where the whole-plane kernel would be chosen by default)."""
     tol = TOL[shape.dtype]
     d = to_device(inputs)
-    y = gpu_forward(d)
-    dx, g = gpu_backward(d)
-    torch.cuda.synchronize()
     y_ref = oracle.forward(inputs["x"], inputs)
     g_ref = oracle.backward(inputs["x"], inputs["dy"], inputs)
-    assert_close("y", np64(y), y_ref, tol)
-    assert_close("dx", np64(dx), g_ref["dx"], tol)
-    for n in GRADS:
-        assert_close(n, np64(g[n]), g_ref[n], tol)
+    for path in ("default", "tiles"):
+        with fwd_path(path):
+            y = gpu_forward(d)
+            dx, g = gpu_backward(d)
+            torch.cuda.synchronize()
+        assert_close(f"y [{path}]", np64(y), y_ref, tol)
+        assert_close(f"dx [{path}]", np64(dx), g_ref["dx"], tol)
+        if path == "default":
+            for n in GRADS:
+                assert_close(n, np64(g[n]), g_ref[n], tol)
     if split:
         dx2, g2 = gpu_backward_split(d)
         torch.cuda.synchronize()
@@ -56,6 +79,8 @@ SWEEP = [
     (17, 3, 8, 8, 1, 5, "bf16"),
     (33, 2, 4, 4, 2, 5, "f32"),
     (2, 2, 96, 64, 5, 5, "bf16"),
+    (2, 3, 6, 130, 1, 5, "f32"),     # rows of more than 32 eight-byte copy chunks
+    (2, 2, 4, 98, 1, 3, "bf16"),
 ]
 
 
@@ -90,7 +115,8 @@ def test_input_gradient_is_forward_with_rotated_kernels():
     assert_close("dx vs rotated forward", np64(dx), np64(y), 1e-6)
 
 
-def test_outputs_stay_in_bounds_and_inputs_untouched():
+@pytest.mark.parametrize("path", ["default", "tiles"])
+def test_outputs_stay_in_bounds_and_inputs_untouched(path):
     """Canary words around every output; inputs byte-identical after the calls."""
     shape = LayerShape(3, 5, 24, 16, 3, 5, "bf16")
     inputs = make_inputs(shape, seed=9)
@@ -102,7 +128,8 @@ def test_outputs_stay_in_bounds_and_inputs_untouched():
     dxbuf = torch.full((n + 2 * pad,), 7.0, dtype=torch.bfloat16, device="cuda")
     y = ybuf[pad:pad + n].view(shape.B, shape.C, shape.H, shape.W)
     dx = dxbuf[pad:pad + n].view(shape.B, shape.C, shape.H, shape.W)
-    W.wtconv_forward(d["x"], *[d[p] for p in PARAMS], y=y)
+    with fwd_path(path):
+        W.wtconv_forward(d["x"], *[d[p] for p in PARAMS], y=y)
     gbufs = {}
     grads = {}
     for gname, p in zip(GRADS, PARAMS):
@@ -110,7 +137,8 @@ def test_outputs_stay_in_bounds_and_inputs_untouched():
         buf = torch.full((m + 2 * 64,), 7.0, device="cuda")
         gbufs[gname] = buf
         grads[gname] = buf[64:64 + m].view_as(d[p])
-    W.wtconv_backward(d["x"], d["dy"], *[d[p] for p in PARAMS], dx=dx, grads=grads)
+    with fwd_path(path):
+        W.wtconv_backward(d["x"], d["dy"], *[d[p] for p in PARAMS], dx=dx, grads=grads)
     torch.cuda.synchronize()
     for buf in (ybuf, dxbuf):
         assert torch.all(buf[:pad] == 7.0) and torch.all(buf[pad + n:] == 7.0)
