@@ -66,7 +66,8 @@ enum wtconv_status {
     WTCONV_ERR_WORKSPACE = 3,   /* workspace smaller than wtconv_workspace_size() */
     WTCONV_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
     WTCONV_ERR_INJECTED = 5,    /* WTCONV_INJECT_FAULT is set */
-    WTCONV_ERR_SCRATCH_LIMIT = 6 /* shape needs more than WTCONV_NOALLOC_SCRATCH_BYTES of scratch */
+    WTCONV_ERR_SCRATCH_LIMIT = 6, /* shape needs more than WTCONV_NOALLOC_SCRATCH_BYTES of scratch */
+    WTCONV_ERR_DEVICE_TIMEOUT = 7 /* a kernel's bounded wait gave up (wtconv_device_status) */
 };
 
 /* Operation selector for wtconv_workspace_size. */
@@ -84,6 +85,14 @@ int wtconv_version(void);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char *wtconv_strerror(int status);
+
+/* Device-side status of the calls made so far on the current device.  Kernels that hand work
+ * between their warps wait on shared-memory barriers for a bounded number of tries; a wait that
+ * gives up (never expected: it would mean a broken handshake, not a slow GPU) raises a sticky
+ * per-device flag and ends its warp, leaving that call's outputs incomplete.  This call
+ * synchronises the device, returns WTCONV_ERR_DEVICE_TIMEOUT if the flag was raised (and clears
+ * it), WTCONV_ERR_CUDA if the synchronisation or the read failed, else WTCONV_OK. */
+int wtconv_device_status(void);
 
 /* Bytes of device workspace `op` needs for this shape on the current device (0 if none).
  * FORWARD and BACKWARD_INPUT need, for L >= 2, one fp32 per level-1 position

@@ -7,6 +7,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -305,6 +306,7 @@ SPlan plan_shallow_uncached(int B, int C, int H, int W, int L, int k, int dtype)
     const bool convert = eb != 4, deep = L >= 2;
     a.sg = make_shallow_geo(H, W, k, TH, TW, G, eb, chunk_e, dchunk_e);
     p.smem = shallow_smem_bytes(a.sg, k, convert, deep);
+    // planes per unit: as many as fill the warp's lanes and fit in shared memory
     while (G > 1 && p.smem + kStaticSmemMargin > (size_t)kMaxSmem) {
         --G;
         a.sg = make_shallow_geo(H, W, k, TH, TW, G, eb, chunk_e, dchunk_e);
@@ -316,11 +318,17 @@ SPlan plan_shallow_uncached(int B, int C, int H, int W, int L, int k, int dtype)
     if (sms <= 0 || occ <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
     const int tiles = a.sg.tiles_r * a.sg.tiles_c;
     a.units = ((B + G - 1) / G) * tiles;
-    const long long target = 4LL * sms * occ;  // about four waves of resident CTAs
-    long long nb = (target + C - 1) / C;
-    if (nb < 1) nb = 1;
-    if (nb > a.units) nb = a.units;
-    a.units_per_cta = (int)((a.units + nb - 1) / nb);
+    // CTAs per channel: minimise (waves of resident CTAs) x (units per CTA)
+    const long long slots = (long long)sms * occ;
+    long long best_nb = 1, best_cost = -1;
+    const long long max_nb = std::max(1, a.units);
+    for (long long nb = 1; nb <= max_nb; ++nb) {
+        const long long upc = (a.units + nb - 1) / nb;
+        const long long waves = (C * nb + slots - 1) / slots;
+        const long long cost = waves * upc;
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_nb = nb; }
+    }
+    a.units_per_cta = (int)((a.units + best_nb - 1) / best_nb);
     a.nb = (a.units + a.units_per_cta - 1) / a.units_per_cta;
     a.tiles = make_fastdiv(tiles);
     a.tiles_c = make_fastdiv(a.sg.tiles_c);
@@ -429,6 +437,24 @@ bool params_ok(const float *base_w, const float *base_bias, const float *base_sc
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? WTCONV_OK : WTCONV_ERR_CUDA; }
 
+// Sticky flag raised by a kernel wait that gave up; read and cleared by wtconv_device_status.
+__device__ int g_wait_timeout;
+
+// Device address of g_wait_timeout on the current device (looked up once per device), or nullptr.
+int *timeout_flag() {
+    static std::mutex mu;
+    static std::map<int, int *> addr;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = addr.find(dev);
+    if (it != addr.end()) return it->second;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_wait_timeout) != cudaSuccess || p == nullptr) return nullptr;
+    addr.emplace(dev, static_cast<int *>(p));
+    return static_cast<int *>(p);
+}
+
 // Scratch of wtconv_backward_weights_noalloc: the weight-gradient partials of one call, in device
 // memory that comes with the library's module instead of from an allocator.
 __device__ __align__(256) unsigned char g_noalloc_scratch[WTCONV_NOALLOC_SCRATCH_BYTES];
@@ -464,6 +490,7 @@ const char *wtconv_strerror(int status) {
     case WTCONV_ERR_CUDA: return "CUDA runtime error";
     case WTCONV_ERR_INJECTED: return "fault injected (WTCONV_INJECT_FAULT)";
     case WTCONV_ERR_SCRATCH_LIMIT: return "shape needs more scratch than the no-alloc entry point's fixed array";
+    case WTCONV_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait gave up (device status flag)";
     default: return "unknown status";
     }
 }
@@ -479,6 +506,16 @@ size_t wtconv_workspace_size(int op, int B, int C, int H, int W, int L, int k, i
         bytes += p.workspace;
     }
     return bytes;
+}
+
+int wtconv_device_status(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return WTCONV_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_wait_timeout, sizeof(int)) != cudaSuccess) return WTCONV_ERR_CUDA;
+    if (v == 0) return WTCONV_OK;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_wait_timeout, &zero, sizeof(int)) != cudaSuccess) return WTCONV_ERR_CUDA;
+    return WTCONV_ERR_DEVICE_TIMEOUT;
 }
 
 int wtconv_launch_count(int op, int B, int C, int H, int W, int L, int k, int dtype) {
@@ -497,6 +534,59 @@ int wtconv_launch_count(int op, int B, int C, int H, int W, int L, int k, int dt
         n += pw.dw_pyramid ? 2 * L + 2 : 2;
     }
     return n;
+}
+
+// ------------------------------------------------------------------ bulk tensor copies (TMA)
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once (nullptr if unavailable).
+EncodeTiledFn encode_tiled() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Tensor map of a contiguous [B][C][H][W] tensor with a box of bw x bh x 1 x bb elements
+// (zero fill outside).  False if the driver refuses it.
+bool encode_map(CUtensorMap *m, CUtensorMapDataType dt, int eb, const void *base, int W, int H, int C, int B,
+                int bw, int bh, int bb) {
+    EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)C, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)W * eb, (cuuint64_t)H * W * eb, (cuuint64_t)C * H * W * eb};
+    const cuuint32_t box[4] = {(cuuint32_t)bw, (cuuint32_t)bh, 1u, (cuuint32_t)bb};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Whether the shallow kernel's tiles can move as bulk tensor copies: every row, box row and box
+// origin 16-byte aligned, box extents within the hardware limit of 256.
+bool shallow_tma_x_ok(const ShallowArgs &a, int eb) {
+    const ShallowGeo &g = a.sg;
+    return ((size_t)a.W * eb) % 16 == 0 && ((size_t)g.xw * eb) % 16 == 0 && ((size_t)g.padx * eb) % 16 == 0 &&
+           ((size_t)g.TW * eb) % 16 == 0 && g.xw <= 256 && g.xrows <= 256 && g.G <= 256;
+}
+bool shallow_tma_d_ok(const ShallowArgs &a) {
+    const ShallowGeo &g = a.sg;
+    return a.L >= 2 && ((a.W / 2) % 4) == 0 && ((g.TW / 2) % 4) == 0 && g.TW / 2 <= 256 && g.TH / 2 <= 256;
+}
+
+CUtensorMapDataType tma_dtype(int dtype) {
+    return dtype == WTCONV_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                               : dtype == WTCONV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
 // The layer's linear operator on `src` (x -> y, or dy -> dx with rotated kernels and no bias):
@@ -543,6 +633,14 @@ static int run_operator(int B, int C, int H, int W, int L, int k, int dtype, con
     a.wavelet_w = wavelet_w; a.wavelet_scale = wavelet_scale;
     a.flip = flip ? 1 : 0;
     a.with_bias = flip ? 0 : 1;
+    a.timeout = timeout_flag();
+    if (a.timeout == nullptr) return WTCONV_ERR_CUDA;
+    const int eb = elem_bytes(dtype);
+    a.tma_x = shallow_tma_x_ok(a, eb) &&
+              encode_map(&a.tmap_x, tma_dtype(dtype), eb, src, W, H, C, B, a.sg.xw, a.sg.xrows, a.sg.G);
+    a.tma_d = deep != nullptr && shallow_tma_d_ok(a) &&
+              encode_map(&a.tmap_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, deep, W / 2, H / 2, C, B, a.sg.TW / 2,
+                         a.sg.TH / 2, a.sg.G);
     return cuda_status(launch_shallow(a, dtype, ps.smem, s));
 }
 

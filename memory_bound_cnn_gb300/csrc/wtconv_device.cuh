@@ -149,6 +149,69 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src)
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// every committed group except the most recent one has completed
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// ------------------------------------------------------------------------------ mbarriers
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(bar)), "r"(count)
+                 : "memory");
+}
+// arrive (release semantics at CTA scope: the caller's earlier shared-memory writes, and those of
+// the threads it synchronised with, are visible to a thread whose wait observes the phase)
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"((uint32_t)__cvta_generic_to_shared(bar))
+                 : "memory");
+}
+// Make an mbarrier's initialisation visible to the asynchronous (TMA) proxy.
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+// Arrive on `bar` and add `bytes` to the transaction count its current phase waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+// Bulk tensor copy (TMA) of one box of a 4-D tensor map into shared memory; completion is
+// counted in bytes on `bar`.  Coordinates are element indices, innermost first; parts of the box
+// outside the tensor are zero-filled.
+__device__ __forceinline__ void tma_load_4d(void *smem_dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"((uint32_t)__cvta_generic_to_shared(bar))
+        : "memory");
+}
+
+// One arrival on `bar`, made by the hardware once every cp.async this thread issued before has
+// completed (the barrier's expected count must include it: .noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"((uint32_t)__cvta_generic_to_shared(bar))
+                 : "memory");
+}
+// Wait until the phase with parity `parity` has completed.  Bounded: each try suspends the
+// thread for at most kWaitHintNs; after kMaxWaitTries unsuccessful tries (about half a second)
+// it raises *timeout (if given) and returns false.
+constexpr uint32_t kMaxWaitTries = 1u << 19;
+constexpr uint32_t kWaitHintNs = 1000;
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *timeout) {
+    const uint32_t addr = (uint32_t)__cvta_generic_to_shared(bar);
+    for (uint32_t i = 0; i < kMaxWaitTries; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(addr), "r"(parity), "n"(kWaitHintNs)
+            : "memory");
+        if (done) return true;
+    }
+    if (timeout) atomicExch(timeout, 1);
+    return false;
+}
 
 // Copy the raw planes b0 .. b0+G-1 of channel c (those that exist) to the staging area.
 template <typename T>

@@ -2,6 +2,7 @@
 // units (wtconv_fwd.cu, wtconv_bwd.cu).  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -14,6 +15,7 @@ constexpr int kMaxSig = 1 + 4 * kMaxLevels;  // base kernel + 4 subbands per lev
 constexpr int kRows = 8;        // output rows of one sliding-window conv item
 constexpr int kCols = 4;        // output columns of one conv item
 constexpr int kMaxSmem = 227 * 1024;
+constexpr int kSmemPerSM = 228 * 1024;  // shared memory of one SM (all resident CTAs)
 
 __host__ __device__ constexpr int round_up(int a, int m) { return (a + m - 1) / m * m; }
 __host__ __device__ constexpr int ceil_div(int a, int m) { return (a + m - 1) / m; }
@@ -201,6 +203,11 @@ struct ShallowArgs {
     // units per plane group (tiles) and tile columns; raw-tile chunks per row and rows per plane;
     // deep-tile chunks per row and rows per plane; level-1 positions per row; X 4-float groups per row
     FastDiv tiles, tiles_c, rchunks_row, xrows, dchunks_row, drows, ycols, xw4;
+    // TMA: when set, one lane loads the whole input tile (box xw x xrows x 1 x G of the 4-D
+    // tensor W, H, C, B) and / or the deep tile with one bulk tensor copy each; zero fill outside
+    int tma_x, tma_d;
+    int *timeout;         // sticky device flag raised by a bounded wait that gave up
+    CUtensorMap tmap_x, tmap_d;
 };
 
 size_t shallow_smem_bytes(const ShallowGeo &sg, int K, bool convert, bool deep);

@@ -24,13 +24,14 @@
 
 namespace wtconv {
 
-// Shared memory: the raw tile buffer (type T; for fp32 it is X itself), the X buffer (narrow
-// types only), the pair images, the deep tile (L >= 2), then the kernels.
+// Shared memory: the raw tile buffer (type T; for fp32 it is X itself) and the deep tile (L >= 2),
+// each starting 128-byte aligned (bulk tensor copies land there), then the X buffer (narrow types
+// only), the pair images and the kernels.
 size_t shallow_smem_bytes(const ShallowGeo &sg, int K, bool convert, bool deep) {
-    size_t bytes = (size_t)sg.raw_bytes;
+    size_t bytes = ((size_t)sg.raw_bytes + 127) / 128 * 128;
+    if (deep) bytes += ((size_t)sg.G * sg.dtile * sizeof(float) + 127) / 128 * 128;
     if (convert) bytes += (size_t)sg.xbuf * sizeof(float);
     bytes += (size_t)sg.G * sg.pslot * sizeof(float);
-    if (deep) bytes += (size_t)sg.G * sg.dtile * sizeof(float);
     return bytes + (size_t)3 * wpairs(K) * sizeof(f2_t);
 }
 
@@ -126,21 +127,30 @@ __device__ __forceinline__ float4 cvt4(const T *p) {
 }
 
 template <int K, typename T>
-__global__ void __launch_bounds__(32) wtconv_shallow_kernel(const ShallowArgs a) {
+__global__ void __launch_bounds__(32, (K <= 5 ? 16 : 8)) wtconv_shallow_kernel(const __grid_constant__ ShallowArgs a) {
     constexpr int P = K / 2, WP = wpairs(K);
     constexpr bool kConvert = sizeof(T) != 4;  // narrow inputs are converted into an fp32 X tile
-    extern __shared__ __align__(16) float smem[];
+    extern __shared__ __align__(128) float smem[];
+    __shared__ __align__(8) uint64_t bar_x, bar_d;  // bulk tensor copies of the input / deep tiles
     const ShallowGeo sg = a.sg;
     const int lane = threadIdx.x;
     const int c = blockIdx.x % a.C;
     const int nbi = blockIdx.x / a.C;
     const int G = sg.G;
     const bool has_deep = a.deep != nullptr;
+    // bulk tensor copies land at 128-byte aligned shared addresses (else the cp.async path runs)
+    const bool smem128 = ((uint32_t)__cvta_generic_to_shared(smem) & 127u) == 0;
+    const bool tma_x = a.tma_x != 0 && smem128, tma_d = has_deep && a.tma_d != 0 && smem128;
     char *raw_base = reinterpret_cast<char *>(smem);
-    float *xconv = reinterpret_cast<float *>(raw_base + (size_t)sg.raw_bytes);  // narrow types only
+    float *dtile = reinterpret_cast<float *>(raw_base + ((size_t)sg.raw_bytes + 127) / 128 * 128);
+    float *xconv = dtile + (has_deep ? (G * sg.dtile + 31) / 32 * 32 : 0);  // narrow types only
     float *pairs = xconv + (kConvert ? sg.xbuf : 0);
-    float *dtile = pairs + G * sg.pslot;
-    f2_t *wts = reinterpret_cast<f2_t *>(dtile + (has_deep ? G * sg.dtile : 0));
+    f2_t *wts = reinterpret_cast<f2_t *>(pairs + G * sg.pslot);
+    if (lane == 0) {
+        mbar_init(&bar_x, 1);
+        mbar_init(&bar_d, 1);
+        mbar_fence_init();
+    }
 
     // kernels, scales folded in: 0 base {w, w}; 1, 2 level-1 subband pairs {w_LL, w_LH}, {w_HL, w_HH}
     {
@@ -207,6 +217,13 @@ __global__ void __launch_bounds__(32) wtconv_shallow_kernel(const ShallowArgs a)
         const int tr = (int)fdiv(fd_tiles_c, (uint32_t)t), tc = t - tr * sg.tiles_c;
         const int b0 = bg * G;
         const int rb = tr * sg.TH - 2 * P, cb = tc * sg.TW - sg.padx;
+        if (tma_x) {  // one bulk tensor copy of the whole box; zero fill outside the tensor
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bar_x, (uint32_t)(G * sg.xrows * sg.xw * (int)sizeof(T)));
+                tma_load_4d(raw_base, &a.tmap_x, cb, rb, c, b0, &bar_x);
+            }
+            return;
+        }
         T *raw = reinterpret_cast<T *>(raw_base);
         // lane -> fixed chunk column (several columns only for rows of more than 32 chunks); rows
         // advance by r_rstep (lanes past r_rstep * nrow idle)
@@ -244,6 +261,13 @@ __global__ void __launch_bounds__(32) wtconv_shallow_kernel(const ShallowArgs a)
         const int bg = (int)fdiv(fd_tiles, (uint32_t)u), t = u - bg * (int)fd_tiles.d;
         const int tr = (int)fdiv(fd_tiles_c, (uint32_t)t), tc = t - tr * sg.tiles_c;
         const int b0 = bg * G;
+        if (tma_d) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bar_d, (uint32_t)(G * dth * dtw * (int)sizeof(float)));
+                tma_load_4d(dtile, &a.tmap_d, tc * dtw, tr * dth, c, b0, &bar_d);
+            }
+            return;
+        }
         if (lane < d_lanes) {
             float *dst = dtile + d_row0 * dtw + d_col;
             const int drb = tr * dth, dc = tc * dtw + d_col;
@@ -277,13 +301,26 @@ __global__ void __launch_bounds__(32) wtconv_shallow_kernel(const ShallowArgs a)
         const int b0 = bg * G;
 
         // 1. this unit's tiles have landed
+        const uint32_t parity = (uint32_t)(u - u_begin) & 1;
         cp_async_wait_all();
+        if (tma_x && !mbar_wait(&bar_x, parity, a.timeout)) break;
+        if (tma_d && !mbar_wait(&bar_d, parity, a.timeout)) break;
         __syncthreads();
         const float *X;
         if constexpr (kConvert) {
-            const T *raw = reinterpret_cast<const T *>(raw_base);
+            // raw -> X in batches of 4 groups per lane: loads first, then the stores (both are
+            // shared memory, so an interleaved sequence would serialise on its latency)
+            const uint2 *raw = reinterpret_cast<const uint2 *>(raw_base);
             float4 *x4 = reinterpret_cast<float4 *>(xconv);
-            for (int i = lane; i < sg.xbuf / 4; i += 32) x4[i] = cvt4<T>(raw + 4 * i);
+            const int n4 = sg.xbuf / 4;
+            for (int i = lane; i < n4; i += 4 * 32) {
+                uint2 v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[q] = raw[i + q * 32 < n4 ? i + q * 32 : i];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (i + q * 32 < n4) x4[i + q * 32] = cvt4<T>(reinterpret_cast<const T *>(&v[q]));
+            }
             __syncthreads();
             if (u + 1 < u_end) issue_raw(u + 1);
             X = xconv;
@@ -297,18 +334,33 @@ __global__ void __launch_bounds__(32) wtconv_shallow_kernel(const ShallowArgs a)
             for (int col = a_col0; col < ycols; col += 32) {
                 const float *xs = X + sg.padx - 2 * P + 2 * col + (2 * a_row0) * sg.xw;
                 float *y0 = pairs + 2 * (a_row0 * sg.ypitch + col);
-#pragma unroll 4
-                for (int ya = a_row0; ya < n_arows; ya += a_rstep) {
-                    // rows (a, b) and (c, d): s = (a+c, b+d), d = (a-c, b-d); LL = s.x + s.y,
-                    // LH = s.x - s.y, HL = d.x + d.y, HH = d.x - d.y
-                    const f2_t t0 = *reinterpret_cast<const f2_t *>(xs);
-                    const f2_t t1 = *reinterpret_cast<const f2_t *>(xs + sg.xw);
-                    const f2_t sv = fadd2(t0, t1), dv = fsub2(t0, t1);
-                    const float s0 = lo2(sv), s1 = hi2(sv), d0 = lo2(dv), d1 = hi2(dv);
-                    *reinterpret_cast<float2 *>(y0) = make_float2(s0 + s1, s0 - s1);
-                    *reinterpret_cast<float2 *>(y0 + G * sg.yimg) = make_float2(d0 + d1, d0 - d1);
-                    xs += 2 * a_rstep * sg.xw;
-                    y0 += 2 * a_rstep * sg.ypitch;
+                // batches of kBatch positions: all loads first, then the butterflies and the
+                // stores (X and the pair images are both shared memory, so an interleaved
+                // load / store sequence would serialise on the shared-memory latency)
+                constexpr int kBatch = 4;
+                for (int ya = a_row0; ya < n_arows; ya += kBatch * a_rstep) {
+                    f2_t t0[kBatch], t1[kBatch];
+#pragma unroll
+                    for (int q = 0; q < kBatch; ++q) {
+                        const bool in = ya + q * a_rstep < n_arows;
+                        const float *xq = xs + (in ? 2 * q * a_rstep * sg.xw : 0);
+                        t0[q] = *reinterpret_cast<const f2_t *>(xq);
+                        t1[q] = *reinterpret_cast<const f2_t *>(xq + sg.xw);
+                    }
+#pragma unroll
+                    for (int q = 0; q < kBatch; ++q) {
+                        if (ya + q * a_rstep < n_arows) {
+                            // rows (a, b) and (c, d): s = (a+c, b+d), d = (a-c, b-d);
+                            // LL = s.x + s.y, LH = s.x - s.y, HL = d.x + d.y, HH = d.x - d.y
+                            const f2_t sv = fadd2(t0[q], t1[q]), dv = fsub2(t0[q], t1[q]);
+                            const float s0 = lo2(sv), s1 = hi2(sv), d0 = lo2(dv), d1 = hi2(dv);
+                            float *yq = y0 + 2 * q * a_rstep * sg.ypitch;
+                            *reinterpret_cast<float2 *>(yq) = make_float2(s0 + s1, s0 - s1);
+                            *reinterpret_cast<float2 *>(yq + G * sg.yimg) = make_float2(d0 + d1, d0 - d1);
+                        }
+                    }
+                    xs += 2 * kBatch * a_rstep * sg.xw;
+                    y0 += 2 * kBatch * a_rstep * sg.ypitch;
                 }
             }
         }

@@ -7,7 +7,7 @@ call raises.
 
 Functions carry the C names: ``wtconv_forward``, ``wtconv_backward_input``,
 ``wtconv_backward_weights``, ``wtconv_backward``, ``wtconv_backward_weights_noalloc``,
-``wtconv_workspace_size``, ``wtconv_launch_count``,
+``wtconv_workspace_size``, ``wtconv_launch_count``, ``wtconv_device_status``,
 ``wtconv_strerror``, ``wtconv_version``.  ``WTConvFunction`` wraps forward and the fused
 backward as a ``torch.autograd.Function``.
 """
@@ -22,14 +22,15 @@ from . import _build
 
 F32, BF16, F16 = 0, 1, 2
 OP_FORWARD, OP_BACKWARD_INPUT, OP_BACKWARD_WEIGHTS, OP_BACKWARD = 0, 1, 2, 3
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_INJECTED, ERR_SCRATCH_LIMIT = range(7)
+(OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_INJECTED, ERR_SCRATCH_LIMIT,
+ ERR_DEVICE_TIMEOUT) = range(8)
 NOALLOC_SCRATCH_BYTES = 4 << 20  # WTCONV_NOALLOC_SCRATCH_BYTES
 TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16, F16: torch.float16}
 DTYPE_CODE = {v: k for k, v in TORCH_DTYPE.items()}
 
 EXPORTED = ("wtconv_version", "wtconv_strerror", "wtconv_workspace_size", "wtconv_forward",
             "wtconv_backward_input", "wtconv_backward_weights", "wtconv_backward",
-            "wtconv_backward_weights_noalloc", "wtconv_launch_count")
+            "wtconv_backward_weights_noalloc", "wtconv_launch_count", "wtconv_device_status")
 
 _lib = None
 
@@ -64,6 +65,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.wtconv_strerror.argtypes = [i]
     lib.wtconv_workspace_size.restype = sz
     lib.wtconv_workspace_size.argtypes = [i] * 8
+    lib.wtconv_device_status.restype = i
+    lib.wtconv_device_status.argtypes = []
     lib.wtconv_launch_count.restype = i
     lib.wtconv_launch_count.argtypes = [i] * 8
     shape = [i] * 7
@@ -92,6 +95,11 @@ def wtconv_strerror(status: int) -> str:
 
 def wtconv_workspace_size(op: int, B: int, C: int, H: int, W: int, L: int, k: int, dtype: int) -> int:
     return load().wtconv_workspace_size(op, B, C, H, W, L, k, dtype)
+
+
+def wtconv_device_status() -> int:
+    """Synchronise the device; WTCONV_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up."""
+    return load().wtconv_device_status()
 
 
 def wtconv_launch_count(op: int, B: int, C: int, H: int, W: int, L: int, k: int, dtype: int) -> int:

@@ -31,7 +31,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_version_and_strerror():
     assert W.wtconv_version() >= 100
-    for s in range(7):
+    for s in range(8):
         assert isinstance(W.wtconv_strerror(s), str) and W.wtconv_strerror(s)
     assert "unknown" in W.wtconv_strerror(99)
 
