@@ -41,6 +41,10 @@
  *   - The forward and the input gradient run one whole-plane kernel where a plane's Haar pyramid
  *     fits in shared memory, else two tiled kernels.  WTCONV_FWD_PATH=tiles selects the tiled
  *     kernels for every shape (same results within fp32 rounding).
+ *   - The weight gradients run a whole-plane kernel where both planes' pyramids fit in shared
+ *     memory, else tiled kernels (tiles with bulk tensor copies, levels >= 2 on their pyramids in
+ *     the workspace), else workspace pyramids for every level.  WTCONV_DW_PATH=tiles or =pyramid
+ *     selects those paths where they apply (same results within fp32 rounding).
  *   - Setting the environment variable WTCONV_INJECT_FAULT=1 makes every compute entry point
  *     return WTCONV_ERR_INJECTED before launching anything (host-side fault injection).
  */

@@ -198,7 +198,7 @@ Plan plan_forward_uncached(int B, int C, int H, int W, int L, int k, int dtype) 
 }
 
 // Weight-gradient kernel: fewer, longer-lived CTAs keep the per-CTA partials small.
-Plan plan_dw_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
+Plan plan_dw_uncached(int B, int C, int H, int W, int L, int k, int dtype, bool force_pyramid) {
     Plan p;
     LayerArgs &a = p.a;
     a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
@@ -206,7 +206,7 @@ Plan plan_dw_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
     set_io_modes(a, dtype);
     const int sms = device_sms();
     if (sms <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
-    if (!choose_launch(a, dtype, dw_smem_bytes, dw_balance, occupancy_dw, &p.smem)) {
+    if (force_pyramid || !choose_launch(a, dtype, dw_smem_bytes, dw_balance, occupancy_dw, &p.smem)) {
         // planes too large for shared memory: pyramids in the workspace, tiled correlations
         p.dw_pyramid = 1;
         const long long units0 = (long long)B * ((H + 15) / 16) * ((W + 63) / 64);
@@ -214,7 +214,7 @@ Plan plan_dw_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
         if (nb > units0) nb = units0;
         if (nb < 1) nb = 1;
         a.nb = (int)nb;
-        p.workspace = dw_pyramid_bytes(B, C, H, W, L) +
+        p.workspace = dw_pyramid_bytes(B, C, H, W, L, 1) +
                       ((size_t)a.nb * C * (1 + 4 * L) * (k * k + 1) * sizeof(float) + 255) / 256 * 256;
         return p;
     }
@@ -367,7 +367,8 @@ Plan cached_plan(int kind, int B, int C, int H, int W, int L, int k, int dtype) 
         if (it != cache.end()) return it->second;
     }
     Plan p = kind == 0   ? plan_forward_uncached(B, C, H, W, L, k, dtype)
-             : kind == 1 ? plan_dw_uncached(B, C, H, W, L, k, dtype)
+             : kind == 1 ? plan_dw_uncached(B, C, H, W, L, k, dtype, false)
+             : kind == 5 ? plan_dw_uncached(B, C, H, W, L, k, dtype, true)
                          : plan_deep_uncached(B, C, H, W, L, k, dtype);
     const char *verbose = getenv("WTCONV_VERBOSE");
     if (verbose && verbose[0] == '1')
@@ -421,6 +422,174 @@ SPlan plan_shallow(int B, int C, int H, int W, int L, int k, int dtype) {
 
 Plan plan_dw(int B, int C, int H, int W, int L, int k, int dtype) {
     return cached_plan(1, B, C, H, W, L, k, dtype);
+}
+
+Plan plan_dw_pyramid_only(int B, int C, int H, int W, int L, int k, int dtype) {
+    return cached_plan(5, B, C, H, W, L, k, dtype);
+}
+
+// ------------------------------------------------------------------ bulk tensor copies (TMA)
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once (nullptr if unavailable).
+EncodeTiledFn encode_tiled() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Tensor map of a contiguous [B][C][H][W] tensor with a box of bw x bh x 1 x bb elements
+// (zero fill outside).  False if the driver refuses it.
+bool encode_map(CUtensorMap *m, CUtensorMapDataType dt, int eb, const void *base, int W, int H, int C, int B,
+                int bw, int bh, int bb) {
+    EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)C, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)W * eb, (cuuint64_t)H * W * eb, (cuuint64_t)C * H * W * eb};
+    const cuuint32_t box[4] = {(cuuint32_t)bw, (cuuint32_t)bh, 1u, (cuuint32_t)bb};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Whether the shallow kernel's tiles can move as bulk tensor copies: every row, box row and box
+// origin 16-byte aligned, box extents within the hardware limit of 256.
+bool shallow_tma_x_ok(const ShallowArgs &a, int eb) {
+    const ShallowGeo &g = a.sg;
+    return ((size_t)a.W * eb) % 16 == 0 && ((size_t)g.xw * eb) % 16 == 0 && ((size_t)g.padx * eb) % 16 == 0 &&
+           ((size_t)g.TW * eb) % 16 == 0 && g.xw <= 256 && g.xrows <= 256 && g.G <= 256;
+}
+bool shallow_tma_d_ok(const ShallowArgs &a) {
+    const ShallowGeo &g = a.sg;
+    return a.L >= 2 && ((a.W / 2) % 4) == 0 && ((g.TW / 2) % 4) == 0 && g.TW / 2 <= 256 && g.TH / 2 <= 256;
+}
+
+CUtensorMapDataType tma_dtype(int dtype) {
+    return dtype == WTCONV_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                               : dtype == WTCONV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+// Tiled weight gradient: the shallow kernel's tiles (bulk tensor copies of x and dy, tiles of a
+// multiple of 16 rows); UNSUPPORTED where those do not apply.
+struct TPlan {
+    int status = WTCONV_OK;
+    DwTileArgs a{};
+    size_t smem = 0;
+    size_t workspace = 0;  // partials, then the pyramids of levels >= 2
+    size_t partial_bytes = 0;
+};
+
+TPlan plan_dw_tile_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
+    TPlan p;
+    const SPlan ps = plan_shallow(B, C, H, W, L, k, dtype);
+    if (ps.status != WTCONV_OK) { p.status = ps.status; return p; }
+    const ShallowGeo &sg = ps.a.sg;
+    const int eb = elem_bytes(dtype);
+    if (!shallow_tma_x_ok(ps.a, eb) || sg.TH % 16 != 0 || ((size_t)sg.TW * eb) % 16 != 0 || sg.TH > 256 ||
+        sg.TW > 256) {
+        p.status = WTCONV_ERR_UNSUPPORTED;
+        return p;
+    }
+    DwTileArgs &a = p.a;
+    a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
+    a.sg = sg;
+    p.smem = dw_tile_smem_bytes(sg, eb);
+    if (p.smem + kStaticSmemMargin > (size_t)kMaxSmem) { p.status = WTCONV_ERR_UNSUPPORTED; return p; }
+    const int sms = device_sms();
+    const int occ = occupancy_dw_tile(dtype, k, p.smem);
+    if (sms <= 0 || occ <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
+    const int tiles = sg.tiles_r * sg.tiles_c;
+    a.units = ((B + sg.G - 1) / sg.G) * tiles;
+    const long long slots = (long long)sms * occ;
+    long long best_nb = 1, best_cost = -1;
+    for (long long nb = 1; nb <= a.units; ++nb) {
+        const long long cost = ((C * nb + slots - 1) / slots) * ((a.units + nb - 1) / nb);
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_nb = nb; }
+    }
+    a.units_per_cta = (int)((a.units + best_nb - 1) / best_nb);
+    a.nb = (a.units + a.units_per_cta - 1) / a.units_per_cta;
+    a.tiles = make_fastdiv(tiles);
+    a.tiles_c = make_fastdiv(sg.tiles_c);
+    p.partial_bytes = ((size_t)a.nb * C * (1 + 4 * L) * (k * k + 1) * sizeof(float) + 255) / 256 * 256;
+    p.workspace = p.partial_bytes + (L >= 2 ? dw_pyramid_bytes(B, C, H, W, L, 2) : 0);
+    return p;
+}
+
+TPlan plan_dw_tile(int B, int C, int H, int W, int L, int k, int dtype) {
+    static std::mutex mu;
+    static std::map<PlanKey, TPlan> cache;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        TPlan p;
+        p.status = WTCONV_ERR_CUDA;
+        return p;
+    }
+    const PlanKey key(6, B, C, H, W, L, k, dtype, dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    TPlan p = plan_dw_tile_uncached(B, C, H, W, L, k, dtype);
+    if (p.status == WTCONV_OK || p.status == WTCONV_ERR_UNSUPPORTED) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache.emplace(key, p);
+    }
+    return p;
+}
+
+// Which weight-gradient path a call takes: the whole-plane kernel where a plane fits, else the
+// tiled kernels where they apply, else the workspace pyramids.  WTCONV_DW_PATH=tiles, =plane or
+// =pyramid selects a path where it applies (for testing and comparison).
+enum DwPath { DW_TILE, DW_PLANE, DW_PYRAMID };
+struct DwChoice {
+    int status = WTCONV_OK;
+    DwPath path = DW_PLANE;
+    TPlan t;
+    Plan p;
+    size_t workspace = 0;
+};
+
+DwChoice choose_dw(int B, int C, int H, int W, int L, int k, int dtype) {
+    DwChoice d;
+    const char *env = getenv("WTCONV_DW_PATH");
+    const bool want_tiles = env && strcmp(env, "tiles") == 0;
+    const bool want_pyramid = env && strcmp(env, "pyramid") == 0;
+    if (!want_tiles && !want_pyramid) {
+        d.p = plan_dw(B, C, H, W, L, k, dtype);
+        if (d.p.status != WTCONV_OK) { d.status = d.p.status; return d; }
+        if (!d.p.dw_pyramid) {
+            d.path = DW_PLANE;
+            d.workspace = d.p.workspace;
+            return d;
+        }
+    }
+    if (!want_pyramid) {
+        d.t = plan_dw_tile(B, C, H, W, L, k, dtype);
+        if (d.t.status == WTCONV_OK) {
+            d.path = DW_TILE;
+            d.workspace = d.t.workspace;
+            return d;
+        }
+        if (d.t.status != WTCONV_ERR_UNSUPPORTED) { d.status = d.t.status; return d; }
+    }
+    d.p = want_pyramid ? plan_dw_pyramid_only(B, C, H, W, L, k, dtype) : plan_dw(B, C, H, W, L, k, dtype);
+    if (d.p.status != WTCONV_OK) { d.status = d.p.status; return d; }
+    d.path = d.p.dw_pyramid ? DW_PYRAMID : DW_PLANE;
+    d.workspace = d.p.workspace;
+    return d;
 }
 
 void set_params(LayerArgs &a, const float *base_w, const float *base_bias, const float *base_scale,
@@ -501,9 +670,9 @@ size_t wtconv_workspace_size(int op, int B, int C, int H, int W, int L, int k, i
     if (op == WTCONV_OP_FORWARD || op == WTCONV_OP_BACKWARD_INPUT || op == WTCONV_OP_BACKWARD)
         bytes += deep_bytes(B, C, H, W, L);
     if (op == WTCONV_OP_BACKWARD_WEIGHTS || op == WTCONV_OP_BACKWARD) {
-        Plan p = plan_dw(B, C, H, W, L, k, dtype);
-        if (p.status != WTCONV_OK) return 0;
-        bytes += p.workspace;
+        const DwChoice d = choose_dw(B, C, H, W, L, k, dtype);
+        if (d.status != WTCONV_OK) return 0;
+        bytes += d.workspace;
     }
     return bytes;
 }
@@ -529,64 +698,12 @@ int wtconv_launch_count(int op, int B, int C, int H, int W, int L, int k, int dt
         else return 0;
     }
     if (op == WTCONV_OP_BACKWARD_WEIGHTS || op == WTCONV_OP_BACKWARD) {
-        const Plan pw = plan_dw(B, C, H, W, L, k, dtype);
-        if (pw.status != WTCONV_OK) return 0;
-        n += pw.dw_pyramid ? 2 * L + 2 : 2;
+        const DwChoice d = choose_dw(B, C, H, W, L, k, dtype);
+        if (d.status != WTCONV_OK) return 0;
+        if (d.path == DW_TILE) n += 2 + (L >= 2 ? 1 + (L - 2) + (L - 1) : 0);  // tiles, level 2, levels, corr, finalize
+        else n += d.path == DW_PYRAMID ? 2 * L + 2 : 2;
     }
     return n;
-}
-
-// ------------------------------------------------------------------ bulk tensor copies (TMA)
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// cuTensorMapEncodeTiled from the driver, looked up once (nullptr if unavailable).
-EncodeTiledFn encode_tiled() {
-    static std::once_flag once;
-    static EncodeTiledFn fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// Tensor map of a contiguous [B][C][H][W] tensor with a box of bw x bh x 1 x bb elements
-// (zero fill outside).  False if the driver refuses it.
-bool encode_map(CUtensorMap *m, CUtensorMapDataType dt, int eb, const void *base, int W, int H, int C, int B,
-                int bw, int bh, int bb) {
-    EncodeTiledFn fn = encode_tiled();
-    if (fn == nullptr) return false;
-    const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)C, (cuuint64_t)B};
-    const cuuint64_t strides[3] = {(cuuint64_t)W * eb, (cuuint64_t)H * W * eb, (cuuint64_t)C * H * W * eb};
-    const cuuint32_t box[4] = {(cuuint32_t)bw, (cuuint32_t)bh, 1u, (cuuint32_t)bb};
-    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Whether the shallow kernel's tiles can move as bulk tensor copies: every row, box row and box
-// origin 16-byte aligned, box extents within the hardware limit of 256.
-bool shallow_tma_x_ok(const ShallowArgs &a, int eb) {
-    const ShallowGeo &g = a.sg;
-    return ((size_t)a.W * eb) % 16 == 0 && ((size_t)g.xw * eb) % 16 == 0 && ((size_t)g.padx * eb) % 16 == 0 &&
-           ((size_t)g.TW * eb) % 16 == 0 && g.xw <= 256 && g.xrows <= 256 && g.G <= 256;
-}
-bool shallow_tma_d_ok(const ShallowArgs &a) {
-    const ShallowGeo &g = a.sg;
-    return a.L >= 2 && ((a.W / 2) % 4) == 0 && ((g.TW / 2) % 4) == 0 && g.TW / 2 <= 256 && g.TH / 2 <= 256;
-}
-
-CUtensorMapDataType tma_dtype(int dtype) {
-    return dtype == WTCONV_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                               : dtype == WTCONV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
 // The layer's linear operator on `src` (x -> y, or dy -> dx with rotated kernels and no bias):
@@ -682,10 +799,10 @@ static int backward_common(bool want_dx, int B, int C, int H, int W, int L, int 
         !params_ok(d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale))
         return WTCONV_ERR_INVALID_ARG;
     if (fault_injected()) return WTCONV_ERR_INJECTED;
-    Plan pw = plan_dw(B, C, H, W, L, k, dtype);
-    if (pw.status != WTCONV_OK) return pw.status;
+    DwChoice dc = choose_dw(B, C, H, W, L, k, dtype);
+    if (dc.status != WTCONV_OK) return dc.status;
     const size_t dbytes = want_dx ? deep_bytes(B, C, H, W, L) : 0;
-    if (workspace_bytes < dbytes + pw.workspace || (dbytes + pw.workspace > 0 && !aligned16(workspace)))
+    if (workspace_bytes < dbytes + dc.workspace || (dbytes + dc.workspace > 0 && !aligned16(workspace)))
         return WTCONV_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (want_dx) {
@@ -693,12 +810,43 @@ static int backward_common(bool want_dx, int B, int C, int H, int W, int L, int 
                           true, workspace, dbytes, s);
         if (st != WTCONV_OK) return st;
     }
-    pw.a.x = x; pw.a.dy = dy;
-    set_params(pw.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
     char *wsp = static_cast<char *>(workspace) + dbytes;
-    if (pw.dw_pyramid) {
+    LayerArgs fin{};  // what the finalize kernel reads
+    if (dc.path == DW_TILE) {
+        // base path and level 1 on tiles (signals 0 .. 4), levels >= 2 on their pyramids
+        DwTileArgs &t = dc.t.a;
+        const int eb = elem_bytes(dtype);
+        t.partials = reinterpret_cast<float *>(wsp);
+        t.timeout = timeout_flag();
+        if (t.timeout == nullptr) return WTCONV_ERR_CUDA;
+        if (!encode_map(&t.tmap_x, tma_dtype(dtype), eb, x, W, H, C, B, t.sg.xw, t.sg.xrows, t.sg.G) ||
+            !encode_map(&t.tmap_dy, tma_dtype(dtype), eb, dy, W, H, C, B, t.sg.TW, t.sg.TH, t.sg.G))
+            return WTCONV_ERR_CUDA;
+        if (launch_dw_tile(t, dtype, dc.t.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+        if (L >= 2) {
+            DwPyramidArgs d{};
+            d.B = B; d.C = C; d.H = H; d.W = W; d.L = L; d.K = k;
+            d.from_level = 2;
+            d.nb = t.nb;
+            d.x = x; d.dy = dy;
+            char *pw = wsp + dc.t.partial_bytes;
+            for (int l = 2; l <= L; ++l) {
+                const size_t lb = ((size_t)B * C * (H >> l) * (W >> l) * sizeof(float4) + 255) / 256 * 256;
+                d.pyr_x[l] = reinterpret_cast<float4 *>(pw);
+                d.pyr_dy[l] = reinterpret_cast<float4 *>(pw + lb);
+                pw += 2 * lb;
+            }
+            d.partials = t.partials;
+            if (launch_dw_pyramid(d, dtype, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+        }
+        fin.B = B; fin.C = C; fin.H = H; fin.W = W; fin.L = L; fin.K = k;
+        fin.nb = t.nb;
+        fin.partials = t.partials;
+    } else if (dc.path == DW_PYRAMID) {
+        Plan &pw = dc.p;
         DwPyramidArgs d{};
         d.B = B; d.C = C; d.H = H; d.W = W; d.L = L; d.K = k;
+        d.from_level = 1;
         d.nb = pw.a.nb;
         d.x = x; d.dy = dy;
         for (int l = 1; l <= L; ++l) {
@@ -708,13 +856,19 @@ static int backward_common(bool want_dx, int B, int C, int H, int W, int L, int 
             wsp += 2 * lb;
         }
         d.partials = reinterpret_cast<float *>(wsp);
-        pw.a.partials = d.partials;
         if (launch_dw_pyramid(d, dtype, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+        fin = pw.a;
+        fin.partials = d.partials;
     } else {
+        Plan &pw = dc.p;
+        pw.a.x = x; pw.a.dy = dy;
+        set_params(pw.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
         pw.a.partials = reinterpret_cast<float *>(wsp);
         if (launch_dw(pw.a, dtype, pw.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+        fin = pw.a;
     }
-    return cuda_status(launch_dw_finalize(pw.a, d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale, s));
+    set_params(fin, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
+    return cuda_status(launch_dw_finalize(fin, d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale, s));
 }
 
 int wtconv_backward_weights(int B, int C, int H, int W, int L, int k, int dtype, const void *x, const void *dy,

@@ -48,6 +48,44 @@ __global__ void __launch_bounds__(256) wtconv_haar_level_kernel(const S *src_x, 
     }
 }
 
+// Level 2 of every plane straight from the input: one thread per level-2 position reads its
+// 4 x 4 pixel block, forms the four level-1 low bands (unnormalised 2 x 2 sums) and their
+// butterfly, and writes the quad (LL, LH, HL, HH) to q2 [B*C][H/4][W/4].  Two positions per
+// iteration keep eight row loads in flight.  W % 4 == 0 (L >= 2), so rows load as vectors.
+// blockIdx.y selects the tensor (x or dy).
+template <typename T>
+__global__ void __launch_bounds__(256) wtconv_level2_kernel(const T *__restrict__ x0, const T *__restrict__ x1,
+                                                            float4 *__restrict__ q0, float4 *__restrict__ q1,
+                                                            long long n, int W4, int W) {
+    const T *__restrict__ x = blockIdx.y ? x1 : x0;
+    float4 *__restrict__ q2 = blockIdx.y ? q1 : q0;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += 2 * stride) {
+        float4 v[2][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const long long i = i0 + h * stride;
+            const long long ii = i < n ? i : i0;
+            const long long prow = ii / W4;  // plane * (H/4) + block row
+            const int bj = (int)(ii - prow * W4);
+            const T *src = x + (size_t)prow * 4 * W + 4 * (size_t)bj;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) v[h][r] = Act<T>::ld4(src + (size_t)r * W);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const long long i = i0 + h * stride;
+            if (i >= n) break;
+            const float ll00 = (v[h][0].x + v[h][0].y) + (v[h][1].x + v[h][1].y);
+            const float ll01 = (v[h][0].z + v[h][0].w) + (v[h][1].z + v[h][1].w);
+            const float ll10 = (v[h][2].x + v[h][2].y) + (v[h][3].x + v[h][3].y);
+            const float ll11 = (v[h][2].z + v[h][2].w) + (v[h][3].z + v[h][3].w);
+            const Quad q = butterfly(ll00, ll01, ll10, ll11);
+            q2[i] = make_float4(q.ll, q.lh, q.hl, q.hh);
+        }
+    }
+}
+
 template <typename S, int NSUB>
 __device__ __forceinline__ void load_sub(const S *p, size_t i, bool in, float (&v)[NSUB]) {
     if constexpr (NSUB == 4) {
@@ -147,8 +185,16 @@ cudaError_t launch_dw_pyramid_t(const DwPyramidArgs &a, cudaStream_t st) {
     const int nsig = 1 + 4 * a.L;
     constexpr int RP = K * K + 2;
     const size_t red_bytes = (size_t)kCorrThreads * RP * sizeof(float);
-    // 1. pyramids, level by level
-    for (int l = 1; l <= a.L; ++l) {
+    // 1. pyramids, level by level (from level 2 on when the tiled kernel covers base and level 1:
+    //    level 2 then comes straight from 4 x 4 pixel blocks)
+    if (a.from_level == 2) {
+        const long long n = planes * (a.H >> 2) * (a.W >> 2);
+        long long blocks = (n + 2 * 256 - 1) / (2 * 256);
+        if (blocks > (1LL << 20)) blocks = 1LL << 20;
+        wtconv_level2_kernel<T><<<dim3((unsigned)blocks, 2), 256, 0, st>>>(
+            static_cast<const T *>(a.x), static_cast<const T *>(a.dy), a.pyr_x[2], a.pyr_dy[2], n, a.W >> 2, a.W);
+    }
+    for (int l = a.from_level == 2 ? 3 : 1; l <= a.L; ++l) {
         const int Hl = a.H >> l, Wl = a.W >> l;
         const long long n = planes * Hl * Wl;
         long long blocks = (n + 255) / 256;
@@ -173,9 +219,10 @@ cudaError_t launch_dw_pyramid_t(const DwPyramidArgs &a, cudaStream_t st) {
                              (int)red_bytes);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(a.nb * a.C));
-    wtconv_dw_corr_kernel<K, 1, T><<<grid, kCorrThreads, red_bytes, st>>>(
-        static_cast<const T *>(a.x), static_cast<const T *>(a.dy), a.B, a.C, a.H, a.W, a.nb, nsig, 0, a.partials);
-    for (int l = 1; l <= a.L; ++l)
+    if (a.from_level == 1)
+        wtconv_dw_corr_kernel<K, 1, T><<<grid, kCorrThreads, red_bytes, st>>>(
+            static_cast<const T *>(a.x), static_cast<const T *>(a.dy), a.B, a.C, a.H, a.W, a.nb, nsig, 0, a.partials);
+    for (int l = a.from_level; l <= a.L; ++l)
         wtconv_dw_corr_kernel<K, 4, float4><<<grid, kCorrThreads, red_bytes, st>>>(
             a.pyr_x[l], a.pyr_dy[l], a.B, a.C, a.H >> l, a.W >> l, a.nb, nsig, 1 + 4 * (l - 1), a.partials);
     return cudaGetLastError();
@@ -183,9 +230,9 @@ cudaError_t launch_dw_pyramid_t(const DwPyramidArgs &a, cudaStream_t st) {
 
 }  // namespace
 
-size_t dw_pyramid_bytes(int B, int C, int H, int W, int L) {
+size_t dw_pyramid_bytes(int B, int C, int H, int W, int L, int from_level) {
     size_t bytes = 0;
-    for (int l = 1; l <= L; ++l) bytes += 2 * (((size_t)B * C * (H >> l) * (W >> l) * sizeof(float4) + 255) / 256 * 256);
+    for (int l = from_level; l <= L; ++l) bytes += 2 * (((size_t)B * C * (H >> l) * (W >> l) * sizeof(float4) + 255) / 256 * 256);
     return bytes;
 }
 

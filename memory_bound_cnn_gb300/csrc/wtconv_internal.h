@@ -231,12 +231,28 @@ size_t dw_smem_bytes(const Geo &geo, int G, int L, int K, int elem_bytes, bool s
 // correlations writing nb partials per (channel, signal, tap) for the finalize kernel.
 struct DwPyramidArgs {
     int B, C, H, W, L, K;
+    int from_level;            // 1: every correlation; 2: levels >= 2 only (the tiled kernel does the rest)
     int nb;                    // partials per (channel, signal, tap): CTAs per channel of each correlation
     const void *x, *dy;
     float4 *pyr_x[kMaxLevels + 1], *pyr_dy[kMaxLevels + 1];
     float *partials;           // [nb][C][1+4L][K*K+1]
 };
-size_t dw_pyramid_bytes(int B, int C, int H, int W, int L);
+size_t dw_pyramid_bytes(int B, int C, int H, int W, int L, int from_level);
+
+// Tiled weight gradient (base path and level 1; levels >= 2 go to the level kernels from level 2):
+// one warp per CTA over units of the shallow kernel's tiling, x and dy tiles by bulk tensor copy.
+struct DwTileArgs {
+    int B, C, H, W, L, K;
+    int units, units_per_cta, nb;  // units per channel; grid = nb * C
+    float *partials;               // [nb][C][1+4L][K*K+1]; this kernel writes signals 0 .. 4
+    ShallowGeo sg;
+    FastDiv tiles, tiles_c;
+    int *timeout;
+    CUtensorMap tmap_x, tmap_dy;   // x: box xw x xrows x 1 x G at (c0 - padx, r0 - 2P); dy: TW x TH x 1 x G
+};
+size_t dw_tile_smem_bytes(const ShallowGeo &sg, int elem_bytes);
+cudaError_t launch_dw_tile(const DwTileArgs &a, int dtype, size_t smem, cudaStream_t st);
+int occupancy_dw_tile(int dtype, int K, size_t smem);
 cudaError_t launch_dw_pyramid(const DwPyramidArgs &a, int dtype, cudaStream_t st);
 
 // Launchers (host side, in the kernel translation units).  dtype: 0 f32, 1 bf16, 2 f16.

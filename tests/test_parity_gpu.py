@@ -18,17 +18,21 @@ pytestmark = pytest.mark.gpu
 
 
 @contextlib.contextmanager
-def fwd_path(path: str):
-    """WTCONV_FWD_PATH for the calls inside (the library reads it at every call)."""
-    old = os.environ.get("WTCONV_FWD_PATH")
-    os.environ["WTCONV_FWD_PATH"] = path
+def env_path(var: str, path: str):
+    """Set an environment variable for the calls inside (the library reads it at every call)."""
+    old = os.environ.get(var)
+    os.environ[var] = path
     try:
         yield
     finally:
         if old is None:
-            del os.environ["WTCONV_FWD_PATH"]
+            del os.environ[var]
         else:
-            os.environ["WTCONV_FWD_PATH"] = old
+            os.environ[var] = old
+
+
+def fwd_path(path: str):
+    return env_path("WTCONV_FWD_PATH", path)
 
 
 def check_layer(shape: LayerShape, inputs: dict, split: bool = True):
@@ -55,6 +59,15 @@ def check_layer(shape: LayerShape, inputs: dict, split: bool = True):
         assert_close("dx (backward_input)", np64(dx2), g_ref["dx"], tol)
         for n in GRADS:
             assert_close(n + " (backward_weights)", np64(g2[n]), g_ref[n], tol)
+    # the weight gradient's other paths: tiled kernels (where they apply) and workspace pyramids
+    for dpath in ("tiles", "pyramid"):
+        if dpath == "pyramid" and shape.numel > 20_000_000:
+            continue  # the pyramid path already runs by default where planes are too large
+        with env_path("WTCONV_DW_PATH", dpath):
+            g3 = W.wtconv_backward_weights(d["x"], d["dy"], *[d[p] for p in PARAMS])
+            torch.cuda.synchronize()
+        for n in GRADS:
+            assert_close(f"{n} [{dpath}]", np64(g3[n]), g_ref[n], tol)
 
 
 @pytest.mark.parametrize("name", WORKLOAD_ORDER)
