@@ -386,10 +386,14 @@ __global__ void __launch_bounds__(32, (K <= 5 ? 16 : 8)) wtconv_shallow_kernel(c
                 init[2 * i][0] = init[2 * i + 1][0] = pk2(d0 + bias, d0 + bias);
                 init[2 * i][1] = init[2 * i + 1][1] = pk2(d1 + bias, d1 + bias);
             }
-#pragma unroll
+            // one copy of the level-1 item code for both subband pairs (a smaller instruction
+            // footprint); the pair's row sign (+1 for LL|LH, -1 for HL|HH) enters as an FMA factor
+#pragma unroll 1
             for (int pp = 0; pp < 2; ++pp) {
                 f2_t z[4][kColsL];
                 level1_item<K>(pairs + y_item + pp * G * sg.yimg, sg.ypitch, wts + (1 + pp) * WP, z);
+                const float sg1 = pp == 0 ? 1.f : -1.f;
+                const f2_t sgn = pk2(sg1, sg1);
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -397,7 +401,7 @@ __global__ void __launch_bounds__(32, (K <= 5 ? 16 : 8)) wtconv_shallow_kernel(c
                         const float s0 = lo2(z[i][q]), s1 = hi2(z[i][q]);
                         const f2_t sv = pk2(s0 + s1, s0 - s1);
                         init[2 * i][q] = fadd2(init[2 * i][q], sv);
-                        init[2 * i + 1][q] = pp == 0 ? fadd2(init[2 * i + 1][q], sv) : fsub2(init[2 * i + 1][q], sv);
+                        init[2 * i + 1][q] = ffma2(sgn, sv, init[2 * i + 1][q]);
                     }
             }
             const int nrows = b < B ? max(0, min(kRows, H - pr)) : 0;
