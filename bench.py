@@ -14,7 +14,8 @@ y, dx and the gradients inside the timed region), the CPU oracle baseline, and S
 during the timed region.
 
 `--impl reference` times the CPU oracle (the plain fp64 reference pipeline) instead, on the host
-cores, on a bounded sample of the same workload.
+cores, on a bounded sample of the same workload.  `--impl torch-cascade` times the same reference
+cascade written with PyTorch ops on the GPU (grouped convs, autograd): a comparison arm.
 """
 from __future__ import annotations
 
@@ -406,12 +407,94 @@ def run_reference(args, world, rank):
 
 # ---------------------------------------------------------------------------------- main
 
+# ----------------------------------------------------------------- PyTorch-op cascade arm
+
+def haar_filters(C: int, device, dtype) -> torch.Tensor:
+    """The four orthonormal 2 x 2 Haar filters (LL, LH, HL, HH sign patterns x 1/2), repeated per
+    channel as a grouped-conv weight [4C, 1, 2, 2] (subband channel 4c+s)."""
+    f = torch.tensor([[[1, 1], [1, 1]], [[1, -1], [1, -1]], [[1, 1], [-1, -1]], [[1, -1], [-1, 1]]],
+                     dtype=torch.float64) * 0.5
+    return f.repeat(C, 1, 1).unsqueeze(1).to(device=device, dtype=dtype)
+
+
+def torch_cascade(x, base_w, base_bias, base_scale, wavelet_w, wavelet_scale):
+    """The reference cascade written with PyTorch ops (grouped convs, autograd for the backward):
+    explicit Haar analysis per level, per-subband conv, separate scale, the synthesis cascade that
+    adds each deeper reconstruction to the scaled LL conv output before the inverse transform, and
+    the scaled base conv with bias.  A comparison arm only: it is not the product path."""
+    import torch.nn.functional as F
+    B, C, H, Wd = x.shape
+    L, k = wavelet_w.shape[0], base_w.shape[-1]
+    P = k // 2
+    filt = haar_filters(C, x.device, x.dtype)
+    ys, ll = [], x
+    for l in range(L):
+        y = F.conv2d(ll, filt, stride=2, groups=C)               # [B, 4C, H/2^l, W/2^l]
+        ys.append(y)
+        ll = y[:, 0::4]
+    r = None
+    for l in reversed(range(L)):
+        z = F.conv2d(ys[l], wavelet_w[l].unsqueeze(1).to(x.dtype), padding=P, groups=4 * C)
+        z = z * wavelet_scale[l].to(x.dtype).view(1, -1, 1, 1)
+        if r is not None:
+            z = torch.cat([z[:, 0::4] + r, z[:, 1::4], z[:, 2::4], z[:, 3::4]], dim=1)
+            z = z.view(B, 4, C, *z.shape[2:]).transpose(1, 2).reshape(B, 4 * C, *z.shape[2:])
+        r = F.conv_transpose2d(z, filt, stride=2, groups=C)
+    base = F.conv2d(x, base_w.unsqueeze(1).to(x.dtype), padding=P, groups=C) + base_bias.to(x.dtype).view(1, -1, 1, 1)
+    return base * base_scale.to(x.dtype).view(1, -1, 1, 1) + r
+
+
+def run_torch_cascade(args, world, rank, local):
+    """fwd + bwd of the PyTorch-op cascade on the GPU (fp32 convs without TF32), same workload."""
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    torch.backends.cudnn.allow_tf32 = False
+    torch.backends.cuda.matmul.allow_tf32 = False
+    shapes = WORKLOADS[args.workload]
+    layers = []
+    for i, s in enumerate(shapes):
+        d = {k2: v.to(dev) for k2, v in make_inputs(s, seed=i).items()}
+        for n in PARAMS:
+            d[n].requires_grad_(True)
+        d["x"].requires_grad_(True)
+        layers.append((s, d))
+
+    def step():
+        for s, d in layers:
+            for t in [d["x"]] + [d[n] for n in PARAMS]:
+                t.grad = None
+            y = torch_cascade(d["x"], *[d[n] for n in PARAMS])
+            y.backward(d["dy"])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    steps = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    elements = sum(s.numel for s, _ in layers)
+    value = whole_job_throughput(elements, world, ms / 1e3)
+    return {
+        "impl": "torch-cascade", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": shapes[0].dtype, "data": "synthetic",
+        "config": {"workload": args.workload, "layers": [s.as_dict() for s in shapes]},
+        "note": "PyTorch grouped convs (cuDNN, no TF32) + autograd of the reference cascade; comparison arm",
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", choices=("cuda", "reference"), default="cuda")
+    ap.add_argument("--impl", choices=("cuda", "reference", "torch-cascade"), default="cuda")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stage1_f32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -424,6 +507,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             line = run_reference(args, world, rank)
+        elif args.impl == "torch-cascade":
+            line = run_torch_cascade(args, world, rank, local)
         else:
             W.load()
             line = run_gpu(args, world, rank, local)
