@@ -71,8 +71,10 @@ def algorithmic(shape: LayerShape) -> dict:
 # these files are unchanged since the capture
 KERNEL_SOURCES = {
     "wtconv_fwd_kernel": ["wtconv_fwd.cu", "wtconv_analysis.cuh", "wtconv_device.cuh", "wtconv_internal.h"],
-    "wtconv_deep_kernel+wtconv_shallow_kernel": ["wtconv_deep.cu", "wtconv_shallow.cu", "wtconv_analysis.cuh",
-                                                 "wtconv_device.cuh", "wtconv_internal.h"],
+    "wtconv_plane_kernel": ["wtconv_plane.cu", "wtconv_items.cuh", "wtconv_analysis.cuh", "wtconv_device.cuh",
+                            "wtconv_internal.h"],
+    "wtconv_deep_kernel+wtconv_shallow_kernel": ["wtconv_deep.cu", "wtconv_shallow.cu", "wtconv_items.cuh",
+                                                 "wtconv_analysis.cuh", "wtconv_device.cuh", "wtconv_internal.h"],
     "wtconv_dw_kernel": ["wtconv_bwd.cu", "wtconv_analysis.cuh", "wtconv_device.cuh", "wtconv_internal.h"],
 }
 
@@ -296,8 +298,8 @@ def run_gpu(args, world, rank, local):
     # its launches in wtconv_forward are timed alone by the fwd events above
     acc = [algorithmic(s) for s, *_ in layers]
     fwd_tot, bwd_tot = sum(fwd_ms), sum(bwd_ms)
-    fwd_launches = [W.wtconv_launch_count(W.OP_FORWARD, *dims(s)) for s in shapes]
-    kname = "wtconv_fwd_kernel" if all(n == 1 for n in fwd_launches) else "wtconv_deep_kernel+wtconv_shallow_kernel"
+    fwd_kernels = {"+".join(W.wtconv_plan_kernels(W.OP_FORWARD, *dims(s))) for s in shapes}
+    kname = fwd_kernels.pop() if len(fwd_kernels) == 1 else "forward kernels (per layer: several)"
     flop, byt = sum(a["fwd_flop"] for a in acc), sum(a["fwd_bytes"] for a in acc)
     ms = fwd_tot
     launches = len(layers)

@@ -38,9 +38,10 @@
  *     the caller's next synchronisation, as with any CUDA launch.
  *   - The library keeps no state between calls; concurrent calls on different streams with
  *     distinct workspaces are safe.
- *   - The forward and the input gradient run one whole-plane kernel where a plane's Haar pyramid
- *     fits in shared memory, else two tiled kernels.  WTCONV_FWD_PATH=tiles selects the tiled
- *     kernels for every shape (same results within fp32 rounding).
+ *   - The forward and the input gradient run one of three kernel sets: the fused whole-plane
+ *     kernel (fp32 planes where it is fastest), the whole-plane kernel (planes whose pyramid fits
+ *     in shared memory), or two tiled kernels (larger planes).  WTCONV_FWD_PATH=fused, =plane or
+ *     =tiles selects a set where it applies (same results within fp32 rounding).
  *   - The weight gradients run a whole-plane kernel where both planes' pyramids fit in shared
  *     memory, else tiled kernels (tiles with bulk tensor copies, levels >= 2 on their pyramids in
  *     the workspace), else workspace pyramids for every level.  WTCONV_DW_PATH=tiles or =pyramid
@@ -105,6 +106,10 @@ int wtconv_device_status(void);
  * gradients need one fp32 partial per (CTA, channel, subband, tap); BACKWARD needs both.
  * Returns 0 for an invalid shape as well; the compute call then reports the error. */
 size_t wtconv_workspace_size(int op, int B, int C, int H, int W, int L, int k, int dtype);
+
+/* Names of the kernels `op` launches for this shape on the current device, joined by '+', in
+ * launch order ("" for an invalid or unsupported shape).  Static storage; never NULL. */
+const char *wtconv_plan_kernels(int op, int B, int C, int H, int W, int L, int k, int dtype);
 
 /* Number of kernel launches `op` makes for this shape on the current device (0 for an invalid
  * or unsupported shape).  Planes whose Haar pyramid fits in shared memory take one launch for

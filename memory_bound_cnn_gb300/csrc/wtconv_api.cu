@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <map>
 #include <mutex>
+#include <string>
 #include <tuple>
 
 #include "wtconv.h"
@@ -35,13 +36,6 @@ int validate_shape(int B, int C, int H, int W, int L, int k, int dtype) {
     if (dtype != WTCONV_F32 && dtype != WTCONV_BF16 && dtype != WTCONV_F16) return WTCONV_ERR_UNSUPPORTED;
     if (k != 3 && k != 5 && k != 7) return WTCONV_ERR_UNSUPPORTED;
     return WTCONV_OK;
-}
-
-// WTCONV_FWD_PATH=tiles: the forward and input gradient take the tiled kernels even where the
-// whole-plane kernel fits (same results within rounding; for testing and comparison).
-bool tiles_forced() {
-    const char *v = getenv("WTCONV_FWD_PATH");
-    return v && strcmp(v, "tiles") == 0;
 }
 
 bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -550,6 +544,125 @@ TPlan plan_dw_tile(int B, int C, int H, int W, int L, int k, int dtype) {
     return p;
 }
 
+// Fused whole-plane kernel: the plane (+ halo) must move as one bulk tensor copy and its whole
+// pyramid, D and one input tile must fit in shared memory.
+struct PPlan {
+    int status = WTCONV_OK;
+    PlaneArgs a{};
+    size_t smem = 0;
+    int occ = 0;  // resident CTAs per SM
+};
+
+PPlan plan_plane_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
+    PPlan p;
+    PlaneArgs &a = p.a;
+    a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
+    const int eb = elem_bytes(dtype);
+    const int e16 = 16 / eb;
+    if (((size_t)W * eb) % 16 != 0) { p.status = WTCONV_ERR_UNSUPPORTED; return p; }
+    const int TW = round_up(W, e16 > 4 ? e16 : 4), TH = round_up(H, kRows);
+    const int dchunk_e = ((W / 2) % 4 == 0 && (TW / 2) % 4 == 0) ? 4 : 2;
+    a.sg = make_shallow_geo(H, W, k, TH, TW, 1, eb, e16, dchunk_e);
+    const ShallowGeo &sg = a.sg;
+    if (((size_t)sg.xw * eb) % 16 != 0 || ((size_t)sg.padx * eb) % 16 != 0 || sg.xw > 256 || sg.xrows > 256) {
+        p.status = WTCONV_ERR_UNSUPPORTED;
+        return p;
+    }
+    a.st_mode = (W % 4) == 0 ? 1 : 0;
+    a.dpitch = round_up(TW / 2, 2);
+    if (L >= 2) {
+        a.dg = make_geo(H, W, L, k, 2);
+        int tot = 0;
+        for (int ci = 3; ci < 1 + 2 * L; ++ci) {
+            const int l = (ci - 1) / 2 + 1;
+            a.deep_item_start[ci] = tot;
+            tot += a.dg.rseg[l] * a.dg.cstr[l];
+        }
+        a.deep_item_start[1 + 2 * L] = tot;
+        a.n_deep_items = tot;
+    }
+    p.smem = plane_smem_bytes(a, eb);
+    if (p.smem + kStaticSmemMargin > (size_t)kMaxSmem) { p.status = WTCONV_ERR_UNSUPPORTED; return p; }
+    const int sms = device_sms();
+    const int occ = occupancy_plane(dtype, k, p.smem);
+    if (sms <= 0 || occ <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
+    p.occ = occ;
+    const long long slots = (long long)sms * occ;
+    long long best_nb = 1, best_cost = -1;
+    for (long long nb = 1; nb <= B; ++nb) {
+        const long long cost = ((C * nb + slots - 1) / slots) * ((B + nb - 1) / nb);
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_nb = nb; }
+    }
+    a.planes_per_cta = (int)((B + best_nb - 1) / best_nb);
+    a.nb = (B + a.planes_per_cta - 1) / a.planes_per_cta;
+    return p;
+}
+
+PPlan plan_plane(int B, int C, int H, int W, int L, int k, int dtype) {
+    static std::mutex mu;
+    static std::map<PlanKey, PPlan> cache;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        PPlan p;
+        p.status = WTCONV_ERR_CUDA;
+        return p;
+    }
+    const PlanKey key(7, B, C, H, W, L, k, dtype, dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    PPlan p = plan_plane_uncached(B, C, H, W, L, k, dtype);
+    const char *verbose = getenv("WTCONV_VERBOSE");
+    if (verbose && verbose[0] == '1')
+        fprintf(stderr, "wtconv plan fused B=%d C=%d H=%d W=%d L=%d k=%d dtype=%d: status %d nb=%d planes/cta=%d smem=%zu\n",
+                B, C, H, W, L, k, dtype, p.status, p.a.nb, p.a.planes_per_cta, p.smem);
+    if (p.status == WTCONV_OK || p.status == WTCONV_ERR_UNSUPPORTED) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache.emplace(key, p);
+    }
+    return p;
+}
+
+// Forward / input-gradient path of a shape (WTCONV_FWD_PATH=fused / tiles / plane selects a path
+// where it applies).  By default the fused whole-plane kernel runs where it measured fastest on
+// GB300: fp32 planes with at least 64 output items and three or more resident CTAs per SM; else
+// the whole-plane kernel where the pyramid fits; else the tiled kernels.
+enum FwdPath { FWD_FUSED, FWD_PLANE, FWD_TILES };
+struct FwdChoice {
+    int status = WTCONV_OK;
+    FwdPath path = FWD_PLANE;
+    PPlan pp;
+    Plan pf;
+};
+
+FwdChoice choose_fwd(int B, int C, int H, int W, int L, int k, int dtype) {
+    FwdChoice f;
+    const char *env = getenv("WTCONV_FWD_PATH");
+    const bool want_fused = env && strcmp(env, "fused") == 0;
+    const bool want_tiles = env && strcmp(env, "tiles") == 0;
+    const bool want_plane = env && strcmp(env, "plane") == 0;
+    if (!want_tiles && !want_plane) {
+        f.pp = plan_plane(B, C, H, W, L, k, dtype);
+        if (f.pp.status != WTCONV_OK && f.pp.status != WTCONV_ERR_UNSUPPORTED) { f.status = f.pp.status; return f; }
+        const bool good = f.pp.status == WTCONV_OK && dtype == WTCONV_F32 && f.pp.occ >= 3 &&
+                          f.pp.a.sg.items_r * f.pp.a.sg.items_c >= 64;
+        if (f.pp.status == WTCONV_OK && (want_fused || good)) {
+            f.path = FWD_FUSED;
+            return f;
+        }
+    }
+    f.pf = plan_forward(B, C, H, W, L, k, dtype);
+    if (f.pf.status == WTCONV_OK && !want_tiles) {
+        f.path = FWD_PLANE;
+        return f;
+    }
+    if (f.pf.status != WTCONV_OK && f.pf.status != WTCONV_ERR_UNSUPPORTED) { f.status = f.pf.status; return f; }
+    f.path = FWD_TILES;
+    return f;
+}
+
 // Which weight-gradient path a call takes: the whole-plane kernel where a plane fits, else the
 // tiled kernels where they apply, else the workspace pyramids.  WTCONV_DW_PATH=tiles, =plane or
 // =pyramid selects a path where it applies (for testing and comparison).
@@ -687,15 +800,50 @@ int wtconv_device_status(void) {
     return WTCONV_ERR_DEVICE_TIMEOUT;
 }
 
+const char *wtconv_plan_kernels(int op, int B, int C, int H, int W, int L, int k, int dtype) {
+    if (validate_shape(B, C, H, W, L, k, dtype) != WTCONV_OK) return "";
+    const bool fwd = op == WTCONV_OP_FORWARD || op == WTCONV_OP_BACKWARD_INPUT;
+    const bool dw = op == WTCONV_OP_BACKWARD_WEIGHTS;
+    const bool both = op == WTCONV_OP_BACKWARD;
+    if (!fwd && !dw && !both) return "";
+    const char *f = "";
+    if (fwd || both) {
+        const FwdChoice fc = choose_fwd(B, C, H, W, L, k, dtype);
+        if (fc.status != WTCONV_OK) return "";
+        f = fc.path == FWD_FUSED ? "wtconv_plane_kernel"
+            : fc.path == FWD_PLANE ? "wtconv_fwd_kernel"
+            : (L >= 2 ? "wtconv_deep_kernel+wtconv_shallow_kernel" : "wtconv_shallow_kernel");
+        if (fwd) return f;
+    }
+    const DwChoice d = choose_dw(B, C, H, W, L, k, dtype);
+    if (d.status != WTCONV_OK) return "";
+    if (dw) {
+        return d.path == DW_PLANE ? "wtconv_dw_kernel+wtconv_dw_finalize_kernel"
+             : d.path == DW_TILE ? "wtconv_dw_tile_kernel+wtconv_level2_kernel+wtconv_haar_level_kernel+"
+                                   "wtconv_dw_corr_kernel+wtconv_dw_finalize_kernel"
+                                 : "wtconv_haar_level_kernel+wtconv_dw_corr_kernel+wtconv_dw_finalize_kernel";
+    }
+    // BACKWARD: the input gradient's kernels, then the weight gradient's (names built once per
+    // combination; static storage)
+    static std::mutex mu;
+    static std::map<std::string, std::string> names;
+    const std::string dws = d.path == DW_PLANE ? "wtconv_dw_kernel+wtconv_dw_finalize_kernel"
+                            : d.path == DW_TILE ? "wtconv_dw_tile_kernel+wtconv_level2_kernel+wtconv_haar_level_kernel+"
+                                                  "wtconv_dw_corr_kernel+wtconv_dw_finalize_kernel"
+                                                : "wtconv_haar_level_kernel+wtconv_dw_corr_kernel+wtconv_dw_finalize_kernel";
+    const std::string key = std::string(f) + "+" + dws;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = names.emplace(key, key).first;
+    return it->second.c_str();
+}
+
 int wtconv_launch_count(int op, int B, int C, int H, int W, int L, int k, int dtype) {
     if (validate_shape(B, C, H, W, L, k, dtype) != WTCONV_OK) return 0;
     int n = 0;
     if (op == WTCONV_OP_FORWARD || op == WTCONV_OP_BACKWARD_INPUT || op == WTCONV_OP_BACKWARD) {
-        const Plan pf = plan_forward(B, C, H, W, L, k, dtype);
-        if (pf.status == WTCONV_OK && !tiles_forced()) n += 1;
-        else if (pf.status == WTCONV_OK) n += L >= 2 ? 2 : 1;
-        else if (pf.status == WTCONV_ERR_UNSUPPORTED) n += L >= 2 ? 2 : 1;
-        else return 0;
+        const FwdChoice f = choose_fwd(B, C, H, W, L, k, dtype);
+        if (f.status != WTCONV_OK) return 0;
+        n += f.path == FWD_TILES ? (L >= 2 ? 2 : 1) : 1;
     }
     if (op == WTCONV_OP_BACKWARD_WEIGHTS || op == WTCONV_OP_BACKWARD) {
         const DwChoice d = choose_dw(B, C, H, W, L, k, dtype);
@@ -713,10 +861,27 @@ static int run_operator(int B, int C, int H, int W, int L, int k, int dtype, con
                         const float *base_bias, const float *base_scale, const float *wavelet_w,
                         const float *wavelet_scale, void *dst, bool flip, void *workspace, size_t workspace_bytes,
                         cudaStream_t s) {
-    // planes whose whole pyramid fits in shared memory: one kernel, no workspace (unless
-    // WTCONV_FWD_PATH=tiles asks for the tiled kernels)
-    Plan pf = plan_forward(B, C, H, W, L, k, dtype);
-    if (pf.status == WTCONV_OK && !tiles_forced()) {
+    const FwdChoice fc = choose_fwd(B, C, H, W, L, k, dtype);
+    if (fc.status != WTCONV_OK) return fc.status;
+    if (fc.path == FWD_FUSED) {
+        PPlan pp = fc.pp;
+        PlaneArgs &a = pp.a;
+        a.x = src;
+        a.out = dst;
+        a.base_w = base_w; a.base_bias = base_bias; a.base_scale = base_scale;
+        a.wavelet_w = wavelet_w; a.wavelet_scale = wavelet_scale;
+        a.flip = flip ? 1 : 0;
+        a.with_bias = flip ? 0 : 1;
+        a.timeout = timeout_flag();
+        if (a.timeout == nullptr) return WTCONV_ERR_CUDA;
+        const int eb = elem_bytes(dtype);
+        if (!encode_map(&a.tmap_x, tma_dtype(dtype), eb, src, W, H, C, B, a.sg.xw, a.sg.xrows, 1))
+            return WTCONV_ERR_CUDA;
+        return cuda_status(launch_plane(a, dtype, pp.smem, s));
+    }
+    if (fc.path == FWD_PLANE) {
+        // planes whose whole pyramid fits in shared memory: one kernel, no workspace
+        Plan pf = fc.pf;
         pf.a.x = src;
         pf.a.out = dst;
         set_params(pf.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
@@ -724,7 +889,6 @@ static int run_operator(int B, int C, int H, int W, int L, int k, int dtype, con
         pf.a.with_bias = flip ? 0 : 1;
         return cuda_status(launch_forward(pf.a, dtype, pf.smem, s));
     }
-    if (pf.status != WTCONV_OK && pf.status != WTCONV_ERR_UNSUPPORTED) return pf.status;
     const size_t dbytes = deep_bytes(B, C, H, W, L);
     Plan pd;
     if (L >= 2) {

@@ -9,7 +9,7 @@
 // Each CTA owns channel c and a run of batch entries in groups of G planes.  Per group: one read
 // of each plane builds level 2 (from 4 x 4 pixel blocks) and the deeper levels on chip; every
 // level's subband-pair convs run as sliding-window items; D is written once.
-#include "wtconv_analysis.cuh"
+#include "wtconv_items.cuh"
 
 namespace wtconv {
 
@@ -62,61 +62,6 @@ __device__ __forceinline__ void deep_analysis_from_global(const LayerArgs &a, co
                 ll[a2][b2] = (v[2 * a2][2 * b2] + v[2 * a2][2 * b2 + 1]) + (v[2 * a2 + 1][2 * b2] + v[2 * a2 + 1][2 * b2 + 1]);
         float *slot = slots + (size_t)g * geo.slot_floats;
         put_quad_pairs(slot, geo, geo.off_y, 2, bi, bj, butterfly(ll[0][0], ll[0][1], ll[1][0], ll[1][1]));
-    }
-}
-
-// D[i][j0 .. j0+7] (level-1 positions, j0 % 8 == 0) from the deep levels' conv outputs.
-__device__ __forceinline__ void deep_gather8(const Geo &geo, const float *slot, int i, int j0, float (&out)[8]) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) out[c] = 0.f;
-    {   // level 2 (relative level 1): four positions; row bit = bit 0 of i, column bit = c & 1
-        const float *z = slot + geo.off_z[2] + 2 * ((i >> 1) * geo.zpitch[2] + (j0 >> 1));
-        const float4 a01 = *reinterpret_cast<const float4 *>(z), b01 = *reinterpret_cast<const float4 *>(z + 4);
-        const float *z2 = z + geo.zimg[2];
-        const float4 a23 = *reinterpret_cast<const float4 *>(z2), b23 = *reinterpret_cast<const float4 *>(z2 + 4);
-        const float ll[4] = {a01.x, a01.z, b01.x, b01.z}, lh[4] = {a01.y, a01.w, b01.y, b01.w};
-        const float hl[4] = {a23.x, a23.z, b23.x, b23.z}, hh[4] = {a23.y, a23.w, b23.y, b23.w};
-        const bool ra = i & 1;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float p = ra ? ll[q] - hl[q] : ll[q] + hl[q];
-            const float r = ra ? lh[q] - hh[q] : lh[q] + hh[q];
-            out[2 * q] += p + r;
-            out[2 * q + 1] += p - r;
-        }
-    }
-    if (geo.L >= 3) {  // level 3: two positions, column bit = bit 1 of c
-        const float *z = slot + geo.off_z[3] + 2 * ((i >> 2) * geo.zpitch[3] + (j0 >> 2));
-        const float4 a01 = *reinterpret_cast<const float4 *>(z);
-        const float4 a23 = *reinterpret_cast<const float4 *>(z + geo.zimg[3]);
-        const bool ra = (i >> 1) & 1;
-        const float p0 = ra ? a01.x - a23.x : a01.x + a23.x, r0 = ra ? a01.y - a23.y : a01.y + a23.y;
-        const float p1 = ra ? a01.z - a23.z : a01.z + a23.z, r1 = ra ? a01.w - a23.w : a01.w + a23.w;
-        const float s0 = p0 + r0, d0 = p0 - r0, s1 = p1 + r1, d1 = p1 - r1;
-        out[0] += s0; out[1] += s0; out[2] += d0; out[3] += d0;
-        out[4] += s1; out[5] += s1; out[6] += d1; out[7] += d1;
-    }
-    float lo = 0.f, hi = 0.f;  // levels >= 4: one position, constant over each half (level 4) or all 8
-    for (int l = 4; l <= geo.L; ++l) {
-        const int t = l - 1;  // level relative to the level-1 grid
-        const float *z = slot + geo.off_z[l] + 2 * ((i >> t) * geo.zpitch[l] + (j0 >> t));
-        const float2 a01 = *reinterpret_cast<const float2 *>(z);
-        const float2 a23 = *reinterpret_cast<const float2 *>(z + geo.zimg[l]);
-        const bool ra = (i >> (t - 1)) & 1;
-        const float p = ra ? a01.x - a23.x : a01.x + a23.x, r = ra ? a01.y - a23.y : a01.y + a23.y;
-        if (t == 3) {
-            lo += p + r;
-            hi += p - r;
-        } else {
-            const float v = ((j0 >> (t - 1)) & 1) ? p - r : p + r;
-            lo += v;
-            hi += v;
-        }
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        out[c] += lo;
-        out[c + 4] += hi;
     }
 }
 

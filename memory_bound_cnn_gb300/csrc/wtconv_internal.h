@@ -250,6 +250,29 @@ struct DwTileArgs {
     int *timeout;
     CUtensorMap tmap_x, tmap_dy;   // x: box xw x xrows x 1 x G at (c0 - padx, r0 - 2P); dy: TW x TH x 1 x G
 };
+// Fused whole-plane forward / input-gradient kernel: one plane per CTA iteration, its whole
+// pyramid on chip, the fused output items of the shallow kernel.
+constexpr int kPlaneThreads = 128;
+struct PlaneArgs {
+    int B, C, H, W, L, K;
+    int nb, planes_per_cta;        // grid = nb * C; CTA n takes batch entries n*ppc .. n*ppc + ppc - 1
+    int st_mode;                   // 1: 4-element vector stores where a row allows
+    const void *x;                 // forward: x; input gradient: dy
+    void *out;                     // y or dx
+    const float *base_w, *base_bias, *base_scale, *wavelet_w, *wavelet_scale;
+    int flip, with_bias;
+    ShallowGeo sg;                 // the whole plane as one tile (TH >= H, TW >= W, G = 1)
+    Geo dg;                        // levels >= 2 slot (L >= 2)
+    int dpitch;                    // row pitch (floats) of D, the deep contribution at level-1 resolution
+    int n_deep_items;              // conv items of the levels >= 2 images
+    int deep_item_start[1 + 2 * kMaxLevels + 1];  // first item of conv image ci (ci = 3 .. 2L), then the end
+    int *timeout;
+    CUtensorMap tmap_x;            // box xw x xrows x 1 x 1 at (-padx, -2P, c, b)
+};
+size_t plane_smem_bytes(const PlaneArgs &a, int elem_bytes);
+cudaError_t launch_plane(const PlaneArgs &a, int dtype, size_t smem, cudaStream_t st);
+int occupancy_plane(int dtype, int K, size_t smem);
+
 size_t dw_tile_smem_bytes(const ShallowGeo &sg, int elem_bytes);
 cudaError_t launch_dw_tile(const DwTileArgs &a, int dtype, size_t smem, cudaStream_t st);
 int occupancy_dw_tile(int dtype, int K, size_t smem);

@@ -20,7 +20,7 @@
 //      and stores each output pixel once.
 // The G planes of a unit are stacked vertically in X and in the pair images, so the per-unit
 // loops index rows of one tall image.
-#include "wtconv_device.cuh"
+#include "wtconv_items.cuh"
 
 namespace wtconv {
 
@@ -33,97 +33,6 @@ size_t shallow_smem_bytes(const ShallowGeo &sg, int K, bool convert, bool deep) 
     if (convert) bytes += (size_t)sg.xbuf * sizeof(float);
     bytes += (size_t)sg.G * sg.pslot * sizeof(float);
     return bytes + (size_t)3 * wpairs(K) * sizeof(f2_t);
-}
-
-// cp.async of `N` bytes (4, 8 or 16); src_bytes = 0 zero-fills the destination without reading.
-template <int N>
-__device__ __forceinline__ void cp_async_n(void *smem_dst, const void *gmem_src, int src_bytes) {
-    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
-    if constexpr (N == 16)
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gmem_src), "r"(src_bytes) : "memory");
-    else
-        asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(d), "l"(gmem_src), "n"(N), "r"(src_bytes)
-                     : "memory");
-}
-
-// Level-1 conv of one subband-pair image for 4 coefficient rows x 2 positions, kept in registers.
-template <int K>
-__device__ __forceinline__ void level1_item(const float *__restrict__ in, int pitch, const f2_t *wsm,
-                                            f2_t (&z)[4][kColsL]) {
-    constexpr int NV = (kColsL + K - 1 + 1) / 2;
-    f2_t w[K * K];
-    load_weights<K>(wsm, w);
-#pragma unroll
-    for (int i = 0; i < 4 + K - 1; ++i) {
-        f2_t x[2 * NV];
-        load_pair_row<NV>(in + 2 * i * pitch, x);
-#pragma unroll
-        for (int v = 0; v < K; ++v) {
-#pragma unroll
-            for (int u = 0; u < K; ++u) {
-                const int j = i - u;
-                if (j >= 0 && j < 4) {
-#pragma unroll
-                    for (int q = 0; q < kColsL; ++q) {
-                        if (u == 0 && v == 0) z[j][q] = fmul2(w[0], x[q]);
-                        else ffma2_acc(z[j][q], w[u * K + v], x[q + v]);
-                    }
-                }
-            }
-        }
-    }
-}
-
-// Base conv of one 8 x 4 pixel block on top of `init`, each finished row rounded and stored:
-// out[r][c] = init[r][c] + sum_{u,v} w[u][v] * X[r + u][c + v - P].  `in` points at the 16-byte
-// aligned X position 4 - P columns left of the window origin (window row r, column 0); three
-// 16-byte loads per window row cover columns 0 .. 11 of that, the window is columns
-// 4 - P .. 4 - P + 3 + K - 1.
-template <int K, typename T>
-__device__ __forceinline__ void base_item_store(const float *__restrict__ in, int pitch, const f2_t *wsm,
-                                                const f2_t (&init)[kRows][2], T *dst, int ld, int nrows,
-                                                int ncols, bool vec) {
-    constexpr int P = K / 2, O = 4 - P;
-    f2_t w[K * K];
-    load_weights<K>(wsm, w);
-    f2_t acc[kRows][2];
-#pragma unroll
-    for (int i = 0; i < kRows + K - 1; ++i) {
-        f2_t e[6], o[5];
-        load_row<3>(in + i * pitch, e, o);
-#pragma unroll
-        for (int v = 0; v < K; ++v) {
-#pragma unroll
-            for (int u = 0; u < K; ++u) {
-                const int j = i - u;
-                if (j >= 0 && j < kRows) {
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const int s0 = O + v + 2 * q;  // first column of the pair
-                        const f2_t xv = (s0 & 1) ? o[(s0 - 1) / 2] : e[s0 / 2];
-                        if (u == 0 && v == 0) acc[j][q] = ffma2(w[0], xv, init[j][q]);
-                        else ffma2_acc(acc[j][q], w[u * K + v], xv);
-                    }
-                }
-            }
-        }
-        const int jd = i - (K - 1);
-        if (jd >= 0 && jd < nrows) {
-            const float vals[4] = {lo2(acc[jd][0]), hi2(acc[jd][0]), lo2(acc[jd][1]), hi2(acc[jd][1])};
-            T *d = dst + (size_t)jd * ld;
-            if (vec && ncols == 4) {
-                Act<T>::st4(d, vals);
-            } else {
-                for (int c = 0; c < ncols; ++c) Act<T>::st(d + c, vals[c]);
-            }
-        }
-    }
-}
-
-// Four narrow activations (8 bytes) to fp32.
-template <typename T>
-__device__ __forceinline__ float4 cvt4(const T *p) {
-    return Act<T>::ld4(p);
 }
 
 template <int K, typename T>

@@ -7,7 +7,7 @@ call raises.
 
 Functions carry the C names: ``wtconv_forward``, ``wtconv_backward_input``,
 ``wtconv_backward_weights``, ``wtconv_backward``, ``wtconv_backward_weights_noalloc``,
-``wtconv_workspace_size``, ``wtconv_launch_count``, ``wtconv_device_status``,
+``wtconv_workspace_size``, ``wtconv_launch_count``, ``wtconv_plan_kernels``, ``wtconv_device_status``,
 ``wtconv_strerror``, ``wtconv_version``.  ``WTConvFunction`` wraps forward and the fused
 backward as a ``torch.autograd.Function``.
 """
@@ -30,7 +30,8 @@ DTYPE_CODE = {v: k for k, v in TORCH_DTYPE.items()}
 
 EXPORTED = ("wtconv_version", "wtconv_strerror", "wtconv_workspace_size", "wtconv_forward",
             "wtconv_backward_input", "wtconv_backward_weights", "wtconv_backward",
-            "wtconv_backward_weights_noalloc", "wtconv_launch_count", "wtconv_device_status")
+            "wtconv_backward_weights_noalloc", "wtconv_launch_count", "wtconv_device_status",
+            "wtconv_plan_kernels")
 
 _lib = None
 
@@ -65,6 +66,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.wtconv_strerror.argtypes = [i]
     lib.wtconv_workspace_size.restype = sz
     lib.wtconv_workspace_size.argtypes = [i] * 8
+    lib.wtconv_plan_kernels.restype = ctypes.c_char_p
+    lib.wtconv_plan_kernels.argtypes = [i] * 8
     lib.wtconv_device_status.restype = i
     lib.wtconv_device_status.argtypes = []
     lib.wtconv_launch_count.restype = i
@@ -95,6 +98,12 @@ def wtconv_strerror(status: int) -> str:
 
 def wtconv_workspace_size(op: int, B: int, C: int, H: int, W: int, L: int, k: int, dtype: int) -> int:
     return load().wtconv_workspace_size(op, B, C, H, W, L, k, dtype)
+
+
+def wtconv_plan_kernels(op: int, B: int, C: int, H: int, W: int, L: int, k: int, dtype: int) -> list[str]:
+    """Kernels `op` launches for this shape, in launch order."""
+    names = load().wtconv_plan_kernels(op, B, C, H, W, L, k, dtype).decode()
+    return names.split("+") if names else []
 
 
 def wtconv_device_status() -> int:

@@ -37,13 +37,13 @@ def fwd_path(path: str):
 
 def check_layer(shape: LayerShape, inputs: dict, split: bool = True):
     """Forward, fused backward and (if `split`) the separate backward entry points against the
-    oracle, on the default kernels and again with the tiled forward / input-gradient kernels
-    forced (where the whole-plane kernel would be chosen by default)."""
+    oracle, on the default kernels and again with the tiled and the fused whole-plane forward /
+    input-gradient kernels selected (where they apply)."""
     tol = TOL[shape.dtype]
     d = to_device(inputs)
     y_ref = oracle.forward(inputs["x"], inputs)
     g_ref = oracle.backward(inputs["x"], inputs["dy"], inputs)
-    for path in ("default", "tiles"):
+    for path in ("default", "tiles", "fused"):
         with fwd_path(path):
             y = gpu_forward(d)
             dx, g = gpu_backward(d)
@@ -128,7 +128,7 @@ def test_input_gradient_is_forward_with_rotated_kernels():
     assert_close("dx vs rotated forward", np64(dx), np64(y), 1e-6)
 
 
-@pytest.mark.parametrize("path", ["default", "tiles"])
+@pytest.mark.parametrize("path", ["default", "tiles", "fused"])
 def test_outputs_stay_in_bounds_and_inputs_untouched(path):
     """Canary words around every output; inputs byte-identical after the calls."""
     shape = LayerShape(3, 5, 24, 16, 3, 5, "bf16")
