@@ -112,6 +112,13 @@ __global__ void __launch_bounds__(kPlaneThreads, (K <= 5 ? 4 : 2)) wtconv_plane_
     const float bias = a.with_bias ? a.base_scale[c] * a.base_bias[c] : 0.f;
     const bool vec_st = a.st_mode >= 1;
     const int n_fused = sg.items_r * sg.items_c;
+    // per-thread coordinates of the analysis loops (computed once: no division per element)
+    const int a_rstep = sg.ycols >= nt ? 1 : nt / sg.ycols;
+    const int a_threads = sg.ycols >= nt ? nt : a_rstep * sg.ycols;
+    const int a_row0 = sg.ycols >= nt ? 0 : tid / sg.ycols, a_col0 = sg.ycols >= nt ? tid : tid - a_row0 * sg.ycols;
+    const int w2c = L >= 2 ? a.dg.w[2] : 1;  // level-2 positions: thread tid starts at (tid / w2, tid % w2)
+    const int l2_row0 = tid / w2c, l2_col0 = tid - l2_row0 * w2c;
+    const int l2_drow = nt / w2c, l2_dcol = nt - l2_drow * w2c;
 
     for (int b = b_begin; b < b_end; ++b) {
         if (!mbar_wait(&bar, (uint32_t)(b - b_begin) & 1, a.timeout)) break;
@@ -129,30 +136,33 @@ __global__ void __launch_bounds__(kPlaneThreads, (K <= 5 ? 4 : 2)) wtconv_plane_
             }
             __syncthreads();
         }
-        // level 1 (+ halo) -> pair images: position (ya, yb) from X rows 2 ya, 2 ya + 1
-        {
-            const int n = sg.yrows * sg.ycols;
-            for (int i0 = tid; i0 < n; i0 += 4 * nt) {
-                f2_t t0[4], t1[4];
+        // level 1 (+ halo) -> pair images: position (ya, yb) from X rows 2 ya, 2 ya + 1; a thread
+        // keeps one column and walks rows (loads of four rows first, then the stores)
+        if (tid < a_threads) {
+            for (int col = a_col0; col < sg.ycols; col += nt) {
+                const float *xs = X + sg.padx - 2 * P + 2 * col + (2 * a_row0) * sg.xw;
+                float *y0 = pairs + 2 * (a_row0 * sg.ypitch + col);
+                for (int ya = a_row0; ya < sg.yrows; ya += 4 * a_rstep) {
+                    f2_t t0[4], t1[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int i = i0 + q * nt < n ? i0 + q * nt : i0;
-                    const int ya = i / sg.ycols, yb = i - ya * sg.ycols;
-                    const float *xs = X + sg.padx - 2 * P + 2 * yb + 2 * ya * sg.xw;
-                    t0[q] = *reinterpret_cast<const f2_t *>(xs);
-                    t1[q] = *reinterpret_cast<const f2_t *>(xs + sg.xw);
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int i = i0 + q * nt;
-                    if (i < n) {
-                        const int ya = i / sg.ycols, yb = i - ya * sg.ycols;
-                        const f2_t sv = fadd2(t0[q], t1[q]), dv = fsub2(t0[q], t1[q]);
-                        const float a0 = lo2(sv), a1 = hi2(sv), d0 = lo2(dv), d1 = hi2(dv);
-                        float *y0 = pairs + 2 * (ya * sg.ypitch + yb);
-                        *reinterpret_cast<float2 *>(y0) = make_float2(a0 + a1, a0 - a1);
-                        *reinterpret_cast<float2 *>(y0 + sg.yimg) = make_float2(d0 + d1, d0 - d1);
+                    for (int q = 0; q < 4; ++q) {
+                        const bool in = ya + q * a_rstep < sg.yrows;
+                        const float *xq = xs + (in ? 2 * q * a_rstep * sg.xw : 0);
+                        t0[q] = *reinterpret_cast<const f2_t *>(xq);
+                        t1[q] = *reinterpret_cast<const f2_t *>(xq + sg.xw);
                     }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (ya + q * a_rstep < sg.yrows) {
+                            const f2_t sv = fadd2(t0[q], t1[q]), dv = fsub2(t0[q], t1[q]);
+                            const float a0 = lo2(sv), a1 = hi2(sv), d0 = lo2(dv), d1 = hi2(dv);
+                            float *yq = y0 + 2 * q * a_rstep * sg.ypitch;
+                            *reinterpret_cast<float2 *>(yq) = make_float2(a0 + a1, a0 - a1);
+                            *reinterpret_cast<float2 *>(yq + sg.yimg) = make_float2(d0 + d1, d0 - d1);
+                        }
+                    }
+                    xs += 8 * a_rstep * sg.xw;
+                    y0 += 8 * a_rstep * sg.ypitch;
                 }
             }
         }
@@ -161,11 +171,13 @@ __global__ void __launch_bounds__(kPlaneThreads, (K <= 5 ? 4 : 2)) wtconv_plane_
             // level 2 from the level-1 low band (pair image 0, even floats; interior position
             // (i, j) of level 1 sits at (i + P, j + P))
             const int h2 = dg.h[2], w2 = dg.w[2];
-            for (int i = tid; i < h2 * w2; i += nt) {
-                const int bi = i / w2, bj = i - bi * w2;
+            for (int bi = l2_row0, bj = l2_col0; bi < h2; ) {
                 const float *l1 = pairs + 2 * ((2 * bi + P) * sg.ypitch + 2 * bj + P);
                 const Quad q = butterfly(l1[0], l1[2], l1[2 * sg.ypitch], l1[2 * sg.ypitch + 2]);
                 put_quad_pairs(dslot, dg, dg.off_y, 2, bi, bj, q);
+                bj += l2_dcol;
+                bi += l2_drow;
+                if (bj >= w2) { bj -= w2; ++bi; }
             }
             __syncthreads();
             for (int l = 3; l <= L; ++l) {
