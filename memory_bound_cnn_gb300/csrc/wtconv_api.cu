@@ -506,9 +506,12 @@ TPlan plan_dw_tile_uncached(int B, int C, int H, int W, int L, int k, int dtype)
     if (sms <= 0 || occ <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
     const int tiles = sg.tiles_r * sg.tiles_c;
     a.units = ((B + sg.G - 1) / sg.G) * tiles;
+    // CTAs per channel: minimise (waves) x (units per CTA) over at most two waves of resident
+    // CTAs -- every CTA per channel adds a row of partials and a CTA to each level correlation
     const long long slots = (long long)sms * occ;
+    const long long nb_max = std::max(1LL, std::min((long long)a.units, 2 * slots / C));
     long long best_nb = 1, best_cost = -1;
-    for (long long nb = 1; nb <= a.units; ++nb) {
+    for (long long nb = 1; nb <= nb_max; ++nb) {
         const long long cost = ((C * nb + slots - 1) / slots) * ((a.units + nb - 1) / nb);
         if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_nb = nb; }
     }
