@@ -4,7 +4,7 @@ This module draws random numbers and casts them to the activation dtype; it hold
 layer's arithmetic.  Both the CUDA path (through the binding) and the CPU oracle consume the very
 same host tensors made here, so a parity check compares the two on identical inputs.
 
-Distributions (the paper's WTConvNeXt-style layer settings as restated for this build):
+Distributions (WTConvNeXt-style layer settings; the second argument of N is the variance):
   x ~ N(0, 1); base_w and wavelet_w ~ N(0, 1/k^2) (variance; std 0.2 at k = 5);
   base_bias ~ N(0, 0.1) (variance); base_scale ~ U(0.5, 1.5); wavelet_scale ~ U(0.05, 0.2)
   per subband channel (4C per level); dy ~ N(0, 1).
