@@ -65,12 +65,17 @@ __device__ __forceinline__ float analysis_from_global(const LayerArgs &a, const 
             float *slot = slots + (size_t)g * geo.slot_floats;
             float *X = slot + x_off + (4 * bi + P) * xp + 4 * bj + P;
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
+            for (int r = 0; r < 4; ++r) {
+                if constexpr ((P & 1) == 0) {  // 8-byte aligned: two wide stores (fewer bank conflicts)
+                    *reinterpret_cast<float2 *>(X + r * xp) = make_float2(v[r][0], v[r][1]);
+                    *reinterpret_cast<float2 *>(X + r * xp + 2) = make_float2(v[r][2], v[r][3]);
+                } else {
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    X[r * xp + cc] = v[r][cc];
-                    sum += v[r][cc];
+                    for (int cc = 0; cc < 4; ++cc) X[r * xp + cc] = v[r][cc];
                 }
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) sum += v[r][cc];
+            }
             Quad q[2][2];
 #pragma unroll
             for (int a2 = 0; a2 < 2; ++a2)
