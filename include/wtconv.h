@@ -42,10 +42,13 @@
  *     kernel (fp32 planes where it is fastest), the whole-plane kernel (planes whose pyramid fits
  *     in shared memory), or two tiled kernels (larger planes).  WTCONV_FWD_PATH=fused, =plane or
  *     =tiles selects a set where it applies (same results within fp32 rounding).
- *   - The weight gradients run a whole-plane kernel where both planes' pyramids fit in shared
- *     memory, else tiled kernels (tiles with bulk tensor copies, levels >= 2 on their pyramids in
- *     the workspace), else workspace pyramids for every level.  WTCONV_DW_PATH=tiles or =pyramid
- *     selects those paths where they apply (same results within fp32 rounding).
+ *   - The weight gradients run the fused whole-plane kernel (x and dy planes moved by bulk
+ *     tensor copies, both pyramids on chip; planes of at least 64 base items where both copies
+ *     fit one box of at most 256 x 256), else a staged whole-plane kernel where both planes'
+ *     pyramids fit in shared memory, else tiled kernels (tiles with bulk tensor copies, levels
+ *     >= 2 on their pyramids in the workspace), else workspace pyramids for every level.
+ *     WTCONV_DW_PATH=fused, =plane, =tiles or =pyramid selects a path where it applies (same
+ *     results within fp32 rounding).
  *   - Setting the environment variable WTCONV_INJECT_FAULT=1 makes every compute entry point
  *     return WTCONV_ERR_INJECTED before launching anything (host-side fault injection).
  */

@@ -628,6 +628,122 @@ PPlan plan_plane(int B, int C, int H, int W, int L, int k, int dtype) {
     return p;
 }
 
+// Fused whole-plane weight gradient: x (+ halo) and dy each move as one bulk tensor copy, both
+// pyramids fit in shared memory.  Threads: whole warps for the base path's items, then one run
+// of threads per level pair image; the split minimises the items per thread per plane.
+struct FPlan {
+    int status = WTCONV_OK;
+    DwPlaneArgs a{};
+    size_t smem = 0;
+    int occ = 0;
+    size_t partial_bytes = 0;
+};
+
+FPlan plan_dw_fused_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
+    FPlan p;
+    DwPlaneArgs &a = p.a;
+    a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
+    const int eb = elem_bytes(dtype);
+    const int e16 = 16 / eb;
+    if (((size_t)W * eb) % 16 != 0) { p.status = WTCONV_ERR_UNSUPPORTED; return p; }
+    const int TW = round_up(W, e16 > 4 ? e16 : 4), TH = round_up(H, kRows);
+    a.sg = make_shallow_geo(H, W, k, TH, TW, 1, eb, e16, 4);
+    const ShallowGeo &sg = a.sg;
+    if (((size_t)sg.xw * eb) % 16 != 0 || ((size_t)sg.padx * eb) % 16 != 0 || ((size_t)TW * eb) % 16 != 0 ||
+        sg.xw > 256 || sg.xrows > 256 || TW > 256 || TH > 256) {
+        p.status = WTCONV_ERR_UNSUPPORTED;
+        return p;
+    }
+    a.th1 = round_up(TH / 2, kRows);
+    a.y1rows = a.th1 + 2 * (k / 2);
+    a.dg = make_geo(H, W, L, k, 3);
+    // thread split: CTA size, base warps and items per thread minimising the item rounds per plane
+    // (ties: fewer threads)
+    const int nbase = sg.items_r * sg.items_c;
+    int best_nt = 0, best_wb = -1, best_pb = 0, best_pl = 0, best_span = 0;
+    for (int nt = 256; nt <= kDwPlaneMaxThreads; nt += 32) {
+        for (int wb = 1; 32 * wb < nt; ++wb) {
+            const int pb = ceil_div(nbase, 32 * wb), avail = nt - 32 * wb;
+            int pl = 1;
+            for (;; ++pl) {
+                int need = 0;
+                for (int l = 1; l <= L; ++l) need += 2 * ceil_div(a.dg.rseg[l] * a.dg.cstr[l], pl);
+                if (need <= avail) break;
+            }
+            const int span = std::max(pb, pl);
+            if (best_wb < 0 || span < best_span) {
+                best_nt = nt; best_wb = wb; best_pb = pb; best_pl = pl; best_span = span;
+            }
+        }
+    }
+    a.nthreads = best_nt;
+    a.per_thread_base = best_pb;
+    a.per_thread = best_pl;
+    a.tstart[0] = 0;
+    a.tstart[1] = 32 * best_wb;
+    for (int ci = 1; ci < 1 + 2 * L; ++ci) {
+        const int l = (ci - 1) / 2 + 1;
+        a.tstart[ci + 1] = a.tstart[ci] + ceil_div(a.dg.rseg[l] * a.dg.cstr[l], best_pl);
+    }
+    // two copy buffers where that keeps as many CTAs resident per SM as one
+    a.nbuf = 1;
+    p.smem = dw_plane_smem_bytes(a, eb);
+    if (p.smem + kStaticSmemMargin > (size_t)kMaxSmem) { p.status = WTCONV_ERR_UNSUPPORTED; return p; }
+    const int sms = device_sms();
+    int occ = occupancy_dw_plane(dtype, k, p.smem, a.nthreads);
+    if (sms <= 0 || occ <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
+    {
+        DwPlaneArgs a2 = a;
+        a2.nbuf = 2;
+        const size_t smem2 = dw_plane_smem_bytes(a2, eb);
+        if (smem2 + kStaticSmemMargin <= (size_t)kMaxSmem && occupancy_dw_plane(dtype, k, smem2, a.nthreads) >= occ) {
+            a.nbuf = 2;
+            p.smem = smem2;
+        }
+    }
+    p.occ = occ;
+    const long long slots = (long long)sms * occ;
+    long long best_nb = 1, best_cost = -1;
+    for (long long nb = 1; nb <= B; ++nb) {
+        const long long cost = ((C * nb + slots - 1) / slots) * ((B + nb - 1) / nb);
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_nb = nb; }
+    }
+    a.planes_per_cta = (int)((B + best_nb - 1) / best_nb);
+    a.nb = (B + a.planes_per_cta - 1) / a.planes_per_cta;
+    p.partial_bytes = ((size_t)a.nb * C * (1 + 4 * L) * (k * k + 1) * sizeof(float) + 255) / 256 * 256;
+    return p;
+}
+
+FPlan plan_dw_fused(int B, int C, int H, int W, int L, int k, int dtype) {
+    static std::mutex mu;
+    static std::map<PlanKey, FPlan> cache;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        FPlan p;
+        p.status = WTCONV_ERR_CUDA;
+        return p;
+    }
+    const PlanKey key(8, B, C, H, W, L, k, dtype, dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    FPlan p = plan_dw_fused_uncached(B, C, H, W, L, k, dtype);
+    const char *verbose = getenv("WTCONV_VERBOSE");
+    if (verbose && verbose[0] == '1')
+        fprintf(stderr,
+                "wtconv plan dw fused B=%d C=%d H=%d W=%d L=%d k=%d dtype=%d: status %d nb=%d planes/cta=%d "
+                "smem=%zu occ=%d buffers %d items/thread base %d levels %d, threads %d of %d\n",
+                B, C, H, W, L, k, dtype, p.status, p.a.nb, p.a.planes_per_cta, p.smem, p.occ, p.a.nbuf,
+                p.a.per_thread_base, p.a.per_thread, p.a.tstart[1 + 2 * L], p.a.nthreads);
+    if (p.status == WTCONV_OK || p.status == WTCONV_ERR_UNSUPPORTED) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache.emplace(key, p);
+    }
+    return p;
+}
+
 // Forward / input-gradient path of a shape (WTCONV_FWD_PATH=fused / tiles / plane selects a path
 // where it applies).  By default the fused whole-plane kernel runs where it measured fastest on
 // GB300: fp32 planes with at least 64 output items and three or more resident CTAs per SM; else
@@ -666,23 +782,43 @@ FwdChoice choose_fwd(int B, int C, int H, int W, int L, int k, int dtype) {
     return f;
 }
 
-// Which weight-gradient path a call takes: the whole-plane kernel where a plane fits, else the
-// tiled kernels where they apply, else the workspace pyramids.  WTCONV_DW_PATH=tiles, =plane or
-// =pyramid selects a path where it applies (for testing and comparison).
-enum DwPath { DW_TILE, DW_PLANE, DW_PYRAMID };
+// Which weight-gradient path a call takes: the fused whole-plane kernel where it applies and
+// measured fastest, else the whole-plane kernel where a plane fits, else the tiled kernels where
+// they apply, else the workspace pyramids.  WTCONV_DW_PATH=fused, =tiles, =plane or =pyramid
+// selects a path where it applies (for testing and comparison).
+enum DwPath { DW_TILE, DW_PLANE, DW_PYRAMID, DW_FUSED };
 struct DwChoice {
     int status = WTCONV_OK;
     DwPath path = DW_PLANE;
     TPlan t;
     Plan p;
+    FPlan f;
     size_t workspace = 0;
 };
+
+// Where the fused kernel measured faster than the staged whole-plane kernel on GB300: fp32
+// planes of at least 64 base items with two resident CTAs per SM (narrow types and larger
+// planes ran up to 2x slower).
+bool dw_fused_default(const FPlan &f, int dtype) {
+    return f.status == WTCONV_OK && dtype == WTCONV_F32 && f.occ >= 2 && f.a.sg.items_r * f.a.sg.items_c >= 64;
+}
 
 DwChoice choose_dw(int B, int C, int H, int W, int L, int k, int dtype) {
     DwChoice d;
     const char *env = getenv("WTCONV_DW_PATH");
     const bool want_tiles = env && strcmp(env, "tiles") == 0;
     const bool want_pyramid = env && strcmp(env, "pyramid") == 0;
+    const bool want_fused = env && strcmp(env, "fused") == 0;
+    const bool want_plane = env && strcmp(env, "plane") == 0;
+    if (!want_tiles && !want_pyramid && !want_plane) {
+        d.f = plan_dw_fused(B, C, H, W, L, k, dtype);
+        if (d.f.status != WTCONV_OK && d.f.status != WTCONV_ERR_UNSUPPORTED) { d.status = d.f.status; return d; }
+        if (d.f.status == WTCONV_OK && (want_fused || dw_fused_default(d.f, dtype))) {
+            d.path = DW_FUSED;
+            d.workspace = d.f.partial_bytes;
+            return d;
+        }
+    }
     if (!want_tiles && !want_pyramid) {
         d.p = plan_dw(B, C, H, W, L, k, dtype);
         if (d.p.status != WTCONV_OK) { d.status = d.p.status; return d; }
@@ -821,7 +957,8 @@ const char *wtconv_plan_kernels(int op, int B, int C, int H, int W, int L, int k
     const DwChoice d = choose_dw(B, C, H, W, L, k, dtype);
     if (d.status != WTCONV_OK) return "";
     if (dw) {
-        return d.path == DW_PLANE ? "wtconv_dw_kernel+wtconv_dw_finalize_kernel"
+        return d.path == DW_FUSED ? "wtconv_dw_plane_kernel+wtconv_dw_finalize_kernel"
+             : d.path == DW_PLANE ? "wtconv_dw_kernel+wtconv_dw_finalize_kernel"
              : d.path == DW_TILE ? "wtconv_dw_tile_kernel+wtconv_level2_kernel+wtconv_haar_level_kernel+"
                                    "wtconv_dw_corr_kernel+wtconv_dw_finalize_kernel"
                                  : "wtconv_haar_level_kernel+wtconv_dw_corr_kernel+wtconv_dw_finalize_kernel";
@@ -830,7 +967,8 @@ const char *wtconv_plan_kernels(int op, int B, int C, int H, int W, int L, int k
     // combination; static storage)
     static std::mutex mu;
     static std::map<std::string, std::string> names;
-    const std::string dws = d.path == DW_PLANE ? "wtconv_dw_kernel+wtconv_dw_finalize_kernel"
+    const std::string dws = d.path == DW_FUSED ? "wtconv_dw_plane_kernel+wtconv_dw_finalize_kernel"
+                            : d.path == DW_PLANE ? "wtconv_dw_kernel+wtconv_dw_finalize_kernel"
                             : d.path == DW_TILE ? "wtconv_dw_tile_kernel+wtconv_level2_kernel+wtconv_haar_level_kernel+"
                                                   "wtconv_dw_corr_kernel+wtconv_dw_finalize_kernel"
                                                 : "wtconv_haar_level_kernel+wtconv_dw_corr_kernel+wtconv_dw_finalize_kernel";
@@ -954,6 +1092,24 @@ int wtconv_backward_input(int B, int C, int H, int W, int L, int k, int dtype, c
                         true, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// Fused whole-plane weight-gradient kernel into `partials`; fills what the finalize reads.
+static int run_dw_fused(FPlan &fp, int dtype, const void *x, const void *dy, float *partials, LayerArgs &fin,
+                        cudaStream_t s) {
+    DwPlaneArgs &f = fp.a;
+    const int eb = elem_bytes(dtype);
+    f.partials = partials;
+    f.timeout = timeout_flag();
+    if (f.timeout == nullptr) return WTCONV_ERR_CUDA;
+    if (!encode_map(&f.tmap_x, tma_dtype(dtype), eb, x, f.W, f.H, f.C, f.B, f.sg.xw, f.sg.xrows, 1) ||
+        !encode_map(&f.tmap_dy, tma_dtype(dtype), eb, dy, f.W, f.H, f.C, f.B, f.sg.TW, f.sg.TH, 1))
+        return WTCONV_ERR_CUDA;
+    if (launch_dw_plane(f, dtype, fp.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+    fin.B = f.B; fin.C = f.C; fin.H = f.H; fin.W = f.W; fin.L = f.L; fin.K = f.K;
+    fin.nb = f.nb;
+    fin.partials = partials;
+    return WTCONV_OK;
+}
+
 static int backward_common(bool want_dx, int B, int C, int H, int W, int L, int k, int dtype, const void *x,
                            const void *dy, const float *base_w, const float *base_bias, const float *base_scale,
                            const float *wavelet_w, const float *wavelet_scale, void *dx, float *d_base_w,
@@ -1009,6 +1165,9 @@ static int backward_common(bool want_dx, int B, int C, int H, int W, int L, int 
         fin.B = B; fin.C = C; fin.H = H; fin.W = W; fin.L = L; fin.K = k;
         fin.nb = t.nb;
         fin.partials = t.partials;
+    } else if (dc.path == DW_FUSED) {
+        st = run_dw_fused(dc.f, dtype, x, dy, reinterpret_cast<float *>(wsp), fin, s);
+        if (st != WTCONV_OK) return st;
     } else if (dc.path == DW_PYRAMID) {
         Plan &pw = dc.p;
         DwPyramidArgs d{};
@@ -1059,17 +1218,28 @@ int wtconv_backward_weights_noalloc(int B, int C, int H, int W, int L, int k, in
         !params_ok(d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale))
         return WTCONV_ERR_INVALID_ARG;
     if (fault_injected()) return WTCONV_ERR_INJECTED;
-    Plan pw = plan_dw(B, C, H, W, L, k, dtype);
-    if (pw.status != WTCONV_OK) return pw.status;
-    if (pw.dw_pyramid || pw.workspace > sizeof(g_noalloc_scratch)) return WTCONV_ERR_SCRATCH_LIMIT;
+    // the same kernels as wtconv_backward_weights where they need nothing but the partials
+    DwChoice dc = choose_dw(B, C, H, W, L, k, dtype);
+    if (dc.status != WTCONV_OK) return dc.status;
+    if ((dc.path != DW_FUSED && dc.path != DW_PLANE) || dc.workspace > sizeof(g_noalloc_scratch))
+        return WTCONV_ERR_SCRATCH_LIMIT;
     void *scratch = noalloc_scratch();
     if (scratch == nullptr) return WTCONV_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    pw.a.x = x; pw.a.dy = dy;
-    set_params(pw.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
-    pw.a.partials = static_cast<float *>(scratch);
-    if (launch_dw(pw.a, dtype, pw.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
-    return cuda_status(launch_dw_finalize(pw.a, d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale, s));
+    LayerArgs fin{};
+    if (dc.path == DW_FUSED) {
+        st = run_dw_fused(dc.f, dtype, x, dy, static_cast<float *>(scratch), fin, s);
+        if (st != WTCONV_OK) return st;
+    } else {
+        Plan &pw = dc.p;
+        pw.a.x = x; pw.a.dy = dy;
+        set_params(pw.a, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
+        pw.a.partials = static_cast<float *>(scratch);
+        if (launch_dw(pw.a, dtype, pw.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+        fin = pw.a;
+    }
+    set_params(fin, base_w, base_bias, base_scale, wavelet_w, wavelet_scale);
+    return cuda_status(launch_dw_finalize(fin, d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale, s));
 }
 
 int wtconv_backward(int B, int C, int H, int W, int L, int k, int dtype, const void *x, const void *dy,

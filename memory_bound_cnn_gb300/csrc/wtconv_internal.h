@@ -47,6 +47,7 @@ struct Geo {
 // kind 0: forward / input-gradient slot (x, pyramid, conv outputs, base buffer)
 // kind 1: weight-gradient slot (x, dy and both pyramids)
 // kind 2: deep slot (levels >= 2 only: pyramid and conv outputs; no full-resolution plane)
+// kind 3: weight-gradient deep slot (levels >= 2 only: both pyramids)
 __host__ __device__ inline Geo make_geo(int H, int W, int L, int K, int kind) {
     Geo g = {};
     g.H = H; g.W = W; g.L = L; g.K = K; g.P = K / 2;
@@ -69,9 +70,9 @@ __host__ __device__ inline Geo make_geo(int H, int W, int L, int K, int kind) {
         }
     }
     int off = 0;
-    const int l0 = kind == 2 ? 2 : 1;  // first stored level
+    const int l0 = kind >= 2 ? 2 : 1;  // first stored level
     g.off_x = -1;
-    if (kind != 2) { g.off_x = off; off += g.rows[0] * g.pitch[0]; }
+    if (kind < 2) { g.off_x = off; off += g.rows[0] * g.pitch[0]; }
     g.off_dy = -1;
     g.off_base = -1;
     if (kind == 1) { g.off_dy = off; off += g.rows[0] * g.pitch[0]; }
@@ -81,7 +82,7 @@ __host__ __device__ inline Geo make_geo(int H, int W, int L, int K, int kind) {
     }
     for (int l = 1; l <= L; ++l) {
         g.off_g[l] = -1;
-        if (kind == 1) { g.off_g[l] = off; off += 2 * g.pimg[l]; }
+        if (kind == 1 || (kind == 3 && l >= 2)) { g.off_g[l] = off; off += 2 * g.pimg[l]; }
     }
     for (int l = 1; l <= L; ++l) {
         g.off_z[l] = -1;
@@ -272,6 +273,30 @@ struct PlaneArgs {
 size_t plane_smem_bytes(const PlaneArgs &a, int elem_bytes);
 cudaError_t launch_plane(const PlaneArgs &a, int dtype, size_t smem, cudaStream_t st);
 int occupancy_plane(int dtype, int K, size_t smem);
+
+// Fused whole-plane weight gradient: one plane of x and of dy per CTA iteration, both pyramids on
+// chip, every thread pinned to a share of one correlation's items for the whole CTA.
+constexpr int kDwPlaneMaxThreads = 256;
+struct DwPlaneArgs {
+    int B, C, H, W, L, K;
+    int nthreads;                  // CTA size: a multiple of 32, at most kDwPlaneMaxThreads
+    int nb, planes_per_cta;        // grid = nb * C
+    int nbuf;                      // copy buffers: 2 = the next plane's copies overlap this plane's work
+    float *partials;               // [nb][C][1+4L][K*K+1]
+    ShallowGeo sg;                 // x as one tile with a 2P halo (TH >= H, TW >= W, G = 1)
+    int th1;                       // level-1 rows padded to the 8-row items: round_up(TH / 2, 8)
+    int y1rows;                    // rows of every level-1 pair image (x and dy): th1 + 2P, pitch sg.ypitch
+    Geo dg;                        // levels >= 2, both pyramids (kind 3)
+    int per_thread_base;           // base-path items each base thread takes per plane
+    int per_thread;                // items of its pair image each level thread takes per plane
+    int tstart[1 + 2 * kMaxLevels + 1];  // first thread of correlation image ci (base, then level
+                                         // l pair p at 1 + 2(l-1) + p), then the end
+    int *timeout;
+    CUtensorMap tmap_x, tmap_dy;   // x: box xw x xrows x 1 x 1 at (-padx, -2P); dy: TW x TH x 1 x 1 at (0, 0)
+};
+size_t dw_plane_smem_bytes(const DwPlaneArgs &a, int elem_bytes);
+cudaError_t launch_dw_plane(const DwPlaneArgs &a, int dtype, size_t smem, cudaStream_t st);
+int occupancy_dw_plane(int dtype, int K, size_t smem, int nthreads);
 
 size_t dw_tile_smem_bytes(const ShallowGeo &sg, int elem_bytes);
 cudaError_t launch_dw_tile(const DwTileArgs &a, int dtype, size_t smem, cudaStream_t st);

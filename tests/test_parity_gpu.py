@@ -59,8 +59,9 @@ def check_layer(shape: LayerShape, inputs: dict, split: bool = True):
         assert_close("dx (backward_input)", np64(dx2), g_ref["dx"], tol)
         for n in GRADS:
             assert_close(n + " (backward_weights)", np64(g2[n]), g_ref[n], tol)
-    # the weight gradient's other paths: tiled kernels (where they apply) and workspace pyramids
-    for dpath in ("tiles", "pyramid"):
+    # the weight gradient's other paths (where they apply): the fused whole-plane kernel, the
+    # staged whole-plane kernel, tiled kernels and workspace pyramids
+    for dpath in ("fused", "plane", "tiles", "pyramid"):
         if dpath == "pyramid" and shape.numel > 20_000_000:
             continue  # the pyramid path already runs by default where planes are too large
         with env_path("WTCONV_DW_PATH", dpath):
@@ -103,8 +104,10 @@ def test_shape_sweep(case):
     check_layer(shape, make_inputs(shape, seed=11))
 
 
-def test_backward_is_deterministic():
-    shape = LayerShape(8, 16, 28, 28, 2, 5, "bf16")
+@pytest.mark.parametrize("case", [(8, 16, 28, 28, 2, 5, "bf16"), (4, 8, 56, 56, 3, 5, "f32")],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_backward_is_deterministic(case):
+    shape = LayerShape(*case)
     d = to_device(make_inputs(shape, seed=3))
     dx1, g1 = gpu_backward(d)
     dx2, g2 = gpu_backward(d)
