@@ -336,6 +336,10 @@ def run_gpu(args, world, rank, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": per_step * args.steps,
         "clocks": clk.summary(),
+        # device memory a step needs beyond the inputs and parameters: y, dx, the gradients and
+        # the workspace of every layer (the autograd arms report the same quantity)
+        "step_mem_bytes": int(sum(out["y"].nbytes + out["dx"].nbytes + ws.nbytes +
+                                  sum(g.nbytes for g in out["grads"].values()) for _, _, _, ws, out in layers)),
     }
     return line
 
@@ -477,9 +481,43 @@ def run_torch_cascade(args, world, rank, local):
             y = torch_cascade(d["x"], *[d[n] for n in PARAMS])
             y.backward(d["dy"])
 
+    leaves = [t for _, d in layers for t in [d["x"]] + [d[n] for n in PARAMS]]
+    line = time_autograd_arm(args, world, dev, layers, step, leaves)
+    # one more step with its forward and backward inside NVTX ranges, so that a profiler can
+    # attribute the DRAM traffic of each (the backward runs on autograd's own thread: a
+    # process-wide start/end range)
+    for s, d in layers:
+        torch.cuda.synchronize(dev)
+        torch.cuda.nvtx.range_push("cascade_fwd")
+        y = torch_cascade(d["x"], *[d[n] for n in PARAMS])
+        torch.cuda.synchronize(dev)
+        torch.cuda.nvtx.range_pop()
+        rid = torch.cuda.nvtx.range_start("cascade_bwd")
+        y.backward(d["dy"])
+        torch.cuda.synchronize(dev)
+        torch.cuda.nvtx.range_end(rid)
+    line.update({"impl": "torch-cascade",
+                 "note": "PyTorch grouped convs (PyTorch's depthwise kernels or cuDNN, as PyTorch picks; no TF32) + "
+                         "autograd of the reference cascade; comparison arm"})
+    return line
+
+
+def time_autograd_arm(args, world, dev, layers, step, leaves):
+    """Warm-up, the device memory one step allocates at its peak beyond what exists before it
+    (activations saved for the backward, outputs, the gradients of `leaves`), then event-timed
+    steps."""
+    shapes = WORKLOADS[args.workload]
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
+    for t in leaves:
+        t.grad = None
+    torch.cuda.synchronize(dev)
+    before = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    step()
+    torch.cuda.synchronize(dev)
+    step_mem = torch.cuda.max_memory_allocated(dev) - before
     steps = max(3, min(args.steps, 20))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -492,12 +530,46 @@ def run_torch_cascade(args, world, rank, local):
     elements = sum(s.numel for s, _ in layers)
     value = whole_job_throughput(elements, world, ms / 1e3)
     return {
-        "impl": "torch-cascade", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": shapes[0].dtype, "data": "synthetic",
         "config": {"workload": args.workload, "layers": [s.as_dict() for s in shapes]},
-        "note": "PyTorch grouped convs (cuDNN, no TF32) + autograd of the reference cascade; comparison arm",
+        "step_mem_bytes": int(step_mem),
     }
+
+
+def run_dwconv(args, world, rank, local, k=7):
+    """fwd + bwd of a plain depthwise k x k conv with bias (torch conv2d, groups=C: PyTorch's
+    depthwise kernels or cuDNN, as PyTorch picks; no TF32) at the workload's shapes: the layer
+    WTConv replaces, timed for context."""
+    import torch.nn.functional as F
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    torch.backends.cudnn.allow_tf32 = False
+    torch.backends.cuda.matmul.allow_tf32 = False
+    g = torch.Generator().manual_seed(0)
+    layers = []
+    for i, s in enumerate(WORKLOADS[args.workload]):
+        d = {k2: v.to(dev) for k2, v in make_inputs(s, seed=i).items() if k2 in ("x", "dy")}
+        act = d["x"].dtype
+        d["w"] = (torch.randn(s.C, 1, k, k, generator=g) / k).to(dev, act).requires_grad_(True)
+        d["b"] = (torch.randn(s.C, generator=g) * 0.1).to(dev, act).requires_grad_(True)
+        d["x"].requires_grad_(True)
+        layers.append((s, d))
+
+    def step():
+        for s, d in layers:
+            for t in (d["x"], d["w"], d["b"]):
+                t.grad = None
+            y = F.conv2d(d["x"], d["w"], d["b"], padding=k // 2, groups=s.C)
+            y.backward(d["dy"])
+
+    leaves = [t for _, d in layers for t in (d["x"], d["w"], d["b"])]
+    line = time_autograd_arm(args, world, dev, layers, step, leaves)
+    line.update({"impl": f"dwconv{k}",
+                 "note": f"plain depthwise {k}x{k} conv + bias (torch conv2d groups=C, no TF32), "
+                         "fwd+bwd at the same shapes; context, not the product"})
+    return line
 
 
 def main(argv=None):
@@ -505,7 +577,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", choices=("cuda", "reference", "torch-cascade"), default="cuda")
+    ap.add_argument("--impl", choices=("cuda", "reference", "torch-cascade", "dwconv7"), default="cuda")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stage1_f32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -520,6 +592,8 @@ def main(argv=None):
             line = run_reference(args, world, rank)
         elif args.impl == "torch-cascade":
             line = run_torch_cascade(args, world, rank, local)
+        elif args.impl == "dwconv7":
+            line = run_dwconv(args, world, rank, local, k=7)
         else:
             W.load()
             line = run_gpu(args, world, rank, local)
