@@ -27,6 +27,10 @@
  *     subband, then inverts the transform.
  *   - Base path: y_base = base_scale * (conv(x, base_w) + base_bias): the bias is scaled too
  *     ("folded into the weights, and into the bias for the base path").
+ *   - Odd sides: a level whose input has an odd number of rows (columns) pads it with one zero
+ *     row (column) at the end before the analysis, as the stride-2 'SAME' Haar conv of the page-4
+ *     snippet does, so level l has ceil(n_(l-1) / 2) positions per side; the synthesis crops each
+ *     level's reconstruction back to the size of that level's input.
  *
  * Parity status: the pages print no worked example, so nothing here is pinned to printed
  * values.  Every function is pinned by the tests to mathematics instead (perfect
@@ -161,6 +165,20 @@ static void dwconv_adjoint_kernel(const double *d_out, int H, int W, const doubl
 
 /* ------------------------------------------------------------ per-plane pipeline -------- */
 
+#define ORACLE_MAX_LEVELS 16
+
+/* Side lengths of every level: hs[0] = H, hs[l] = ceil(hs[l-1] / 2) (odd sides padded with one
+ * zero at the end before the analysis); likewise ws. */
+static void level_sizes(int H, int W, int L, int *hs, int *ws)
+{
+    hs[0] = H;
+    ws[0] = W;
+    for (int l = 1; l <= L; ++l) {
+        hs[l] = (hs[l - 1] + 1) / 2;
+        ws[l] = (ws[l - 1] + 1) / 2;
+    }
+}
+
 typedef struct {
     int B, C, H, W, L, k;
     const double *x, *dy;
@@ -177,7 +195,8 @@ typedef struct {
     double **Y;     /* Y[l]: [4][H_l][W_l], analysis coefficients of level l (1-based) */
     double **T;     /* T[l]: conv outputs before the scale */
     double **Z;     /* Z[l]: scaled conv outputs (LL later receives the reconstruction) */
-    double *R, *R2; /* reconstruction buffers, up to H x W */
+    double *R, *R2; /* reconstruction buffers, up to 2*hs[1] x 2*ws[1] */
+    double *Pd;     /* a level's input padded to even sides */
     double *base;   /* conv(x, base_w) */
     double **dZ, **dT, **dY;
     double *dR, *dR2, *dbase;
@@ -186,7 +205,9 @@ typedef struct {
 static int scratch_alloc(scratch_t *s, int H, int W, int L)
 {
     memset(s, 0, sizeof(*s));
-    size_t HW = (size_t)H * W;
+    int hs[ORACLE_MAX_LEVELS + 1], ws[ORACLE_MAX_LEVELS + 1];
+    level_sizes(H, W, L, hs, ws);
+    size_t HW = (size_t)H * W, HW2 = (size_t)(2 * hs[1]) * (2 * ws[1]);
     s->Y = calloc((size_t)L + 1, sizeof(double *));
     s->T = calloc((size_t)L + 1, sizeof(double *));
     s->Z = calloc((size_t)L + 1, sizeof(double *));
@@ -196,7 +217,7 @@ static int scratch_alloc(scratch_t *s, int H, int W, int L)
     if (!s->Y || !s->T || !s->Z || !s->dZ || !s->dT || !s->dY)
         return -1;
     for (int l = 1; l <= L; ++l) {
-        size_t n = 4 * (size_t)(H >> l) * (size_t)(W >> l);
+        size_t n = 4 * (size_t)hs[l] * (size_t)ws[l];
         s->Y[l] = malloc(n * sizeof(double));
         s->T[l] = malloc(n * sizeof(double));
         s->Z[l] = malloc(n * sizeof(double));
@@ -206,13 +227,14 @@ static int scratch_alloc(scratch_t *s, int H, int W, int L)
         if (!s->Y[l] || !s->T[l] || !s->Z[l] || !s->dZ[l] || !s->dT[l] || !s->dY[l])
             return -1;
     }
-    s->R = malloc(HW * sizeof(double));
-    s->R2 = malloc(HW * sizeof(double));
+    s->R = malloc(HW2 * sizeof(double));
+    s->R2 = malloc(HW2 * sizeof(double));
+    s->Pd = malloc(HW2 * sizeof(double));
     s->base = malloc(HW * sizeof(double));
-    s->dR = malloc(HW * sizeof(double));
-    s->dR2 = malloc(HW * sizeof(double));
+    s->dR = malloc(HW2 * sizeof(double));
+    s->dR2 = malloc(HW2 * sizeof(double));
     s->dbase = malloc(HW * sizeof(double));
-    if (!s->R || !s->R2 || !s->base || !s->dR || !s->dR2 || !s->dbase)
+    if (!s->R || !s->R2 || !s->Pd || !s->base || !s->dR || !s->dR2 || !s->dbase)
         return -1;
     return 0;
 }
@@ -228,7 +250,7 @@ static void scratch_free(scratch_t *s, int L)
         if (s->dY) free(s->dY[l]);
     }
     free(s->Y); free(s->T); free(s->Z); free(s->dZ); free(s->dT); free(s->dY);
-    free(s->R); free(s->R2); free(s->base); free(s->dR); free(s->dR2); free(s->dbase);
+    free(s->R); free(s->R2); free(s->Pd); free(s->base); free(s->dR); free(s->dR2); free(s->dbase);
 }
 
 /* Forward of one (b, c) plane through the reference pipeline. Leaves the materialised
@@ -237,17 +259,29 @@ static void plane_forward(const job_t *J, int c, const double *x, double *y, scr
 {
     int H = J->H, W = J->W, L = J->L, k = J->k, C = J->C;
     size_t kk = (size_t)k * k;
+    int hs[ORACLE_MAX_LEVELS + 1], ws[ORACLE_MAX_LEVELS + 1];
+    level_sizes(H, W, L, hs, ws);
 
-    /* (1) analysis cascade: Y^(l) = WT(LL_(l-1)), LL_0 = x, LL_l = subband 0 of Y^(l) */
+    /* (1) analysis cascade: Y^(l) = WT(LL_(l-1)), LL_0 = x, LL_l = subband 0 of Y^(l); an odd
+     *     side of LL_(l-1) gets one zero row / column at its end first */
     const double *LL = x;
     for (int l = 1; l <= L; ++l) {
-        oracle_haar_analysis(LL, H >> (l - 1), W >> (l - 1), s->Y[l]);
-        LL = s->Y[l]; /* subband 0 is the first [H_l][W_l] block */
+        int hi = hs[l - 1], wi = ws[l - 1], h = hs[l], w = ws[l];
+        if (hi == 2 * h && wi == 2 * w) {
+            oracle_haar_analysis(LL, hi, wi, s->Y[l]);
+        } else {
+            memset(s->Pd, 0, (size_t)(2 * h) * (2 * w) * sizeof(double));
+            for (int i = 0; i < hi; ++i)
+                for (int j = 0; j < wi; ++j)
+                    s->Pd[i * (2 * w) + j] = LL[i * wi + j];
+            oracle_haar_analysis(s->Pd, 2 * h, 2 * w, s->Y[l]);
+        }
+        LL = s->Y[l]; /* subband 0 is the first [h_l][w_l] block */
     }
 
     /* (2) depthwise conv per subband, (3) the learned scale as its own pass */
     for (int l = 1; l <= L; ++l) {
-        int h = H >> l, w = W >> l;
+        int h = hs[l], w = ws[l];
         size_t n = (size_t)h * w;
         for (int sb = 0; sb < 4; ++sb) {
             const double *ker = J->wavelet_w + ((size_t)(l - 1) * 4 * C + 4 * c + sb) * kk;
@@ -263,14 +297,16 @@ static void plane_forward(const job_t *J, int c, const double *x, double *y, scr
     /* (4) synthesis cascade, levels L..1: add the previous reconstruction to the LL subband,
      *     then invert the transform. R holds the reconstruction at the current resolution. */
     {
-        int hL = H >> L, wL = W >> L;
-        memset(s->R, 0, (size_t)hL * wL * sizeof(double));
+        memset(s->R, 0, (size_t)hs[L] * ws[L] * sizeof(double));
         for (int l = L; l >= 1; --l) {
-            int h = H >> l, w = W >> l;
+            int h = hs[l], w = ws[l], ho = hs[l - 1], wo = ws[l - 1];
             for (int i = 0; i < h * w; ++i)
                 s->Z[l][i] += s->R[i]; /* subband 0 = LL */
             oracle_haar_synthesis(s->Z[l], h, w, s->R2);
-            memcpy(s->R, s->R2, (size_t)(2 * h) * (2 * w) * sizeof(double));
+            /* back to the size of this level's input (drops a padded row / column) */
+            for (int i = 0; i < ho; ++i)
+                for (int j = 0; j < wo; ++j)
+                    s->R[i * wo + j] = s->R2[i * (2 * w) + j];
         }
     }
 
@@ -290,6 +326,8 @@ static void plane_backward(const job_t *J, int c, const double *x, const double 
     int H = J->H, W = J->W, L = J->L, k = J->k, C = J->C;
     size_t kk = (size_t)k * k, HW = (size_t)H * W;
     double sb_ = J->base_scale[c], bb = J->base_bias[c];
+    int hs[ORACLE_MAX_LEVELS + 1], ws[ORACLE_MAX_LEVELS + 1];
+    level_sizes(H, W, L, hs, ws);
 
     /* (5) base path.  y = sb * (base + bb) + R. */
     double acc_scale = 0.0, acc_bias = 0.0;
@@ -305,20 +343,25 @@ static void plane_backward(const job_t *J, int c, const double *x, const double 
     dwconv_adjoint_input(s->dbase, H, W, J->base_w + (size_t)c * kk, k, dx);
 
     /* (4) synthesis cascade in reverse, levels 1..L.  The forward step at level l was
-     *     Z[l].LL += R_(l+1); R_l = IWT(Z[l]).  Reversed: dZ[l] = IWT^T dR_l, then
-     *     dR_(l+1) = dZ[l].LL (the reconstruction entered the LL subband with weight 1). */
+     *     Z[l].LL += R_(l+1); R_l = crop(IWT(Z[l])).  Reversed: the crop's transpose pads dR_l
+     *     with zeros to 2h x 2w, dZ[l] = IWT^T of that, then dR_(l+1) = dZ[l].LL (the
+     *     reconstruction entered the LL subband with weight 1). */
     memcpy(s->dR, dy, HW * sizeof(double)); /* y = ... + R_1 */
     for (int l = 1; l <= L; ++l) {
-        int h = H >> l, w = W >> l;
+        int h = hs[l], w = ws[l], ho = hs[l - 1], wo = ws[l - 1];
         size_t n = 4 * (size_t)h * w;
+        memset(s->dR2, 0, (size_t)(2 * h) * (2 * w) * sizeof(double));
+        for (int i = 0; i < ho; ++i)
+            for (int j = 0; j < wo; ++j)
+                s->dR2[i * (2 * w) + j] = s->dR[i * wo + j];
         memset(s->dZ[l], 0, n * sizeof(double));
-        haar_synthesis_adjoint(s->dR, h, w, s->dZ[l]);
+        haar_synthesis_adjoint(s->dR2, h, w, s->dZ[l]);
         memcpy(s->dR, s->dZ[l], (size_t)h * w * sizeof(double)); /* LL block */
     }
 
     /* (3) scale pass and (2) conv, per level and subband */
     for (int l = 1; l <= L; ++l) {
-        int h = H >> l, w = W >> l;
+        int h = hs[l], w = ws[l];
         size_t n = (size_t)h * w;
         memset(s->dY[l], 0, 4 * n * sizeof(double));
         for (int sb = 0; sb < 4; ++sb) {
@@ -338,15 +381,19 @@ static void plane_backward(const job_t *J, int c, const double *x, const double 
     }
 
     /* (1) analysis cascade in reverse, levels L..1: LL_l = Y^(l).LL feeds level l+1, so its
-     *     gradient collects from there before flowing through WT^T into LL_(l-1). */
+     *     gradient collects from there before flowing through WT^T into the padded LL_(l-1);
+     *     the padding's transpose then drops the padded row / column. */
     {
-        memset(s->dR2, 0, HW * sizeof(double)); /* dLL_l, starts at zero for l = L */
+        memset(s->dR2, 0, (size_t)hs[L] * ws[L] * sizeof(double)); /* dLL_L = 0 */
         for (int l = L; l >= 1; --l) {
-            int h = H >> l, w = W >> l;
+            int h = hs[l], w = ws[l], hi = hs[l - 1], wi = ws[l - 1];
             for (int i = 0; i < h * w; ++i)
                 s->dY[l][i] += s->dR2[i];
-            memset(s->dR2, 0, (size_t)(2 * h) * (2 * w) * sizeof(double));
-            haar_analysis_adjoint(s->dY[l], 2 * h, 2 * w, s->dR2);
+            memset(s->Pd, 0, (size_t)(2 * h) * (2 * w) * sizeof(double));
+            haar_analysis_adjoint(s->dY[l], 2 * h, 2 * w, s->Pd);
+            for (int i = 0; i < hi; ++i)
+                for (int j = 0; j < wi; ++j)
+                    s->dR2[i * wi + j] = s->Pd[i * (2 * w) + j];
         }
         for (size_t i = 0; i < HW; ++i)
             dx[i] += s->dR2[i]; /* LL_0 = x */
@@ -391,9 +438,7 @@ static void *worker(void *arg)
 
 static int check_shape(int B, int C, int H, int W, int L, int k)
 {
-    if (B <= 0 || C <= 0 || H <= 0 || W <= 0 || L < 1 || k < 1 || (k % 2) == 0)
-        return -1;
-    if ((H % (1 << L)) != 0 || (W % (1 << L)) != 0)
+    if (B <= 0 || C <= 0 || H <= 0 || W <= 0 || L < 1 || L > ORACLE_MAX_LEVELS || k < 1 || (k % 2) == 0)
         return -1;
     return 0;
 }

@@ -177,24 +177,38 @@ def _conv_matrix(h, w, ker):
     return K
 
 
+def _pad_matrix(h, w):
+    """h x w plane -> the same plane with one zero row / column appended to an odd side."""
+    he, we = h + (h & 1), w + (w & 1)
+    Pm = np.zeros((he * we, h * w))
+    for i in range(h):
+        for j in range(w):
+            Pm[i * we + j, i * w + j] = 1.0
+    return Pm
+
+
 def layer_matrix(p, c, H, W, L):
-    """Dense matrix M of one channel's layer (y = M x + s_b b), stage by stage."""
+    """Dense matrix M of one channel's layer (y = M x + s_b b), stage by stage.  A level whose
+    input has an odd side zero-pads it at the end before the analysis; the synthesis is the
+    transpose of that (the transposed Haar conv, then the crop back to the input size)."""
     n0 = H * W
     ll = np.eye(n0)                      # maps x -> LL_(l-1)
     Zs, As = [], []
+    h, w = H, W                          # sides of LL_(l-1)
     for lvl in range(1, L + 1):
-        h, w = H >> (lvl - 1), W >> (lvl - 1)
-        A = _analysis_matrix(h, w)
+        he, we = h + (h & 1), w + (w & 1)
+        A = _analysis_matrix(he, we) @ _pad_matrix(h, w)
         Y = A @ ll                       # maps x -> Y^(l)
-        m = (h // 2) * (w // 2)
+        h, w = he // 2, we // 2
+        m = h * w
         Z = np.zeros_like(Y)
         for s in range(4):
-            K = _conv_matrix(h // 2, w // 2, p["wavelet_w"][lvl - 1, 4 * c + s])
+            K = _conv_matrix(h, w, p["wavelet_w"][lvl - 1, 4 * c + s])
             Z[s * m:(s + 1) * m] = p["wavelet_scale"][lvl - 1, 4 * c + s] * (K @ Y[s * m:(s + 1) * m])
         Zs.append(Z)
         As.append(A)
         ll = Y[:m]
-    R = np.zeros(((H >> L) * (W >> L), n0))
+    R = np.zeros((h * w, n0))
     for lvl in range(L, 0, -1):
         Z = Zs[lvl - 1].copy()
         m = R.shape[0]
@@ -205,7 +219,8 @@ def layer_matrix(p, c, H, W, L):
 
 def check_dense_matrix(orc):
     rng = np.random.default_rng(6)
-    for (C, H, W, L, k) in ((2, 8, 8, 1, 3), (2, 8, 8, 2, 5), (1, 8, 8, 3, 3), (1, 16, 16, 3, 5)):
+    for (C, H, W, L, k) in ((2, 8, 8, 1, 3), (2, 8, 8, 2, 5), (1, 8, 8, 3, 3), (1, 16, 16, 3, 5),
+                            (2, 7, 5, 2, 3), (1, 5, 9, 3, 3), (1, 3, 6, 2, 5), (1, 11, 1, 2, 3)):
         B = 2
         p = random_params(rng, C, L, k)
         x = rng.standard_normal((B, C, H, W))
@@ -260,6 +275,69 @@ def check_finite_differences(orc):
         assert abs(got - want) <= 1e-10 * max(1.0, abs(want)), f"finite differences dx[{i}]: {got} vs {want}"
 
 
+def check_odd_sides_match_zero_padding(orc):
+    """Per-level padding of odd sides and cropping of the reconstructions equals zero-padding x
+    at its end to multiples of 2^L, running the layer there and cropping y (a padded row or
+    column of a level is never an ancestor of a pixel inside the plane); dx and every parameter
+    gradient likewise (dy padded with zeros)."""
+    rng = np.random.default_rng(11)
+    for (B, C, H, W, L, k) in ((2, 3, 7, 5, 2, 3), (1, 2, 5, 11, 3, 5), (2, 1, 9, 6, 1, 3), (1, 1, 3, 3, 2, 5),
+                               (1, 2, 13, 4, 2, 7)):
+        p = random_params(rng, C, L, k)
+        x = rng.standard_normal((B, C, H, W))
+        dy = rng.standard_normal((B, C, H, W))
+        Hp, Wp = -(-H // 2 ** L) * 2 ** L, -(-W // 2 ** L) * 2 ** L
+        xp = np.zeros((B, C, Hp, Wp))
+        xp[:, :, :H, :W] = x
+        dyp = np.zeros((B, C, Hp, Wp))
+        dyp[:, :, :H, :W] = dy
+        tag = f"{H}x{W} L={L} k={k}"
+        _close(orc.forward(x, p), orc.forward(xp, p)[:, :, :H, :W], 1e-12, f"odd sides y {tag}")
+        g, gp = orc.backward(x, dy, p), orc.backward(xp, dyp, p)
+        _close(g["dx"], gp["dx"][:, :, :H, :W], 1e-12, f"odd sides dx {tag}")
+        for n in g:
+            if n != "dx":
+                _close(g[n], gp[n], 1e-11, f"odd sides {n} {tag}")
+
+
+def check_finite_differences_odd_sides(orc):
+    """Central differences of <dy, y(theta)> on odd sides (every level pads)."""
+    rng = np.random.default_rng(12)
+    B, C, H, W, L, k = 1, 2, 7, 5, 2, 3
+    p = random_params(rng, C, L, k)
+    x = rng.standard_normal((B, C, H, W))
+    dy = rng.standard_normal((B, C, H, W))
+    g = orc.backward(x, dy, p)
+    h = 0.5
+
+    def loss(xx, pp):
+        return float(np.sum(dy * orc.forward(xx, pp, nthreads=1)))
+
+    for name in ("base_w", "base_bias", "base_scale", "wavelet_w", "wavelet_scale"):
+        fd = np.zeros_like(p[name])
+        flat = p[name].reshape(-1)
+        for i in range(flat.size):
+            old = flat[i]
+            flat[i] = old + h
+            lp = loss(x, p)
+            flat[i] = old - h
+            lm = loss(x, p)
+            flat[i] = old
+            fd.reshape(-1)[i] = (lp - lm) / (2 * h)
+        _close(g["d_" + name], fd, 1e-10, f"finite differences (odd sides) d_{name}")
+    xf = x.reshape(-1)
+    for i in range(x.size):
+        old = xf[i]
+        xf[i] = old + h
+        lp = loss(x, p)
+        xf[i] = old - h
+        lm = loss(x, p)
+        xf[i] = old
+        want = (lp - lm) / (2 * h)
+        got = g["dx"].reshape(-1)[i]
+        assert abs(got - want) <= 1e-10 * max(1.0, abs(want)), f"finite differences (odd) dx[{i}]: {got} vs {want}"
+
+
 def check_euler_identities(orc):
     """Homogeneity: sum w*dw = s*ds per subband channel; base: sum w_b dw_b + b db = s_b ds_b;
     <dx, x> = <dy, y - s_b b>."""
@@ -292,6 +370,8 @@ def check_thread_invariance(orc):
 
 
 ALL_CHECKS = [
+    check_odd_sides_match_zero_padding,
+    check_finite_differences_odd_sides,
     check_haar_filters,
     check_perfect_reconstruction,
     check_parseval,

@@ -23,8 +23,16 @@ MUTANTS = [
      "double sc = J->wavelet_scale[(size_t)(l - 1) * 4 * C + 4 * c];"),
     ("reconstruction added to LH instead of LL", "s->Z[l][i] += s->R[i]; /* subband 0 = LL */",
      "s->Z[l][h * w + i] += s->R[i];"),
-    ("next level analyses LH instead of LL", "LL = s->Y[l]; /* subband 0 is the first [H_l][W_l] block */",
-     "LL = s->Y[l] + (size_t)(H >> l) * (W >> l);"),
+    ("next level analyses LH instead of LL", "LL = s->Y[l]; /* subband 0 is the first [h_l][w_l] block */",
+     "LL = s->Y[l] + (size_t)h * w;"),
+    ("odd side padded at the start", "s->Pd[i * (2 * w) + j] = LL[i * wi + j];",
+     "s->Pd[(i + 2 * h - hi) * (2 * w) + j + 2 * w - wi] = LL[i * wi + j];"),
+    ("reconstruction cropped at the start", "s->R[i * wo + j] = s->R2[i * (2 * w) + j];",
+     "s->R[i * wo + j] = s->R2[(i + 2 * h - ho) * (2 * w) + j + 2 * w - wo];"),
+    ("backward: crop transpose pads at the start", "s->dR2[i * (2 * w) + j] = s->dR[i * wo + j];",
+     "s->dR2[(i + 2 * h - ho) * (2 * w) + j + 2 * w - wo] = s->dR[i * wo + j];"),
+    ("backward: pad transpose keeps the end", "s->dR2[i * wi + j] = s->Pd[i * (2 * w) + j];",
+     "s->dR2[i * wi + j] = s->Pd[(i + 2 * h - hi) * (2 * w) + j + 2 * w - wi];"),
     ("base bias not scaled", "y[i] = sb_ * (s->base[i] + bb) + s->R[i];",
      "y[i] = sb_ * s->base[i] + bb + s->R[i];"),
     ("backward: base scale dropped from dbase", "s->dbase[i] = sb_ * dy[i];", "s->dbase[i] = dy[i];"),

@@ -15,6 +15,6 @@ def test_oracle_rejects_bad_shapes():
 
     o = oracle.default()
     rng = np.random.default_rng(0)
-    p = oracle_pins.random_params(rng, 1, 2, 3)
+    p = oracle_pins.random_params(rng, 1, 2, 4)
     with pytest.raises(ValueError):
-        o.forward(np.zeros((1, 1, 6, 8)), p)  # 6 is not divisible by 2^2
+        o.forward(np.zeros((1, 1, 6, 8)), p)  # even k
