@@ -19,7 +19,14 @@
  *
  * Conventions shared by every entry point:
  *   - B, C, H, W > 0; 1 <= L <= WTCONV_MAX_LEVELS; k odd, 1 <= k <= 7 (k in {3, 5, 7} run;
- *     other odd k return WTCONV_ERR_UNSUPPORTED); H and W divisible by 2^L.
+ *     other odd k return WTCONV_ERR_UNSUPPORTED); B*C < 2^31 and Hp*Wp <= 2^30, where Hp, Wp
+ *     are H, W rounded up to multiples of 2^L.
+ *   - Sides that are not multiples of 2^L: a level whose input has an odd side pads it with one
+ *     zero row / column at its end before the analysis (the stride-2 'SAME' Haar conv of the
+ *     page-4 snippet), and the synthesis crops that level's reconstruction back to the input's
+ *     size.  That equals the layer on the plane zero-padded at its end to Hp x Wp, cropped back
+ *     to H x W, which is how it runs: the activations are padded into the workspace (one
+ *     Hp x Wp tensor per activation the call reads or writes), and the results cropped out.
  *   - dtype (WTCONV_F32 / WTCONV_BF16 / WTCONV_F16) is the type of the activations x, y, dy,
  *     dx.  Parameters and parameter gradients are always fp32; all arithmetic is fp32 with
  *     round-to-nearest-even on the final store of a bf16 / fp16 activation.
@@ -107,6 +114,9 @@ int wtconv_device_status(void);
  * (B*C*(H/2)*(W/2)*4 bytes, rounded up to 256): the contribution of the Haar levels >= 2, which a
  * first kernel computes per plane and the second kernel adds to every output pixel.  The weight
  * gradients need one fp32 partial per (CTA, channel, subband, tap); BACKWARD needs both.
+ * Sides that are not multiples of 2^L add the padded activations (each B*C*Hp*Wp elements,
+ * rounded up to 256 bytes): two for FORWARD, BACKWARD_INPUT and BACKWARD_WEIGHTS, three for
+ * BACKWARD.
  * Returns 0 for an invalid shape as well; the compute call then reports the error. */
 size_t wtconv_workspace_size(int op, int B, int C, int H, int W, int L, int k, int dtype);
 
@@ -119,7 +129,9 @@ const char *wtconv_plan_kernels(int op, int B, int C, int H, int W, int L, int k
  * the forward and the input gradient and two for the weight gradients (correlations +
  * finalize); larger planes take two for the forward / input gradient (levels >= 2, then the
  * base conv and level 1) and 2L + 2 for the weight gradients (L pyramid levels, L + 1
- * correlations, finalize).  BACKWARD is the sum of BACKWARD_INPUT and BACKWARD_WEIGHTS. */
+ * correlations, finalize).  BACKWARD is the sum of BACKWARD_INPUT and BACKWARD_WEIGHTS.
+ * Sides that are not multiples of 2^L add the pads and the crop: two launches for
+ * FORWARD, BACKWARD_INPUT and BACKWARD_WEIGHTS, three for BACKWARD. */
 int wtconv_launch_count(int op, int B, int C, int H, int W, int L, int k, int dtype);
 
 /* Forward pass (Metodologia: fused on-chip Haar analysis, folded scales, closed-form
@@ -175,9 +187,10 @@ int wtconv_backward(int B, int C, int H, int W, int L, int k, int dtype, const v
  *     address (cudaGetSymbolAddress) and plans the shape; later calls reuse both.  Make that
  *     first call for each device and shape before any stream capture begins.
  *   - Limit: if this shape needs more scratch than WTCONV_NOALLOC_SCRATCH_BYTES (many channels
- *     and levels, or planes too large for the whole-plane kernel, which need their Haar
- *     pyramids in scratch), the call returns WTCONV_ERR_SCRATCH_LIMIT and launches nothing;
- *     use wtconv_backward_weights with a workspace then.
+ *     and levels, planes too large for the whole-plane kernel, which need their Haar pyramids
+ *     in scratch, or sides that are not multiples of 2^L, which need padded copies of x and
+ *     dy), the call returns WTCONV_ERR_SCRATCH_LIMIT and launches nothing; use
+ *     wtconv_backward_weights with a workspace then.
  *   - Nothing in the scratch has to start at zero: every partial is written before it is read.
  *   - The scratch is shared by every call on the device.  Calls whose execution overlaps (on
  *     different streams, or issued from different host threads without ordering) race on it

@@ -27,12 +27,15 @@ bool fault_injected() {
     return v && v[0] && strcmp(v, "0") != 0;
 }
 
+// Shapes the public entry points accept.  Sides need not be multiples of 2^L: such planes run
+// zero-padded to the next multiples (see PadDims); the limits apply to the padded planes.
 int validate_shape(int B, int C, int H, int W, int L, int k, int dtype) {
     if (B <= 0 || C <= 0 || H <= 0 || W <= 0) return WTCONV_ERR_INVALID_ARG;
     if (L < 1 || L > WTCONV_MAX_LEVELS) return WTCONV_ERR_INVALID_ARG;
     if (k < 1 || (k % 2) == 0) return WTCONV_ERR_INVALID_ARG;
-    if ((H % (1 << L)) != 0 || (W % (1 << L)) != 0) return WTCONV_ERR_INVALID_ARG;
-    if ((long long)B * C > (1LL << 31) - 1 || (long long)H * W > (1LL << 30)) return WTCONV_ERR_INVALID_ARG;
+    if (H > (1 << 30) || W > (1 << 30)) return WTCONV_ERR_INVALID_ARG;
+    const long long m = 1LL << L, Hp = (H + m - 1) / m * m, Wp = (W + m - 1) / m * m;
+    if ((long long)B * C > (1LL << 31) - 1 || Hp * Wp > (1LL << 30)) return WTCONV_ERR_INVALID_ARG;
     if (dtype != WTCONV_F32 && dtype != WTCONV_BF16 && dtype != WTCONV_F16) return WTCONV_ERR_UNSUPPORTED;
     if (k != 3 && k != 5 && k != 7) return WTCONV_ERR_UNSUPPORTED;
     return WTCONV_OK;
@@ -40,6 +43,26 @@ int validate_shape(int B, int C, int H, int W, int L, int k, int dtype) {
 
 bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 bool aligned4(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
+
+// Planes whose sides are not multiples of 2^L run as the plane zero-padded at the end of each
+// side to the next multiples, cropped back (equal to padding each level's odd sides with one zero
+// at the end before the analysis and cropping each reconstruction: a padded row or column is never
+// an ancestor of a pixel inside the plane).  The padded activations live in the workspace.
+struct PadDims {
+    bool on;
+    int Hp, Wp;
+    size_t act_bytes;  // one padded activation tensor, 256-byte rounded
+};
+PadDims pad_dims(int B, int C, int H, int W, int L, int dtype) {
+    PadDims p;
+    const int m = 1 << L;
+    p.Hp = (H + m - 1) / m * m;
+    p.Wp = (W + m - 1) / m * m;
+    p.on = p.Hp != H || p.Wp != W;
+    const size_t eb = dtype == WTCONV_F32 ? 4 : 2;
+    p.act_bytes = ((size_t)B * C * p.Hp * p.Wp * eb + 255) / 256 * 256;
+    return p;
+}
 
 struct Plan {
     int status = WTCONV_OK;
@@ -898,6 +921,26 @@ void *noalloc_scratch() {
 
 }  // namespace
 
+// Workspace of `op` on planes whose sides are multiples of 2^L.
+static int workspace_inner(int op, int B, int C, int H, int W, int L, int k, int dtype, size_t *bytes) {
+    *bytes = 0;
+    if (op != WTCONV_OP_FORWARD && op != WTCONV_OP_BACKWARD_INPUT && op != WTCONV_OP_BACKWARD_WEIGHTS &&
+        op != WTCONV_OP_BACKWARD)
+        return WTCONV_ERR_INVALID_ARG;
+    if (op == WTCONV_OP_FORWARD || op == WTCONV_OP_BACKWARD_INPUT || op == WTCONV_OP_BACKWARD)
+        *bytes += deep_bytes(B, C, H, W, L);
+    if (op == WTCONV_OP_BACKWARD_WEIGHTS || op == WTCONV_OP_BACKWARD) {
+        const DwChoice d = choose_dw(B, C, H, W, L, k, dtype);
+        if (d.status != WTCONV_OK) return d.status;
+        *bytes += d.workspace;
+    }
+    return WTCONV_OK;
+}
+
+// Padded activation tensors `op` keeps in the workspace when the sides are not multiples of 2^L:
+// forward x and y, input gradient dy and dx, weight gradients x and dy, backward x, dy and dx.
+static int pad_buffers(int op) { return op == WTCONV_OP_BACKWARD ? 3 : 2; }
+
 extern "C" {
 
 int wtconv_version(void) { return 100; }
@@ -918,15 +961,10 @@ const char *wtconv_strerror(int status) {
 
 size_t wtconv_workspace_size(int op, int B, int C, int H, int W, int L, int k, int dtype) {
     if (validate_shape(B, C, H, W, L, k, dtype) != WTCONV_OK) return 0;
+    const PadDims pd = pad_dims(B, C, H, W, L, dtype);
     size_t bytes = 0;
-    if (op == WTCONV_OP_FORWARD || op == WTCONV_OP_BACKWARD_INPUT || op == WTCONV_OP_BACKWARD)
-        bytes += deep_bytes(B, C, H, W, L);
-    if (op == WTCONV_OP_BACKWARD_WEIGHTS || op == WTCONV_OP_BACKWARD) {
-        const DwChoice d = choose_dw(B, C, H, W, L, k, dtype);
-        if (d.status != WTCONV_OK) return 0;
-        bytes += d.workspace;
-    }
-    return bytes;
+    if (workspace_inner(op, B, C, pd.Hp, pd.Wp, L, k, dtype, &bytes) != WTCONV_OK) return 0;
+    return bytes + (pd.on ? pad_buffers(op) * pd.act_bytes : 0);
 }
 
 int wtconv_device_status(void) {
@@ -939,8 +977,7 @@ int wtconv_device_status(void) {
     return WTCONV_ERR_DEVICE_TIMEOUT;
 }
 
-const char *wtconv_plan_kernels(int op, int B, int C, int H, int W, int L, int k, int dtype) {
-    if (validate_shape(B, C, H, W, L, k, dtype) != WTCONV_OK) return "";
+static const char *plan_kernels_inner(int op, int B, int C, int H, int W, int L, int k, int dtype) {
     const bool fwd = op == WTCONV_OP_FORWARD || op == WTCONV_OP_BACKWARD_INPUT;
     const bool dw = op == WTCONV_OP_BACKWARD_WEIGHTS;
     const bool both = op == WTCONV_OP_BACKWARD;
@@ -978,8 +1015,34 @@ const char *wtconv_plan_kernels(int op, int B, int C, int H, int W, int L, int k
     return it->second.c_str();
 }
 
+const char *wtconv_plan_kernels(int op, int B, int C, int H, int W, int L, int k, int dtype) {
+    if (validate_shape(B, C, H, W, L, k, dtype) != WTCONV_OK) return "";
+    const PadDims pd = pad_dims(B, C, H, W, L, dtype);
+    const char *inner = plan_kernels_inner(op, B, C, pd.Hp, pd.Wp, L, k, dtype);
+    if (!pd.on || inner[0] == 0) return inner;
+    // padded planes: the pads before, the crop after
+    const bool two_in = op == WTCONV_OP_BACKWARD_WEIGHTS || op == WTCONV_OP_BACKWARD;
+    const bool crop = op != WTCONV_OP_BACKWARD_WEIGHTS;
+    const std::string key = std::string(two_in ? "wtconv_pad_kernel+wtconv_pad_kernel+" : "wtconv_pad_kernel+") +
+                            inner + (crop ? "+wtconv_crop_kernel" : "");
+    static std::mutex mu;
+    static std::map<std::string, std::string> names;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = names.emplace(key, key).first;
+    return it->second.c_str();
+}
+
+static int launch_count_inner(int op, int B, int C, int H, int W, int L, int k, int dtype);
+
 int wtconv_launch_count(int op, int B, int C, int H, int W, int L, int k, int dtype) {
     if (validate_shape(B, C, H, W, L, k, dtype) != WTCONV_OK) return 0;
+    const PadDims pd = pad_dims(B, C, H, W, L, dtype);
+    const int n = launch_count_inner(op, B, C, pd.Hp, pd.Wp, L, k, dtype);
+    if (!pd.on || n == 0) return n;
+    return n + (op == WTCONV_OP_BACKWARD ? 3 : 2);  // pads and crop
+}
+
+static int launch_count_inner(int op, int B, int C, int H, int W, int L, int k, int dtype) {
     int n = 0;
     if (op == WTCONV_OP_FORWARD || op == WTCONV_OP_BACKWARD_INPUT || op == WTCONV_OP_BACKWARD) {
         const FwdChoice f = choose_fwd(B, C, H, W, L, k, dtype);
@@ -1066,6 +1129,27 @@ static int run_operator(int B, int C, int H, int W, int L, int k, int dtype, con
     return cuda_status(launch_shallow(a, dtype, ps.smem, s));
 }
 
+// The operator on planes padded to multiples of 2^L: pad src into the workspace, run, crop into dst.
+static int run_padded_operator(int B, int C, int H, int W, int L, int k, int dtype, const PadDims &pd,
+                               const void *src, const float *base_w, const float *base_bias, const float *base_scale,
+                               const float *wavelet_w, const float *wavelet_scale, void *dst, bool flip,
+                               void *workspace, size_t workspace_bytes, cudaStream_t s) {
+    size_t inner = 0;
+    int st = workspace_inner(flip ? WTCONV_OP_BACKWARD_INPUT : WTCONV_OP_FORWARD, B, C, pd.Hp, pd.Wp, L, k, dtype,
+                             &inner);
+    if (st != WTCONV_OK) return st;
+    const size_t bufs = 2 * pd.act_bytes;
+    if (workspace_bytes < bufs + inner || !aligned16(workspace)) return WTCONV_ERR_WORKSPACE;
+    char *w = static_cast<char *>(workspace);
+    const int eb = elem_bytes(dtype);
+    const long long planes = (long long)B * C;
+    if (launch_pad_planes(src, w, planes, H, W, pd.Hp, pd.Wp, eb, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+    st = run_operator(B, C, pd.Hp, pd.Wp, L, k, dtype, w, base_w, base_bias, base_scale, wavelet_w, wavelet_scale,
+                      w + pd.act_bytes, flip, w + bufs, workspace_bytes - bufs, s);
+    if (st != WTCONV_OK) return st;
+    return cuda_status(launch_crop_planes(w + pd.act_bytes, dst, planes, H, W, pd.Hp, pd.Wp, eb, s));
+}
+
 int wtconv_forward(int B, int C, int H, int W, int L, int k, int dtype, const void *x, const float *base_w,
                    const float *base_bias, const float *base_scale, const float *wavelet_w,
                    const float *wavelet_scale, void *y, void *workspace, size_t workspace_bytes,
@@ -1075,6 +1159,11 @@ int wtconv_forward(int B, int C, int H, int W, int L, int k, int dtype, const vo
     if (!aligned16(x) || !aligned16(y) || !params_ok(base_w, base_bias, base_scale, wavelet_w, wavelet_scale))
         return WTCONV_ERR_INVALID_ARG;
     if (fault_injected()) return WTCONV_ERR_INJECTED;
+    const PadDims pd = pad_dims(B, C, H, W, L, dtype);
+    if (pd.on)
+        return run_padded_operator(B, C, H, W, L, k, dtype, pd, x, base_w, base_bias, base_scale, wavelet_w,
+                                   wavelet_scale, y, false, workspace, workspace_bytes,
+                                   reinterpret_cast<cudaStream_t>(stream));
     return run_operator(B, C, H, W, L, k, dtype, x, base_w, base_bias, base_scale, wavelet_w, wavelet_scale, y,
                         false, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1088,6 +1177,11 @@ int wtconv_backward_input(int B, int C, int H, int W, int L, int k, int dtype, c
     if (!aligned16(dy) || !aligned16(dx) || !params_ok(base_w, base_bias, base_scale, wavelet_w, wavelet_scale))
         return WTCONV_ERR_INVALID_ARG;
     if (fault_injected()) return WTCONV_ERR_INJECTED;
+    const PadDims pd = pad_dims(B, C, H, W, L, dtype);
+    if (pd.on)
+        return run_padded_operator(B, C, H, W, L, k, dtype, pd, dy, base_w, base_bias, base_scale, wavelet_w,
+                                   wavelet_scale, dx, true, workspace, workspace_bytes,
+                                   reinterpret_cast<cudaStream_t>(stream));
     return run_operator(B, C, H, W, L, k, dtype, dy, base_w, base_bias, base_scale, wavelet_w, wavelet_scale, dx,
                         true, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1197,14 +1291,54 @@ static int backward_common(bool want_dx, int B, int C, int H, int W, int L, int 
     return cuda_status(launch_dw_finalize(fin, d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale, s));
 }
 
+// Backward entry points: planes whose sides are multiples of 2^L go straight to backward_common;
+// others are padded into the workspace first (x and dy) and dx is cropped back.
+static int backward_entry(bool want_dx, int B, int C, int H, int W, int L, int k, int dtype, const void *x,
+                          const void *dy, const float *base_w, const float *base_bias, const float *base_scale,
+                          const float *wavelet_w, const float *wavelet_scale, void *dx, float *d_base_w,
+                          float *d_base_bias, float *d_base_scale, float *d_wavelet_w, float *d_wavelet_scale,
+                          void *workspace, size_t workspace_bytes, wtconv_stream_t stream) {
+    int st = validate_shape(B, C, H, W, L, k, dtype);
+    if (st != WTCONV_OK) return st;
+    const PadDims pd = pad_dims(B, C, H, W, L, dtype);
+    if (!pd.on)
+        return backward_common(want_dx, B, C, H, W, L, k, dtype, x, dy, base_w, base_bias, base_scale, wavelet_w,
+                               wavelet_scale, dx, d_base_w, d_base_bias, d_base_scale, d_wavelet_w,
+                               d_wavelet_scale, workspace, workspace_bytes, stream);
+    if (!aligned16(x) || !aligned16(dy) || (want_dx && !aligned16(dx)) ||
+        !params_ok(base_w, base_bias, base_scale, wavelet_w, wavelet_scale) ||
+        !params_ok(d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale))
+        return WTCONV_ERR_INVALID_ARG;
+    if (fault_injected()) return WTCONV_ERR_INJECTED;
+    const int op = want_dx ? WTCONV_OP_BACKWARD : WTCONV_OP_BACKWARD_WEIGHTS;
+    size_t inner = 0;
+    st = workspace_inner(op, B, C, pd.Hp, pd.Wp, L, k, dtype, &inner);
+    if (st != WTCONV_OK) return st;
+    const size_t bufs = pad_buffers(op) * pd.act_bytes;
+    if (workspace_bytes < bufs + inner || !aligned16(workspace)) return WTCONV_ERR_WORKSPACE;
+    char *w = static_cast<char *>(workspace);
+    char *xp = w, *dyp = w + pd.act_bytes, *dxp = want_dx ? w + 2 * pd.act_bytes : nullptr;
+    const int eb = elem_bytes(dtype);
+    const long long planes = (long long)B * C;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_pad_planes(x, xp, planes, H, W, pd.Hp, pd.Wp, eb, s) != cudaSuccess ||
+        launch_pad_planes(dy, dyp, planes, H, W, pd.Hp, pd.Wp, eb, s) != cudaSuccess)
+        return WTCONV_ERR_CUDA;
+    st = backward_common(want_dx, B, C, pd.Hp, pd.Wp, L, k, dtype, xp, dyp, base_w, base_bias, base_scale,
+                         wavelet_w, wavelet_scale, dxp, d_base_w, d_base_bias, d_base_scale, d_wavelet_w,
+                         d_wavelet_scale, w + bufs, workspace_bytes - bufs, stream);
+    if (st != WTCONV_OK || !want_dx) return st;
+    return cuda_status(launch_crop_planes(dxp, dx, planes, H, W, pd.Hp, pd.Wp, eb, s));
+}
+
 int wtconv_backward_weights(int B, int C, int H, int W, int L, int k, int dtype, const void *x, const void *dy,
                             const float *base_w, const float *base_bias, const float *base_scale,
                             const float *wavelet_w, const float *wavelet_scale, float *d_base_w,
                             float *d_base_bias, float *d_base_scale, float *d_wavelet_w, float *d_wavelet_scale,
                             void *workspace, size_t workspace_bytes, wtconv_stream_t stream) {
-    return backward_common(false, B, C, H, W, L, k, dtype, x, dy, base_w, base_bias, base_scale, wavelet_w,
-                           wavelet_scale, nullptr, d_base_w, d_base_bias, d_base_scale, d_wavelet_w,
-                           d_wavelet_scale, workspace, workspace_bytes, stream);
+    return backward_entry(false, B, C, H, W, L, k, dtype, x, dy, base_w, base_bias, base_scale, wavelet_w,
+                          wavelet_scale, nullptr, d_base_w, d_base_bias, d_base_scale, d_wavelet_w,
+                          d_wavelet_scale, workspace, workspace_bytes, stream);
 }
 
 int wtconv_backward_weights_noalloc(int B, int C, int H, int W, int L, int k, int dtype, const void *x,
@@ -1218,6 +1352,7 @@ int wtconv_backward_weights_noalloc(int B, int C, int H, int W, int L, int k, in
         !params_ok(d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale))
         return WTCONV_ERR_INVALID_ARG;
     if (fault_injected()) return WTCONV_ERR_INJECTED;
+    if (pad_dims(B, C, H, W, L, dtype).on) return WTCONV_ERR_SCRATCH_LIMIT;  // padded planes need buffers
     // the same kernels as wtconv_backward_weights where they need nothing but the partials
     DwChoice dc = choose_dw(B, C, H, W, L, k, dtype);
     if (dc.status != WTCONV_OK) return dc.status;
@@ -1247,9 +1382,9 @@ int wtconv_backward(int B, int C, int H, int W, int L, int k, int dtype, const v
                     const float *wavelet_scale, void *dx, float *d_base_w, float *d_base_bias,
                     float *d_base_scale, float *d_wavelet_w, float *d_wavelet_scale, void *workspace,
                     size_t workspace_bytes, wtconv_stream_t stream) {
-    return backward_common(true, B, C, H, W, L, k, dtype, x, dy, base_w, base_bias, base_scale, wavelet_w,
-                           wavelet_scale, dx, d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale,
-                           workspace, workspace_bytes, stream);
+    return backward_entry(true, B, C, H, W, L, k, dtype, x, dy, base_w, base_bias, base_scale, wavelet_w,
+                          wavelet_scale, dx, d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale,
+                          workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

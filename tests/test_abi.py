@@ -45,8 +45,9 @@ def _fwd(lib, B=2, C=3, H=16, Wd=16, L=2, k=5, dt=0, x=FAKE, y=FAKE):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(B=0), W.ERR_INVALID_ARG), (dict(C=-1), W.ERR_INVALID_ARG), (dict(L=0), W.ERR_INVALID_ARG),
-    (dict(L=6), W.ERR_INVALID_ARG), (dict(k=4), W.ERR_INVALID_ARG), (dict(H=12, L=3), W.ERR_INVALID_ARG),
-    (dict(Wd=10, L=2), W.ERR_INVALID_ARG), (dict(x=None), W.ERR_INVALID_ARG),
+    (dict(L=6), W.ERR_INVALID_ARG), (dict(k=4), W.ERR_INVALID_ARG), (dict(H=0), W.ERR_INVALID_ARG),
+    (dict(Wd=-3), W.ERR_INVALID_ARG), (dict(H=1 << 16, Wd=(1 << 14) + 1, L=5), W.ERR_INVALID_ARG),
+    (dict(x=None), W.ERR_INVALID_ARG), (dict(H=13, Wd=7, x=None), W.ERR_INVALID_ARG),
     (dict(y=ctypes.c_void_p(264)), W.ERR_INVALID_ARG), (dict(dt=7), W.ERR_UNSUPPORTED),
     (dict(k=9), W.ERR_UNSUPPORTED), (dict(k=1), W.ERR_UNSUPPORTED),
 ])
@@ -65,13 +66,14 @@ def test_backward_entry_points_reject_invalid_arguments():
                                None, 0, None) == W.ERR_INVALID_ARG
     noalloc = lib.wtconv_backward_weights_noalloc
     assert noalloc(*shape, FAKE, None, *p5, *p5, None) == W.ERR_INVALID_ARG
-    assert noalloc(2, 3, 12, 16, 3, 5, 0, FAKE, FAKE, *p5, *p5, None) == W.ERR_INVALID_ARG
+    assert noalloc(2, 3, 12, 16, 3, 5, 0, FAKE, FAKE, *p5, *p5, None) == W.ERR_SCRATCH_LIMIT  # padded planes
+    assert noalloc(2, 3, 12, 0, 3, 5, 0, FAKE, FAKE, *p5, *p5, None) == W.ERR_INVALID_ARG
     assert noalloc(2, 3, 16, 16, 2, 5, 0, FAKE, FAKE, *p5, FAKE, ctypes.c_void_p(258), FAKE, FAKE, FAKE,
                    None) == W.ERR_INVALID_ARG
 
 
 def test_launch_count_of_invalid_shape_is_zero():
-    assert W.wtconv_launch_count(W.OP_BACKWARD, 2, 3, 12, 16, 3, 5, 0) == 0
+    assert W.wtconv_launch_count(W.OP_BACKWARD, 2, 3, 0, 16, 3, 5, 0) == 0
     assert W.wtconv_launch_count(W.OP_FORWARD, 2, 3, 16, 16, 2, 4, 0) == 0
 
 

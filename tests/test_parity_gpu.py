@@ -95,6 +95,13 @@ SWEEP = [
     (2, 2, 96, 64, 5, 5, "bf16"),
     (2, 3, 6, 130, 1, 5, "f32"),     # rows of more than 32 eight-byte copy chunks
     (2, 2, 4, 98, 1, 3, "bf16"),
+    # sides that are not multiples of 2^L: the planes run zero-padded and are cropped back
+    (2, 3, 7, 9, 2, 3, "f32"),
+    (1, 2, 13, 10, 3, 5, "bf16"),
+    (3, 2, 5, 21, 1, 7, "f16"),
+    (2, 2, 30, 45, 2, 5, "f32"),
+    (2, 3, 57, 55, 3, 5, "f32"),
+    (1, 2, 3, 3, 2, 5, "f32"),
 ]
 
 
@@ -180,10 +187,10 @@ def test_autograd_function_matches_oracle():
 def test_invalid_call_raises_and_writes_nothing(monkeypatch):
     shape = LayerShape(2, 3, 16, 16, 2, 5, "f32")
     d = to_device(make_inputs(shape, seed=1))
-    x_bad = d["x"][:, :, :, :14].contiguous()       # W = 14 is not divisible by 2^L = 4
-    y = torch.full_like(x_bad, 3.0)
+    y = torch.full_like(d["x"], 3.0)
+    bad_w = d["base_w"][:, :4, :4].contiguous()      # an even kernel size
     with pytest.raises(W.WTConvError) as e:
-        W.wtconv_forward(x_bad, *[d[p] for p in PARAMS], y=y)
+        W.wtconv_forward(d["x"], bad_w, *[d[p] for p in PARAMS[1:]], y=y)
     assert e.value.status == W.ERR_INVALID_ARG
     y2 = torch.full_like(d["x"], 3.0)
     monkeypatch.setenv("WTCONV_INJECT_FAULT", "1")
