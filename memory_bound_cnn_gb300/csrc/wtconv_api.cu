@@ -15,6 +15,7 @@
 
 #include "wtconv.h"
 #include "wtconv_internal.h"
+#include "wtconv_pad.h"
 
 using namespace wtconv;
 

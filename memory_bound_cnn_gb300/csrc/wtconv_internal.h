@@ -298,13 +298,6 @@ size_t dw_plane_smem_bytes(const DwPlaneArgs &a, int elem_bytes);
 cudaError_t launch_dw_plane(const DwPlaneArgs &a, int dtype, size_t smem, cudaStream_t st);
 int occupancy_dw_plane(int dtype, int K, size_t smem, int nthreads);
 
-// Planes whose sides are not multiples of 2^L: zero padding at the end of each side into a
-// [planes][Hp][Wp] buffer, and the crop back to [planes][H][W] (elements of 2 or 4 bytes).
-cudaError_t launch_pad_planes(const void *src, void *dst, long long planes, int H, int W, int Hp, int Wp,
-                              int elem_bytes, cudaStream_t st);
-cudaError_t launch_crop_planes(const void *src, void *dst, long long planes, int H, int W, int Hp, int Wp,
-                               int elem_bytes, cudaStream_t st);
-
 size_t dw_tile_smem_bytes(const ShallowGeo &sg, int elem_bytes);
 cudaError_t launch_dw_tile(const DwTileArgs &a, int dtype, size_t smem, cudaStream_t st);
 int occupancy_dw_tile(int dtype, int K, size_t smem);

@@ -10,7 +10,9 @@
 // One warp per destination row, its lanes striding over the columns: one division per row, and
 // neighbouring lanes touch neighbouring elements.  Elements are copied as raw bits (2 or 4 bytes);
 // the padding is all-zero bits, +0.0 in every supported type.
-#include "wtconv_internal.h"
+#include <stdint.h>
+
+#include "wtconv_pad.h"
 
 namespace wtconv {
 
