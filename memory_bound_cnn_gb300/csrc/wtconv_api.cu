@@ -603,7 +603,7 @@ PPlan plan_plane_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
         for (int ci = 3; ci < 1 + 2 * L; ++ci) {
             const int l = (ci - 1) / 2 + 1;
             a.deep_item_start[ci] = tot;
-            tot += a.dg.rseg[l] * a.dg.cstr[l];
+            tot += ceil_div(a.dg.h[l], kPlaneDeepRows) * a.dg.cstr[l];
         }
         a.deep_item_start[1 + 2 * L] = tot;
         a.n_deep_items = tot;

@@ -254,6 +254,7 @@ struct DwTileArgs {
 // Fused whole-plane forward / input-gradient kernel: one plane per CTA iteration, its whole
 // pyramid on chip, the fused output items of the shallow kernel.
 constexpr int kPlaneThreads = 128;
+constexpr int kPlaneDeepRows = 4;  // rows per conv item of a level >= 2 image in the fused kernel
 struct PlaneArgs {
     int B, C, H, W, L, K;
     int nb, planes_per_cta;        // grid = nb * C; CTA n takes batch entries n*ppc .. n*ppc + ppc - 1
@@ -265,7 +266,7 @@ struct PlaneArgs {
     ShallowGeo sg;                 // the whole plane as one tile (TH >= H, TW >= W, G = 1)
     Geo dg;                        // levels >= 2 slot (L >= 2)
     int dpitch;                    // row pitch (floats) of D, the deep contribution at level-1 resolution
-    int n_deep_items;              // conv items of the levels >= 2 images
+    int n_deep_items;              // conv items (kPlaneDeepRows x kColsL) of the levels >= 2 images
     int deep_item_start[1 + 2 * kMaxLevels + 1];  // first item of conv image ci (ci = 3 .. 2L), then the end
     int *timeout;
     CUtensorMap tmap_x;            // box xw x xrows x 1 x 1 at (-padx, -2P, c, b)

@@ -6,7 +6,8 @@
 //   2. Haar level 1 of the plane (+ P coefficients of halo) is computed as two subband-pair
 //      images (LL|LH, HL|HH); levels >= 2 are built from the level-1 low band on chip, each
 //      level's subbands as pair images with a zero halo;
-//   3. the levels >= 2 run their subband-pair conv items (folded kernels, packed f32x2 FMAs);
+//   3. the levels >= 2 run their subband-pair conv items (folded kernels, packed f32x2 FMAs,
+//      kPlaneDeepRows rows per item);
 //   4. their closed-form synthesis is gathered at level-1 resolution into D (shared memory);
 //   5. every thread owns 8 x 4 pixel output blocks and computes, in registers, the level-1 convs
 //      of its 4 x 2 coefficients, their synthesis onto its pixels, D and the bias, and the base
@@ -44,6 +45,43 @@ __host__ __device__ inline PlaneLayout plane_layout(const PlaneArgs &a, int elem
     o = p.wts + (size_t)(1 + 2 * a.L) * wpairs(a.K) * sizeof(f2_t);
     p.total_bytes = o + 128;  // room to align the base
     return p;
+}
+
+// Conv item of kPlaneDeepRows x kColsL positions on a subband-pair image of a level >= 2:
+// out[r][c] = sum_{u,v} w[u][v] * in[r + u][c + v] elementwise on the two subbands; `in` points at
+// the padded window origin, `out` at the compact pair output; pitches in positions.  Shorter than
+// the 8-row items of level 1 so that more threads share the small deep images.
+template <int K>
+__device__ __forceinline__ void deep_item(const float *__restrict__ in, int pitch, const f2_t (&w)[K * K],
+                                          float *__restrict__ out, int opitch) {
+    constexpr int R = kPlaneDeepRows, NV = (kColsL + K - 1 + 1) / 2;
+    f2_t acc[R][kColsL];
+#pragma unroll
+    for (int i = 0; i < R + K - 1; ++i) {
+        f2_t x[2 * NV];
+        load_pair_row<NV>(in + 2 * i * pitch, x);
+#pragma unroll
+        for (int v = 0; v < K; ++v) {
+#pragma unroll
+            for (int u = 0; u < K; ++u) {
+                const int j = i - u;
+                if (j >= 0 && j < R) {
+#pragma unroll
+                    for (int q = 0; q < kColsL; ++q) {
+                        if (u == 0 && v == 0) acc[j][q] = fmul2(w[0], x[q]);
+                        else ffma2_acc(acc[j][q], w[u * K + v], x[q + v]);
+                    }
+                }
+            }
+        }
+        const int jd = i - (K - 1);
+        if (jd >= 0) {
+            ulonglong2 t;
+            t.x = acc[jd][0];
+            t.y = acc[jd][1];
+            *reinterpret_cast<ulonglong2 *>(out + 2 * jd * opitch) = t;
+        }
+    }
 }
 
 }  // namespace
@@ -168,27 +206,53 @@ __global__ void __launch_bounds__(kPlaneThreads, (K <= 5 ? 4 : 2)) wtconv_plane_
         }
         __syncthreads();
         if (L >= 2) {
-            // level 2 from the level-1 low band (pair image 0, even floats; interior position
-            // (i, j) of level 1 sits at (i + P, j + P))
-            const int h2 = dg.h[2], w2 = dg.w[2];
-            for (int bi = l2_row0, bj = l2_col0; bi < h2; ) {
-                const float *l1 = pairs + 2 * ((2 * bi + P) * sg.ypitch + 2 * bj + P);
-                const Quad q = butterfly(l1[0], l1[2], l1[2 * sg.ypitch], l1[2 * sg.ypitch + 2]);
-                put_quad_pairs(dslot, dg, dg.off_y, 2, bi, bj, q);
-                bj += l2_dcol;
-                bi += l2_drow;
-                if (bj >= w2) { bj -= w2; ++bi; }
+            // levels >= 2 from the level-1 low band (pair image 0, even floats; interior position
+            // (i, j) of level 1 sits at (i + P, j + P)).  L = 2: one pass over the level-2
+            // positions; L >= 3: two levels per pass, a thread reading a 4 x 4 block of the finer
+            // low band and writing four quads of level l and one of level l + 1
+            if (L == 2) {
+                const int h2 = dg.h[2], w2 = dg.w[2];
+                for (int bi = l2_row0, bj = l2_col0; bi < h2; ) {
+                    const float *l1 = pairs + 2 * ((2 * bi + P) * sg.ypitch + 2 * bj + P);
+                    const Quad q = butterfly(l1[0], l1[2], l1[2 * sg.ypitch], l1[2 * sg.ypitch + 2]);
+                    put_quad_pairs(dslot, dg, dg.off_y, 2, bi, bj, q);
+                    bj += l2_dcol;
+                    bi += l2_drow;
+                    if (bj >= w2) { bj -= w2; ++bi; }
+                }
+                __syncthreads();
             }
-            __syncthreads();
-            for (int l = 3; l <= L; ++l) {
-                const int hl = dg.h[l], wl = dg.w[l];
-                for (int i = tid; i < hl * wl; i += nt) {
-                    const int bi = i / wl, bj = i - bi * wl;
-                    const Quad q = butterfly(get_ll(dslot, dg, dg.off_y, l - 1, 2 * bi, 2 * bj),
-                                             get_ll(dslot, dg, dg.off_y, l - 1, 2 * bi, 2 * bj + 1),
-                                             get_ll(dslot, dg, dg.off_y, l - 1, 2 * bi + 1, 2 * bj),
-                                             get_ll(dslot, dg, dg.off_y, l - 1, 2 * bi + 1, 2 * bj + 1));
-                    put_quad_pairs(dslot, dg, dg.off_y, l, bi, bj, q);
+            for (int l = 2; L >= 3 && l <= L; l += 2) {
+                const bool two = l + 1 <= L;
+                const int ho = two ? dg.h[l + 1] : dg.h[l], wo = two ? dg.w[l + 1] : dg.w[l];
+                for (int i = tid; i < ho * wo; i += nt) {
+                    const int bi = i / wo, bj = i - bi * wo;
+                    auto ll = [&](int r, int cc) {  // level l-1 low band at interior (r, cc)
+                        return l == 2 ? pairs[2 * ((r + P) * sg.ypitch + cc + P)]
+                                      : get_ll(dslot, dg, dg.off_y, l - 1, r, cc);
+                    };
+                    if (two) {
+                        float v[4][4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+#pragma unroll
+                            for (int cc = 0; cc < 4; ++cc) v[r][cc] = ll(4 * bi + r, 4 * bj + cc);
+                        Quad q[2][2];
+#pragma unroll
+                        for (int a2 = 0; a2 < 2; ++a2)
+#pragma unroll
+                            for (int b2 = 0; b2 < 2; ++b2) {
+                                q[a2][b2] = butterfly(v[2 * a2][2 * b2], v[2 * a2][2 * b2 + 1], v[2 * a2 + 1][2 * b2],
+                                                      v[2 * a2 + 1][2 * b2 + 1]);
+                                put_quad_pairs(dslot, dg, dg.off_y, l, 2 * bi + a2, 2 * bj + b2, q[a2][b2]);
+                            }
+                        put_quad_pairs(dslot, dg, dg.off_y, l + 1, bi, bj,
+                                       butterfly(q[0][0].ll, q[0][1].ll, q[1][0].ll, q[1][1].ll));
+                    } else {
+                        put_quad_pairs(dslot, dg, dg.off_y, l, bi, bj,
+                                       butterfly(ll(2 * bi, 2 * bj), ll(2 * bi, 2 * bj + 1), ll(2 * bi + 1, 2 * bj),
+                                                 ll(2 * bi + 1, 2 * bj + 1)));
+                    }
                 }
                 __syncthreads();
             }
@@ -201,10 +265,10 @@ __global__ void __launch_bounds__(kPlaneThreads, (K <= 5 ? 4 : 2)) wtconv_plane_
                 const int rs = e / dg.cstr[l], cs = e - rs * dg.cstr[l];
                 f2_t w[KK];
                 load_weights<K>(wts + ci * WP, w);
-                conv_item_pair<K>(dslot + dg.off_y[l] + pp * dg.pimg[l] + 2 * ((rs * kRows) * dg.pitch[l] + cs * kColsL),
-                                  dg.pitch[l], w,
-                                  dslot + dg.off_z[l] + pp * dg.zimg[l] + 2 * ((rs * kRows) * dg.zpitch[l] + cs * kColsL),
-                                  dg.zpitch[l]);
+                const int r0 = rs * kPlaneDeepRows;
+                deep_item<K>(dslot + dg.off_y[l] + pp * dg.pimg[l] + 2 * (r0 * dg.pitch[l] + cs * kColsL), dg.pitch[l], w,
+                             dslot + dg.off_z[l] + pp * dg.zimg[l] + 2 * (r0 * dg.zpitch[l] + cs * kColsL),
+                             dg.zpitch[l]);
             }
             __syncthreads();
             // their synthesis at level-1 resolution -> D
