@@ -603,7 +603,7 @@ PPlan plan_plane_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
         for (int ci = 3; ci < 1 + 2 * L; ++ci) {
             const int l = (ci - 1) / 2 + 1;
             a.deep_item_start[ci] = tot;
-            tot += ceil_div(a.dg.h[l], kPlaneDeepRows) * a.dg.cstr[l];
+            tot += ceil_div(a.dg.h[l], kPlaneDeepRows) * round_up(a.dg.cstr[l], 8);  // 8-slot item rows
         }
         a.deep_item_start[1 + 2 * L] = tot;
         a.n_deep_items = tot;
@@ -682,24 +682,30 @@ FPlan plan_dw_fused_uncached(int B, int C, int H, int W, int L, int k, int dtype
     a.y1rows = a.th1 + 2 * (k / 2);
     a.dg = make_geo(H, W, L, k, 3);
     // thread split: CTA size, base warps and items per thread minimising the item rounds per plane
-    // (ties: fewer threads)
-    const int nbase = sg.items_r * sg.items_c;
+    // (ties: fewer threads).  Items are counted by slot, item rows padded to multiples of 8 slots,
+    // and every image's threads start at a multiple of 8 (the kernel's quarter-warp layout).
+    const int nbase = sg.items_r * round_up(sg.items_c, 8);
+    auto level_slots = [&](int l) { return a.dg.rseg[l] * round_up(a.dg.cstr[l], 8); };
     int best_nt = 0, best_wb = -1, best_pb = 0, best_pl = 0, best_span = 0;
     for (int nt = 256; nt <= kDwPlaneMaxThreads; nt += 32) {
         for (int wb = 1; 32 * wb < nt; ++wb) {
             const int pb = ceil_div(nbase, 32 * wb), avail = nt - 32 * wb;
-            int pl = 1;
-            for (;; ++pl) {
+            int max_slots = 1;
+            for (int l = 1; l <= L; ++l) max_slots = std::max(max_slots, level_slots(l));
+            int pl = 0;  // fewest items per level thread whose threads fit (0: none do)
+            for (int t = 1; t <= max_slots && pl == 0; ++t) {
                 int need = 0;
-                for (int l = 1; l <= L; ++l) need += 2 * ceil_div(a.dg.rseg[l] * a.dg.cstr[l], pl);
-                if (need <= avail) break;
+                for (int l = 1; l <= L; ++l) need += 2 * round_up(ceil_div(level_slots(l), t), 8);
+                if (need <= avail) pl = t;
             }
+            if (pl == 0) continue;
             const int span = std::max(pb, pl);
             if (best_wb < 0 || span < best_span) {
                 best_nt = nt; best_wb = wb; best_pb = pb; best_pl = pl; best_span = span;
             }
         }
     }
+    if (best_wb < 0) { p.status = WTCONV_ERR_UNSUPPORTED; return p; }
     a.nthreads = best_nt;
     a.per_thread_base = best_pb;
     a.per_thread = best_pl;
@@ -707,7 +713,7 @@ FPlan plan_dw_fused_uncached(int B, int C, int H, int W, int L, int k, int dtype
     a.tstart[1] = 32 * best_wb;
     for (int ci = 1; ci < 1 + 2 * L; ++ci) {
         const int l = (ci - 1) / 2 + 1;
-        a.tstart[ci + 1] = a.tstart[ci] + ceil_div(a.dg.rseg[l] * a.dg.cstr[l], best_pl);
+        a.tstart[ci + 1] = a.tstart[ci] + round_up(ceil_div(level_slots(l), best_pl), 8);
     }
     // two copy buffers where that keeps as many CTAs resident per SM as one
     a.nbuf = 1;

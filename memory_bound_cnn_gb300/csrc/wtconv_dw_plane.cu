@@ -118,22 +118,25 @@ __global__ void __launch_bounds__(kDwPlaneMaxThreads, (K <= 5 ? 2 : 1))
     int ci = -1;
     for (int k = 0; k < nimg; ++k)
         if (tid >= a.tstart[k] && tid < a.tstart[k + 1]) ci = k;
-    int n_img = 0, icols = 1, pitch = yp, pt = a.per_thread;
+    // items by slot: every item row has a multiple of 8 slots (those past the row's items idle),
+    // so that the 8 threads of each quarter warp read neighbouring 16-byte columns of one item row
+    // and never share banks across a row boundary
+    int n_img = 0, icols = 8, ncols = 0, pitch = yp, pt = a.per_thread;
     const float *ybase = nullptr, *gbase = nullptr;
     if (ci == 0) {
-        n_img = sg.items_r * sg.items_c;
-        icols = sg.items_c;
+        ncols = sg.items_c;
+        icols = (ncols + 7) & ~7;
+        n_img = sg.items_r * icols;
         pt = a.per_thread_base;
     } else if (ci > 0) {
         const int lvl = (ci - 1) / 2 + 1, pp = (ci - 1) & 1;
+        ncols = dg.cstr[lvl];
+        icols = (ncols + 7) & ~7;
+        n_img = dg.rseg[lvl] * icols;
         if (lvl == 1) {
-            icols = dg.cstr[1];
-            n_img = dg.rseg[1] * icols;
             ybase = Y1 + pp * l1img;
             gbase = G1 + pp * l1img + 2 * (P * yp + P);
         } else {
-            icols = dg.cstr[lvl];
-            n_img = dg.rseg[lvl] * icols;
             pitch = dg.pitch[lvl];
             ybase = dslot + dg.off_y[lvl] + pp * dg.pimg[lvl];
             gbase = dslot + dg.off_g[lvl] + pp * dg.pimg[lvl] + 2 * (P * pitch + P);
@@ -309,6 +312,7 @@ __global__ void __launch_bounds__(kDwPlaneMaxThreads, (K <= 5 ? 2 : 1))
         if (ci == 0) {
             for (int it = it_first; it < it_end; it += it_step) {
                 const int rs = it / icols, cs = it - rs * icols;
+                if (cs >= ncols) continue;
                 const float *xw = X + (kRows * rs + P) * sg.xw + kCols * cs + sg.padx - 4;
                 const float *dw = DY + (kRows * rs) * TW + kCols * cs;
                 f2_t gr[kRows][2];
@@ -343,6 +347,7 @@ __global__ void __launch_bounds__(kDwPlaneMaxThreads, (K <= 5 ? 2 : 1))
         } else {
             for (int it = it_first; it < it_end; it += it_step) {
                 const int rs = it / icols, cs = it - rs * icols;
+                if (cs >= ncols) continue;
                 const int off = 2 * ((rs * kRows) * pitch + cs * kColsL);
                 dw_item_pair<K>(ybase + off, gbase + off, pitch, acc);
             }

@@ -149,7 +149,11 @@ __global__ void __launch_bounds__(kPlaneThreads, (K <= 5 ? 4 : 2)) wtconv_plane_
     const size_t HW = (size_t)H * W;
     const float bias = a.with_bias ? a.base_scale[c] * a.base_bias[c] : 0.f;
     const bool vec_st = a.st_mode >= 1;
-    const int n_fused = sg.items_r * sg.items_c;
+    // output items by slot: every item row has a multiple of 8 slots (those past the row's items
+    // idle), so that the 8 threads of each quarter warp read neighbouring 16-byte columns of one
+    // item row and never share banks across a row boundary
+    const int fused_cpad = (sg.items_c + 7) & ~7;
+    const int n_fused = sg.items_r * fused_cpad;
     // per-thread coordinates of the analysis loops (computed once: no division per element)
     const int a_rstep = sg.ycols >= nt ? 1 : nt / sg.ycols;
     const int a_threads = sg.ycols >= nt ? nt : a_rstep * sg.ycols;
@@ -262,7 +266,9 @@ __global__ void __launch_bounds__(kPlaneThreads, (K <= 5 ? 4 : 2)) wtconv_plane_
                 while (it >= a.deep_item_start[ci + 1]) ++ci;
                 const int l = (ci - 1) / 2 + 1, pp = (ci - 1) & 1;
                 const int e = it - a.deep_item_start[ci];
-                const int rs = e / dg.cstr[l], cs = e - rs * dg.cstr[l];
+                const int cpad = (dg.cstr[l] + 7) & ~7;  // slots per item row, as for the output items
+                const int rs = e / cpad, cs = e - rs * cpad;
+                if (cs >= dg.cstr[l]) continue;
                 f2_t w[KK];
                 load_weights<K>(wts + ci * WP, w);
                 const int r0 = rs * kPlaneDeepRows;
@@ -286,7 +292,8 @@ __global__ void __launch_bounds__(kPlaneThreads, (K <= 5 ? 4 : 2)) wtconv_plane_
         __syncthreads();
         // fused output items
         for (int it = tid; it < n_fused; it += nt) {
-            const int irs = it / sg.items_c, ics = it - irs * sg.items_c;
+            const int irs = it / fused_cpad, ics = it - irs * fused_cpad;
+            if (ics >= sg.items_c) continue;
             const int pr = kRows * irs, pc = kCols * ics;
             f2_t init[kRows][2];
             const float *dt = D + (4 * irs) * a.dpitch + 2 * ics;
