@@ -251,6 +251,16 @@ def run_gpu(args, world, rank, local):
             step(events[k])
         torch.cuda.synchronize(dev)
         barrier(world)
+    # warm: the same steps back to back without the L2 flush (small workloads stay in the 129 MB L2)
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    w0.record(stream)
+    for k in range(args.steps):
+        step()
+    w1.record(stream)
+    torch.cuda.synchronize(dev)
+    warm_ms = max_over_ranks(w0.elapsed_time(w1) / args.steps, world)
     fwd_ms = [sum(events[k][i][0].elapsed_time(events[k][i][1]) for k in range(args.steps)) / args.steps for i in range(nl)]
     bwd_ms = [sum(events[k][i][1].elapsed_time(events[k][i][2]) for k in range(args.steps)) / args.steps for i in range(nl)]
     step_ms_local = sum(fwd_ms) + sum(bwd_ms)
@@ -373,6 +383,8 @@ def run_gpu(args, world, rank, local):
                    "l2": "flushed before every timed step (256 MiB write, outside the event bracket)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "fwd_ms": round(fwd_tot, 5), "bwd_ms": round(bwd_tot, 5),
+        "warm": {"value": round(whole_job_throughput(elements, world, warm_ms / 1e3), 3), "unit": UNIT,
+                 "ms_per_step": round(warm_ms, 5), "note": "same steps back to back, L2 not flushed"},
         "roofline": roofline,
         "e2e": {"value": round(whole_job_throughput(elements, world, e2e_ms / 1e3), 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
