@@ -441,9 +441,14 @@ def cpu_baseline(workload: str, budget_s: float) -> dict:
         elements += e
         secs += t
         passes += 1
+    # and on one host thread, on a smaller sample (about a quarter of the budget)
+    b1 = oracle_sample_size(layers, budget_s / 4, 1)
+    e1, t1 = oracle_run(layers, b1, 1)
     return {"value": round(elements / secs / 1e9, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"first {b} batch entries of every layer of {workload}, fwd+bwd, fp64, "
-                      f"{threads} threads, {passes} passes, {secs:.2f} s"}
+                      f"{threads} threads, {passes} passes, {secs:.2f} s",
+            "single_thread": {"value": round(e1 / t1 / 1e9, 6), "unit": UNIT, "cores": 1,
+                              "sample": f"first {b1} batch entries of every layer, fwd+bwd, fp64, {t1:.2f} s"}}
 
 
 def run_reference(args, world, rank):
