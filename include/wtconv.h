@@ -43,15 +43,16 @@
  *     synchronise.  Arguments are validated on the host before anything is launched: on any
  *     error no kernel runs and no output is touched.  Faults in a launched kernel surface at
  *     the caller's next synchronisation, as with any CUDA launch.
- *   - The library keeps no state between calls; concurrent calls on different streams with
- *     distinct workspaces are safe.
+ *   - No state carries results from one call to the next (the library caches per-shape launch
+ *     plans on the host, per device); concurrent calls on different streams with distinct
+ *     workspaces are safe.
  *   - The forward and the input gradient run one of three kernel sets: the fused whole-plane
  *     kernel (fp32 planes where it is fastest), the whole-plane kernel (planes whose pyramid fits
  *     in shared memory), or two tiled kernels (larger planes).  WTCONV_FWD_PATH=fused, =plane or
  *     =tiles selects a set where it applies (same results within fp32 rounding).
  *   - The weight gradients run the fused whole-plane kernel (x and dy planes moved by bulk
- *     tensor copies, both pyramids on chip; planes of at least 64 base items where both copies
- *     fit one box of at most 256 x 256), else a staged whole-plane kernel where both planes'
+ *     tensor copies, both pyramids on chip; fp32 planes of at least 64 base items where both
+ *     copies fit one box of at most 256 x 256), else a staged whole-plane kernel where both planes'
  *     pyramids fit in shared memory, else tiled kernels (tiles with bulk tensor copies, levels
  *     >= 2 on their pyramids in the workspace), else workspace pyramids for every level.
  *     WTCONV_DW_PATH=fused, =plane, =tiles or =pyramid selects a path where it applies (same
