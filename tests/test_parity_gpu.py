@@ -102,6 +102,8 @@ SWEEP = [
     (2, 2, 30, 45, 2, 5, "f32"),
     (2, 3, 57, 55, 3, 5, "f32"),
     (1, 2, 3, 3, 2, 5, "f32"),
+    (1, 1, 1, 1, 1, 3, "f32"),       # a single pixel: every level pads
+    (2, 2, 1, 37, 3, 5, "bf16"),     # one row, odd width
 ]
 
 
