@@ -110,6 +110,13 @@ const char *wtconv_strerror(int status);
  * it), WTCONV_ERR_CUDA if the synchronisation or the read failed, else WTCONV_OK. */
 int wtconv_device_status(void);
 
+/* Diagnostic of the failure path above, with no fault: launches one kernel on `stream` whose
+ * single waiting thread waits on a shared-memory barrier that nothing ever completes.  The wait
+ * gives up after its bounded number of tries (about half a second) and raises the flag, so the
+ * next wtconv_device_status() returns WTCONV_ERR_DEVICE_TIMEOUT (and clears it).  Returns
+ * WTCONV_OK once launched, WTCONV_ERR_CUDA if the launch failed. */
+int wtconv_selftest_wait_timeout(wtconv_stream_t stream);
+
 /* Bytes of device workspace `op` needs for this shape on the current device (0 if none).
  * FORWARD and BACKWARD_INPUT need, for L >= 2, one fp32 per level-1 position
  * (B*C*(H/2)*(W/2)*4 bytes, rounded up to 256): the contribution of the Haar levels >= 2, which a

@@ -16,6 +16,7 @@
 #include "wtconv.h"
 #include "wtconv_internal.h"
 #include "wtconv_pad.h"
+#include "wtconv_selftest.h"
 
 using namespace wtconv;
 
@@ -972,6 +973,12 @@ size_t wtconv_workspace_size(int op, int B, int C, int H, int W, int L, int k, i
     size_t bytes = 0;
     if (workspace_inner(op, B, C, pd.Hp, pd.Wp, L, k, dtype, &bytes) != WTCONV_OK) return 0;
     return bytes + (pd.on ? pad_buffers(op) * pd.act_bytes : 0);
+}
+
+int wtconv_selftest_wait_timeout(wtconv_stream_t stream) {
+    int *flag = timeout_flag();
+    if (flag == nullptr) return WTCONV_ERR_CUDA;
+    return cuda_status(launch_wait_selftest(flag, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int wtconv_device_status(void) {

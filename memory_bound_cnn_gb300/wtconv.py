@@ -8,7 +8,7 @@ call raises.
 Functions carry the C names: ``wtconv_forward``, ``wtconv_backward_input``,
 ``wtconv_backward_weights``, ``wtconv_backward``, ``wtconv_backward_weights_noalloc``,
 ``wtconv_workspace_size``, ``wtconv_launch_count``, ``wtconv_plan_kernels``, ``wtconv_device_status``,
-``wtconv_strerror``, ``wtconv_version``.  ``WTConvFunction`` wraps forward and the fused
+``wtconv_selftest_wait_timeout``, ``wtconv_strerror``, ``wtconv_version``.  ``WTConvFunction`` wraps forward and the fused
 backward as a ``torch.autograd.Function``.
 """
 from __future__ import annotations
@@ -31,7 +31,7 @@ DTYPE_CODE = {v: k for k, v in TORCH_DTYPE.items()}
 EXPORTED = ("wtconv_version", "wtconv_strerror", "wtconv_workspace_size", "wtconv_forward",
             "wtconv_backward_input", "wtconv_backward_weights", "wtconv_backward",
             "wtconv_backward_weights_noalloc", "wtconv_launch_count", "wtconv_device_status",
-            "wtconv_plan_kernels")
+            "wtconv_plan_kernels", "wtconv_selftest_wait_timeout")
 
 _lib = None
 
@@ -70,6 +70,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.wtconv_plan_kernels.argtypes = [i] * 8
     lib.wtconv_device_status.restype = i
     lib.wtconv_device_status.argtypes = []
+    lib.wtconv_selftest_wait_timeout.restype = i
+    lib.wtconv_selftest_wait_timeout.argtypes = [ctypes.c_void_p]
     lib.wtconv_launch_count.restype = i
     lib.wtconv_launch_count.argtypes = [i] * 8
     shape = [i] * 7
@@ -109,6 +111,12 @@ def wtconv_plan_kernels(op: int, B: int, C: int, H: int, W: int, L: int, k: int,
 def wtconv_device_status() -> int:
     """Synchronise the device; WTCONV_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up."""
     return load().wtconv_device_status()
+
+
+def wtconv_selftest_wait_timeout(stream=None) -> None:
+    """Launch the diagnostic whose one bounded wait is never completed: the next
+    wtconv_device_status() then returns ERR_DEVICE_TIMEOUT."""
+    _raise(load().wtconv_selftest_wait_timeout(_stream(stream)), "wtconv_selftest_wait_timeout")
 
 
 def wtconv_launch_count(op: int, B: int, C: int, H: int, W: int, L: int, k: int, dtype: int) -> int:

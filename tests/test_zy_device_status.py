@@ -28,3 +28,18 @@ def test_no_bounded_wait_gave_up():
             os.environ["WTCONV_FWD_PATH"] = old
     torch.cuda.synchronize()
     assert W.wtconv_device_status() == W.OK
+
+
+@pytest.mark.gpu
+def test_a_wait_that_gives_up_is_reported_once():
+    """The failure path without a fault: a kernel whose bounded wait is never completed raises
+    the flag; the host reads it as ERR_DEVICE_TIMEOUT once, and the context stays usable."""
+    assert W.wtconv_device_status() == W.OK
+    W.wtconv_selftest_wait_timeout()
+    assert W.wtconv_device_status() == W.ERR_DEVICE_TIMEOUT
+    assert W.wtconv_device_status() == W.OK
+    shape = I.LayerShape(B=1, C=2, H=16, W=16, L=2, k=3, dtype="f32")
+    d = to_device(I.make_inputs(shape, seed=22))
+    y = W.wtconv_forward(d["x"], *[d[p] for p in PARAMS])
+    torch.cuda.synchronize()
+    assert torch.isfinite(y).all()
