@@ -160,11 +160,28 @@ def _workspace(op: int, shape, device, workspace: torch.Tensor | None):
     return workspace, nbytes
 
 
-def _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, device):
+def _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, act):
+    """Checks every parameter against the activation's channel count (the library reads them
+    through bare pointers, so a short tensor would be read past its end) and returns pointers."""
+    device, C = act.device, act.shape[1]
     for t, n in ((base_w, "base_w"), (base_bias, "base_bias"), (base_scale, "base_scale"),
                  (wavelet_w, "wavelet_w"), (wavelet_scale, "wavelet_scale")):
         _check_param(t, n, device)
+    k = base_w.shape[-1] if base_w.dim() == 3 else -1
+    L = wavelet_w.shape[0] if wavelet_w.dim() == 4 else -1
+    want = {"base_w": (C, k, k), "base_bias": (C,), "base_scale": (C,), "wavelet_w": (L, 4 * C, k, k),
+            "wavelet_scale": (L, 4 * C)}
+    for t, n in ((base_w, "base_w"), (base_bias, "base_bias"), (base_scale, "base_scale"),
+                 (wavelet_w, "wavelet_w"), (wavelet_scale, "wavelet_scale")):
+        if tuple(t.shape) != want[n]:
+            raise ValueError(f"{n} has shape {tuple(t.shape)}, expected {want[n]} for {C} channels")
     return [_ptr(base_w), _ptr(base_bias), _ptr(base_scale), _ptr(wavelet_w), _ptr(wavelet_scale)]
+
+
+def _check_out(t: torch.Tensor, name: str, like: torch.Tensor):
+    _check_act(t, name)
+    if t.shape != like.shape or t.dtype != like.dtype or t.device != like.device:
+        raise ValueError(f"{name} must match the input's shape, dtype and device")
 
 
 def _raise(status: int, where: str):
@@ -177,10 +194,10 @@ def wtconv_forward(x, base_w, base_bias, base_scale, wavelet_w, wavelet_scale, y
     """y = WTConv(x); x (B, C, H, W) fp32 / bf16 / fp16 on CUDA, parameters fp32."""
     _check_act(x, "x")
     shape = _shape(x, wavelet_w, base_w)
-    p = _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, x.device)
+    p = _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, x)
     if y is None:
         y = torch.empty_like(x)
-    _check_act(y, "y")
+    _check_out(y, "y", x)
     ws, nbytes = _workspace(OP_FORWARD, shape, x.device, workspace)
     rc = load().wtconv_forward(*shape, _ptr(x), *p, _ptr(y), _ptr(ws), nbytes, _stream(stream))
     _raise(rc, "wtconv_forward")
@@ -192,10 +209,10 @@ def wtconv_backward_input(dy, base_w, base_bias, base_scale, wavelet_w, wavelet_
     """dx = WTConv^T(dy) (the input gradient)."""
     _check_act(dy, "dy")
     shape = _shape(dy, wavelet_w, base_w)
-    p = _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, dy.device)
+    p = _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, dy)
     if dx is None:
         dx = torch.empty_like(dy)
-    _check_act(dx, "dx")
+    _check_out(dx, "dx", dy)
     ws, nbytes = _workspace(OP_BACKWARD_INPUT, shape, dy.device, workspace)
     rc = load().wtconv_backward_input(*shape, *p, _ptr(dy), _ptr(dx), _ptr(ws), nbytes, _stream(stream))
     _raise(rc, "wtconv_backward_input")
@@ -210,8 +227,10 @@ def _grad_buffers(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, grads
             "d_wavelet_scale": torch.empty_like(wavelet_scale),
         }
     order = ("d_base_w", "d_base_bias", "d_base_scale", "d_wavelet_w", "d_wavelet_scale")
-    for n in order:
+    for n, like in zip(order, (base_w, base_bias, base_scale, wavelet_w, wavelet_scale)):
         _check_param(grads[n], n, base_w.device)
+        if grads[n].shape != like.shape:
+            raise ValueError(f"{n} has shape {tuple(grads[n].shape)}, expected {tuple(like.shape)}")
     return grads, [_ptr(grads[n]) for n in order]
 
 
@@ -220,8 +239,9 @@ def wtconv_backward_weights(x, dy, base_w, base_bias, base_scale, wavelet_w, wav
     """Every parameter gradient (dict d_base_w, d_base_bias, d_base_scale, d_wavelet_w, d_wavelet_scale)."""
     _check_act(x, "x")
     _check_act(dy, "dy")
+    _check_out(dy, "dy", x)
     shape = _shape(x, wavelet_w, base_w)
-    p = _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, x.device)
+    p = _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, x)
     grads, gp = _grad_buffers(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, grads)
     ws, nbytes = _workspace(OP_BACKWARD_WEIGHTS, shape, x.device, workspace)
     rc = load().wtconv_backward_weights(*shape, _ptr(x), _ptr(dy), *p, *gp, _ptr(ws), nbytes, _stream(stream))
@@ -239,8 +259,9 @@ def wtconv_backward_weights_noalloc(x, dy, base_w, base_bias, base_scale, wavele
         raise ValueError("wtconv_backward_weights_noalloc needs preallocated gradient buffers")
     _check_act(x, "x")
     _check_act(dy, "dy")
+    _check_out(dy, "dy", x)
     shape = _shape(x, wavelet_w, base_w)
-    p = _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, x.device)
+    p = _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, x)
     grads, gp = _grad_buffers(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, grads)
     rc = load().wtconv_backward_weights_noalloc(*shape, _ptr(x), _ptr(dy), *p, *gp, _stream(stream))
     _raise(rc, "wtconv_backward_weights_noalloc")
@@ -253,10 +274,11 @@ def wtconv_backward(x, dy, base_w, base_bias, base_scale, wavelet_w, wavelet_sca
     _check_act(x, "x")
     _check_act(dy, "dy")
     shape = _shape(x, wavelet_w, base_w)
-    p = _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, x.device)
+    p = _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, x)
     if dx is None:
         dx = torch.empty_like(x)
-    _check_act(dx, "dx")
+    _check_out(dx, "dx", x)
+    _check_out(dy, "dy", x)
     grads, gp = _grad_buffers(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, grads)
     ws, nbytes = _workspace(OP_BACKWARD, shape, x.device, workspace)
     rc = load().wtconv_backward(*shape, _ptr(x), _ptr(dy), *p, _ptr(dx), *gp, _ptr(ws), nbytes,

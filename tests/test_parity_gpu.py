@@ -190,10 +190,14 @@ def test_invalid_call_raises_and_writes_nothing(monkeypatch):
     shape = LayerShape(2, 3, 16, 16, 2, 5, "f32")
     d = to_device(make_inputs(shape, seed=1))
     y = torch.full_like(d["x"], 3.0)
-    bad_w = d["base_w"][:, :4, :4].contiguous()      # an even kernel size
+    # an even kernel size: consistent shapes, rejected by the library's validation
+    even = dict(d, base_w=d["base_w"][:, :4, :4].contiguous(), wavelet_w=d["wavelet_w"][:, :, :4, :4].contiguous())
     with pytest.raises(W.WTConvError) as e:
-        W.wtconv_forward(d["x"], bad_w, *[d[p] for p in PARAMS[1:]], y=y)
+        W.wtconv_forward(d["x"], *[even[p] for p in PARAMS], y=y)
     assert e.value.status == W.ERR_INVALID_ARG
+    # a parameter shorter than the channel count: rejected by the binding before any call
+    with pytest.raises(ValueError):
+        W.wtconv_forward(d["x"], *[d[p] for p in PARAMS[:4]], d["wavelet_scale"][:, :4].contiguous(), y=y)
     y2 = torch.full_like(d["x"], 3.0)
     monkeypatch.setenv("WTCONV_INJECT_FAULT", "1")
     with pytest.raises(W.WTConvError) as e:
