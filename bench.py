@@ -636,7 +636,7 @@ def run_dwconv(args, world, rank, local, k=7):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("cuda", "reference", "torch-cascade", "dwconv7"), default="cuda")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stage1_f32")
