@@ -383,6 +383,10 @@ def run_gpu(args, world, rank, local):
                    "l2": "flushed before every timed step (256 MiB write, outside the event bracket)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "fwd_ms": round(fwd_tot, 5), "bwd_ms": round(bwd_tot, 5),
+        # every layer on its own (this rank's event times): fwd + bwd throughput of the layer
+        "per_layer": [{"layer": i, "fwd_ms": round(fwd_ms[i], 5), "bwd_ms": round(bwd_ms[i], 5),
+                       "value": round(layers[i][0].numel / ((fwd_ms[i] + bwd_ms[i]) / 1e3) / 1e9, 3)}
+                      for i in range(nl)],
         "warm": {"value": round(whole_job_throughput(elements, world, warm_ms / 1e3), 3), "unit": UNIT,
                  "ms_per_step": round(warm_ms, 5), "note": "same steps back to back, L2 not flushed"},
         "roofline": roofline,
