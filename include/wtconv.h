@@ -46,17 +46,20 @@
  *   - No state carries results from one call to the next (the library caches per-shape launch
  *     plans on the host, per device); concurrent calls on different streams with distinct
  *     workspaces are safe.
- *   - The forward and the input gradient run one of three kernel sets: the fused whole-plane
- *     kernel (fp32 planes where it is fastest), the whole-plane kernel (planes whose pyramid fits
- *     in shared memory), or two tiled kernels (larger planes).  WTCONV_FWD_PATH=fused, =plane or
- *     =tiles selects a set where it applies (same results within fp32 rounding).
- *   - The weight gradients run the fused whole-plane kernel (x and dy planes moved by bulk
- *     tensor copies, both pyramids on chip; fp32 planes of at least 64 base items where both
- *     copies fit one box of at most 256 x 256), else a staged whole-plane kernel where both planes'
- *     pyramids fit in shared memory, else tiled kernels (tiles with bulk tensor copies, levels
- *     >= 2 on their pyramids in the workspace), else workspace pyramids for every level.
- *     WTCONV_DW_PATH=fused, =plane, =tiles or =pyramid selects a path where it applies (same
- *     results within fp32 rounding).
+ *   - The forward and the input gradient run one of four kernel sets: the batch-pair kernel
+ *     (two batch entries per packed fp32 pair, whole pyramids of several pairs on chip; small
+ *     planes), the fused whole-plane kernel (fp32 planes where it is fastest), the whole-plane
+ *     kernel (planes whose pyramid fits in shared memory), or two tiled kernels (larger planes).
+ *     WTCONV_FWD_PATH=pair, =fused, =plane or =tiles selects a set where it applies (same results
+ *     within fp32 rounding); WTCONV_PAIR=0 / =1 keeps the batch-pair kernels off / makes them the
+ *     default wherever they apply.
+ *   - The weight gradients run the batch-pair kernel on small planes, else the fused
+ *     whole-plane kernel (x and dy planes moved by bulk tensor copies, both pyramids on chip; fp32
+ *     planes of at least 64 base items where both copies fit one box of at most 256 x 256), else a
+ *     staged whole-plane kernel where both planes' pyramids fit in shared memory, else tiled
+ *     kernels (tiles with bulk tensor copies, levels >= 2 on their pyramids in the workspace),
+ *     else workspace pyramids for every level.  WTCONV_DW_PATH=pair, =fused, =plane, =tiles or
+ *     =pyramid selects a path where it applies (same results within fp32 rounding).
  *   - Setting the environment variable WTCONV_INJECT_FAULT=1 makes every compute entry point
  *     return WTCONV_ERR_INJECTED before launching anything (host-side fault injection).
  */

@@ -16,6 +16,7 @@
 #include "wtconv.h"
 #include "wtconv_internal.h"
 #include "wtconv_pad.h"
+#include "wtconv_pair.cuh"
 #include "wtconv_selftest.h"
 
 using namespace wtconv;
@@ -775,16 +776,283 @@ FPlan plan_dw_fused(int B, int C, int H, int W, int L, int k, int dtype) {
     return p;
 }
 
+// ------------------------------------------------------------------ batch-pair kernels
+// Item shapes the pair kernels can take (base columns x rows, level columns x rows) and their
+// relative per-FMA speed measured on GB300 (isolated strip items: two-column strips have no
+// shared-memory bank conflicts; four-row strips re-read a larger share of halo rows).
+struct PairShape { int q0, s0, ql, sl, qd, sd; double eff; };
+const PairShape kPairShapes[] = {
+    {4, 8, 4, 8, 4, 8, 1.00}, {4, 8, 2, 8, 2, 8, 1.05}, {2, 8, 2, 8, 2, 8, 1.10}, {2, 8, 2, 8, 2, 4, 1.08},
+    {4, 4, 4, 4, 4, 4, 0.76}, {2, 4, 2, 4, 2, 4, 0.70},
+};
+
+struct PairPlan {
+    int status = WTCONV_ERR_UNSUPPORTED;
+    PairArgs a{};
+    size_t smem = 0;
+    int occ = 0;
+    double score = 0.0;
+    size_t workspace = 0;  // weight gradient: partials
+};
+
+void pair_counts(PairArgs &a) {
+    const PairGeo &g = a.geo;
+    const int L = a.L;
+    a.n_a = L >= 2 ? (a.H / 4) * (a.W / 4) : (a.H / 2) * (a.W / 2);
+    a.dv_na = make_fastdiv((uint32_t)a.n_a);
+    a.dv_naw = make_fastdiv((uint32_t)(L >= 2 ? a.W / 4 : a.W / 2));
+    int tot = 0;
+    for (int l = 1; l <= L; ++l) {
+        a.conv_start[l] = tot;
+        tot += 4 * g.ns[l] * g.ng[l];
+    }
+    a.conv_start[L + 1] = tot;
+    a.n_conv = tot;
+    a.dv_nconv = make_fastdiv((uint32_t)tot);
+    for (int l = 0; l <= L; ++l) {
+        a.dv_lvl[l] = make_fastdiv((uint32_t)(g.ns[l] * g.ng[l]));
+        a.dv_lvl_ns[l] = make_fastdiv((uint32_t)g.ns[l]);
+    }
+    a.n_gather = L >= 2 ? g.h[2] * g.w[2] : 0;
+    a.dv_ngather = make_fastdiv((uint32_t)(a.n_gather > 0 ? a.n_gather : 1));
+    a.dv_gw = make_fastdiv((uint32_t)(L >= 2 ? g.w[2] : 1));
+    a.n_out = g.ns[0] * g.ng[0];
+    a.dv_nout = make_fastdiv((uint32_t)a.n_out);
+    a.dv_out_ns = make_fastdiv((uint32_t)g.ns[0]);
+    a.dv_xn = make_fastdiv((uint32_t)(a.H * (a.W / 2)));
+    a.dv_xw = make_fastdiv((uint32_t)(a.W / 2));
+}
+
+// Persistent grid: one CTA per resident slot (at most one per unit), contiguous unit ranges.
+void pair_grid(PairArgs &a, int sms, int occ, int chunk_groups) {
+    a.chunk_groups = chunk_groups;
+    a.nchunks = (a.ngroups + chunk_groups - 1) / chunk_groups;
+    a.nb = a.nchunks;
+    a.units = a.C * a.nchunks;
+    a.grid = std::min(a.units, sms * occ);
+}
+
+// Thread-slot utilisation of a phase of n items (cost c each, thread-time c / eff) on T threads.
+void add_phase(double &work, double &tim, long long n, double c, double eff, int T) {
+    if (n <= 0) return;
+    work += n * c;
+    tim += (double)((n + T - 1) / T) * T * c / eff;
+}
+
+// Forward / input gradient on batch pairs: every pair's pyramid and outputs in shared memory.
+PairPlan plan_pair_fwd_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
+    PairPlan best;
+    const int eb = elem_bytes(dtype);
+    const int sms = device_sms();
+    if (sms <= 0) { best.status = WTCONV_ERR_CUDA; return best; }
+    const int npairs = (B + 1) / 2;
+    const int KK = k * k;
+    for (const PairShape &sh : kPairShapes) {
+        for (int T : {128, 256}) {
+            for (int G = 1; G <= std::min(npairs, kPairMaxSlots); ++G) {
+                PairArgs a{};
+                a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
+                a.npairs = npairs;
+                a.G = G;
+                a.ngroups = (npairs + G - 1) / G;
+                a.nthreads = T;
+                a.geo = make_pair_geo(H, W, L, k, 0, sh.q0, sh.s0, sh.ql, sh.sl, sh.qd, sh.sd);
+                a.tma = ((size_t)H * W * eb) % 16 == 0;
+                a.raw_pair_bytes = (int)(((size_t)2 * H * W * eb + 15) / 16 * 16);
+                a.vec_st = (W % 4) == 0;
+                pair_counts(a);
+                const size_t smem = pair_fwd_smem_bytes(a, eb);
+                if (smem + kStaticSmemMargin > (size_t)kMaxSmem) break;
+                const int occ = occupancy_pair_fwd(dtype, k, smem, T);
+                if (occ <= 0) break;
+                const PairGeo &g = a.geo;
+                double work = 0.0, tim = 0.0;
+                add_phase(work, tim, (long long)G * a.n_out, (double)g.Q[0] * g.S[0] * KK, sh.eff, T);
+                double cmax = 0.0;
+                for (int l = 1; l <= L; ++l) cmax = std::max(cmax, (double)g.Q[l] * g.S[l] * KK);
+                double wconv = 0.0;
+                for (int l = 1; l <= L; ++l) wconv += 4.0 * G * g.ns[l] * g.ng[l] * g.Q[l] * g.S[l] * KK;
+                const long long nconv = (long long)G * a.n_conv;
+                work += wconv;
+                tim += (double)((nconv + T - 1) / T) * T * cmax / sh.eff;
+                // resident warps (beyond 16 per SM more warps no longer help); a single resident
+                // CTA also loses its phases' barrier waits, which other CTAs would fill
+                const double warps = std::min((double)occ * T / 32.0, 16.0) * (occ >= 2 ? 1.0 : 0.8);
+                const double score = work / tim * warps;
+                if (score > best.score * 1.02) {
+                    best.status = WTCONV_OK;
+                    best.a = a;
+                    best.smem = smem;
+                    best.occ = occ;
+                    best.score = score;
+                }
+            }
+        }
+    }
+    if (best.status == WTCONV_OK) pair_grid(best.a, sms, best.occ, 1);
+    return best;
+}
+
+// Weight gradient on batch pairs: both pyramids in shared memory; threads pinned to signals.
+PairPlan plan_pair_dw_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
+    PairPlan best;
+    const int eb = elem_bytes(dtype);
+    const int sms = device_sms();
+    if (sms <= 0) { best.status = WTCONV_ERR_CUDA; return best; }
+    const int npairs = (B + 1) / 2;
+    const int KK = k * k, nsig = 1 + 4 * L;
+    for (const PairShape &sh : kPairShapes) {
+        for (int T : {128, 256}) {
+            for (int G = 1; G <= std::min(npairs, kPairMaxSlots); ++G) {
+                PairArgs a{};
+                a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
+                a.npairs = npairs;
+                a.G = G;
+                a.ngroups = (npairs + G - 1) / G;
+                a.nthreads = T;
+                a.geo = make_pair_geo(H, W, L, k, 1, sh.q0, sh.s0, sh.ql, sh.sl, sh.qd, sh.sd);
+                a.tma = ((size_t)H * W * eb) % 16 == 0;
+                a.raw_pair_bytes = (int)(((size_t)4 * H * W * eb + 15) / 16 * 16);
+                pair_counts(a);
+                const size_t smem = pair_dw_smem_bytes(a, eb);
+                if (smem + kStaticSmemMargin > (size_t)kMaxSmem) break;
+                const int occ = occupancy_pair_dw(dtype, k, smem, T);
+                if (occ <= 0) break;
+                // items per signal per group, and the smallest per-thread count that fits T threads
+                const PairGeo &g = a.geo;
+                long long n[1 + 4 * kMaxLevels];
+                double cost[1 + 4 * kMaxLevels];
+                for (int s = 0; s < nsig; ++s) {
+                    const int l = s == 0 ? 0 : (s - 1) / 4 + 1;
+                    n[s] = (long long)G * g.ns[l] * g.ng[l];
+                    cost[s] = (double)g.Q[l] * g.S[l] * KK;
+                }
+                int d = 1;
+                for (;; ++d) {
+                    long long need = 0;
+                    for (int s = 0; s < nsig; ++s) need += (n[s] + d - 1) / d;
+                    if (need <= T) break;
+                }
+                // a warp takes as long as its slowest thread; a warp mixing item shapes runs each
+                // shape's code in turn
+                double work = 0.0, tmax = 0.0;
+                {
+                    constexpr int kW = kPairMaxThreads / 32;
+                    double tshape[kW][3] = {};  // slowest thread per item shape (S x Q: 3 kinds at most)
+                    int t0 = 0;
+                    for (int s = 0; s < nsig; ++s) {
+                        work += n[s] * cost[s];
+                        const int l = s == 0 ? 0 : (s - 1) / 4 + 1;
+                        const int kind = l == 0 ? 0 : (l == 1 ? 1 : 2);
+                        const int nth = (int)((n[s] + d - 1) / d);
+                        const double tt = std::min<double>(d, (double)n[s]) * cost[s];
+                        for (int t = t0; t < t0 + nth; ++t) tshape[t / 32][kind] = std::max(tshape[t / 32][kind], tt);
+                        t0 += nth;
+                    }
+                    for (int wi = 0; wi < T / 32; ++wi) {
+                        // kinds with the same item shape share their code
+                        double tw = tshape[wi][0];
+                        tw = (g.Q[1] == g.Q[0] && g.S[1] == g.S[0]) ? std::max(tw, tshape[wi][1]) : tw + tshape[wi][1];
+                        if (L >= 2) {
+                            const bool same1 = g.Q[2] == g.Q[1] && g.S[2] == g.S[1];
+                            tw = same1 ? std::max(tw, tshape[wi][2]) : tw + tshape[wi][2];
+                        }
+                        tmax = std::max(tmax, tw);
+                    }
+                }
+                const double warps = std::min((double)occ * T / 32.0, 16.0) * (occ >= 2 ? 1.0 : 0.8);
+                const double score = work / ((double)T * tmax / sh.eff) * warps;
+                if (score > best.score * 1.02) {
+                    int t0 = 0;
+                    for (int s = 0; s < nsig; ++s) {
+                        a.sig_start[s] = t0;
+                        t0 += (int)((n[s] + d - 1) / d);
+                    }
+                    a.sig_start[nsig] = t0;
+                    a.per_thread = d;
+                    best.status = WTCONV_OK;
+                    best.a = a;
+                    best.smem = smem;
+                    best.occ = occ;
+                    best.score = score;
+                }
+            }
+        }
+    }
+    if (best.status == WTCONV_OK) {
+        // units of several groups (one partial each): few enough partials to keep the flush and
+        // the finalize small, enough units to keep every resident CTA busy
+        PairArgs &a = best.a;
+        const long long slots = (long long)sms * best.occ;
+        int cg = 1;
+        while (cg < a.ngroups && (long long)C * ((a.ngroups + 2 * cg - 1) / (2 * cg)) >= 2 * slots) cg *= 2;
+        pair_grid(a, sms, best.occ, cg);
+        best.workspace = ((size_t)a.nchunks * C * nsig * (KK + 1) * sizeof(float) + 255) / 256 * 256;
+    }
+    return best;
+}
+
+PairPlan cached_pair_plan(int kind, int B, int C, int H, int W, int L, int k, int dtype) {
+    static std::mutex mu;
+    static std::map<PlanKey, PairPlan> cache;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        PairPlan p;
+        p.status = WTCONV_ERR_CUDA;
+        return p;
+    }
+    const PlanKey key(kind, B, C, H, W, L, k, dtype, dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    PairPlan p = kind == 10 ? plan_pair_fwd_uncached(B, C, H, W, L, k, dtype)
+                            : plan_pair_dw_uncached(B, C, H, W, L, k, dtype);
+    const char *verbose = getenv("WTCONV_VERBOSE");
+    if (verbose && verbose[0] == '1')
+        fprintf(stderr, "wtconv plan pair-%s B=%d C=%d H=%d W=%d L=%d k=%d dtype=%d: status %d G=%d items %dx%d/%dx%d "
+                        "threads=%d grid=%d units=%d chunk=%d smem=%zu occ=%d tma=%d d=%d score=%.2f\n",
+                kind == 10 ? "fwd" : "dw", B, C, H, W, L, k, dtype, p.status, p.a.G, p.a.geo.Q[0], p.a.geo.S[0],
+                p.a.geo.Q[1], p.a.geo.S[1], p.a.nthreads, p.a.grid, p.a.units, p.a.chunk_groups, p.smem, p.occ,
+                p.a.tma, p.a.per_thread, p.score);
+    if (p.status == WTCONV_OK || p.status == WTCONV_ERR_UNSUPPORTED) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache.emplace(key, p);
+    }
+    return p;
+}
+
+PairPlan plan_pair_fwd(int B, int C, int H, int W, int L, int k, int dtype) {
+    return cached_pair_plan(10, B, C, H, W, L, k, dtype);
+}
+PairPlan plan_pair_dw(int B, int C, int H, int W, int L, int k, int dtype) {
+    return cached_pair_plan(11, B, C, H, W, L, k, dtype);
+}
+
+// Whether the batch-pair kernels run by default.  Measured on GB300 (bf16, k = 5, B = 128): they
+// win on small planes, where the whole-plane kernels' per-plane setup does not amortise (8 x 8
+// planes: forward 56 vs 79 us, weight gradient 138 vs 208 us; 16 x 16: weight gradient 201 vs 208
+// us, forward 93 vs 85 us), and lose on larger ones (32 x 32 forward 203 vs 154 us).
+// WTCONV_PAIR=0 turns them off, =1 makes them the default wherever they apply.
+bool pair_default(bool weight_gradient, int H, int W) {
+    const char *v = getenv("WTCONV_PAIR");
+    if (v && strcmp(v, "0") == 0) return false;
+    if (v && strcmp(v, "1") == 0) return true;
+    return (long long)H * W <= (weight_gradient ? 256 : 64);
+}
+
 // Forward / input-gradient path of a shape (WTCONV_FWD_PATH=fused / tiles / plane selects a path
 // where it applies).  By default the fused whole-plane kernel runs where it measured fastest on
 // GB300: fp32 planes with at least 64 output items and three or more resident CTAs per SM; else
 // the whole-plane kernel where the pyramid fits; else the tiled kernels.
-enum FwdPath { FWD_FUSED, FWD_PLANE, FWD_TILES };
+enum FwdPath { FWD_FUSED, FWD_PLANE, FWD_TILES, FWD_PAIR };
 struct FwdChoice {
     int status = WTCONV_OK;
     FwdPath path = FWD_PLANE;
     PPlan pp;
     Plan pf;
+    PairPlan pr;
 };
 
 FwdChoice choose_fwd(int B, int C, int H, int W, int L, int k, int dtype) {
@@ -793,6 +1061,15 @@ FwdChoice choose_fwd(int B, int C, int H, int W, int L, int k, int dtype) {
     const bool want_fused = env && strcmp(env, "fused") == 0;
     const bool want_tiles = env && strcmp(env, "tiles") == 0;
     const bool want_plane = env && strcmp(env, "plane") == 0;
+    const bool want_pair = env && strcmp(env, "pair") == 0;
+    if (!want_tiles && !want_plane && !want_fused) {
+        f.pr = plan_pair_fwd(B, C, H, W, L, k, dtype);
+        if (f.pr.status != WTCONV_OK && f.pr.status != WTCONV_ERR_UNSUPPORTED) { f.status = f.pr.status; return f; }
+        if (f.pr.status == WTCONV_OK && (want_pair || pair_default(false, H, W))) {
+            f.path = FWD_PAIR;
+            return f;
+        }
+    }
     if (!want_tiles && !want_plane) {
         f.pp = plan_plane(B, C, H, W, L, k, dtype);
         if (f.pp.status != WTCONV_OK && f.pp.status != WTCONV_ERR_UNSUPPORTED) { f.status = f.pp.status; return f; }
@@ -817,13 +1094,14 @@ FwdChoice choose_fwd(int B, int C, int H, int W, int L, int k, int dtype) {
 // measured fastest, else the whole-plane kernel where a plane fits, else the tiled kernels where
 // they apply, else the workspace pyramids.  WTCONV_DW_PATH=fused, =tiles, =plane or =pyramid
 // selects a path where it applies (for testing and comparison).
-enum DwPath { DW_TILE, DW_PLANE, DW_PYRAMID, DW_FUSED };
+enum DwPath { DW_TILE, DW_PLANE, DW_PYRAMID, DW_FUSED, DW_PAIR };
 struct DwChoice {
     int status = WTCONV_OK;
     DwPath path = DW_PLANE;
     TPlan t;
     Plan p;
     FPlan f;
+    PairPlan pr;
     size_t workspace = 0;
 };
 
@@ -841,6 +1119,16 @@ DwChoice choose_dw(int B, int C, int H, int W, int L, int k, int dtype) {
     const bool want_pyramid = env && strcmp(env, "pyramid") == 0;
     const bool want_fused = env && strcmp(env, "fused") == 0;
     const bool want_plane = env && strcmp(env, "plane") == 0;
+    const bool want_pair = env && strcmp(env, "pair") == 0;
+    if (!want_tiles && !want_pyramid && !want_plane && !want_fused) {
+        d.pr = plan_pair_dw(B, C, H, W, L, k, dtype);
+        if (d.pr.status != WTCONV_OK && d.pr.status != WTCONV_ERR_UNSUPPORTED) { d.status = d.pr.status; return d; }
+        if (d.pr.status == WTCONV_OK && (want_pair || pair_default(true, H, W))) {
+            d.path = DW_PAIR;
+            d.workspace = d.pr.workspace;
+            return d;
+        }
+    }
     if (!want_tiles && !want_pyramid && !want_plane) {
         d.f = plan_dw_fused(B, C, H, W, L, k, dtype);
         if (d.f.status != WTCONV_OK && d.f.status != WTCONV_ERR_UNSUPPORTED) { d.status = d.f.status; return d; }
@@ -1000,7 +1288,8 @@ static const char *plan_kernels_inner(int op, int B, int C, int H, int W, int L,
     if (fwd || both) {
         const FwdChoice fc = choose_fwd(B, C, H, W, L, k, dtype);
         if (fc.status != WTCONV_OK) return "";
-        f = fc.path == FWD_FUSED ? "wtconv_plane_kernel"
+        f = fc.path == FWD_PAIR ? "wtconv_pair_fwd_kernel"
+            : fc.path == FWD_FUSED ? "wtconv_plane_kernel"
             : fc.path == FWD_PLANE ? "wtconv_fwd_kernel"
             : (L >= 2 ? "wtconv_deep_kernel+wtconv_shallow_kernel" : "wtconv_shallow_kernel");
         if (fwd) return f;
@@ -1008,7 +1297,8 @@ static const char *plan_kernels_inner(int op, int B, int C, int H, int W, int L,
     const DwChoice d = choose_dw(B, C, H, W, L, k, dtype);
     if (d.status != WTCONV_OK) return "";
     if (dw) {
-        return d.path == DW_FUSED ? "wtconv_dw_plane_kernel+wtconv_dw_finalize_kernel"
+        return d.path == DW_PAIR ? "wtconv_pair_dw_kernel+wtconv_dw_finalize_kernel"
+             : d.path == DW_FUSED ? "wtconv_dw_plane_kernel+wtconv_dw_finalize_kernel"
              : d.path == DW_PLANE ? "wtconv_dw_kernel+wtconv_dw_finalize_kernel"
              : d.path == DW_TILE ? "wtconv_dw_tile_kernel+wtconv_level2_kernel+wtconv_haar_level_kernel+"
                                    "wtconv_dw_corr_kernel+wtconv_dw_finalize_kernel"
@@ -1018,7 +1308,8 @@ static const char *plan_kernels_inner(int op, int B, int C, int H, int W, int L,
     // combination; static storage)
     static std::mutex mu;
     static std::map<std::string, std::string> names;
-    const std::string dws = d.path == DW_FUSED ? "wtconv_dw_plane_kernel+wtconv_dw_finalize_kernel"
+    const std::string dws = d.path == DW_PAIR ? "wtconv_pair_dw_kernel+wtconv_dw_finalize_kernel"
+                            : d.path == DW_FUSED ? "wtconv_dw_plane_kernel+wtconv_dw_finalize_kernel"
                             : d.path == DW_PLANE ? "wtconv_dw_kernel+wtconv_dw_finalize_kernel"
                             : d.path == DW_TILE ? "wtconv_dw_tile_kernel+wtconv_level2_kernel+wtconv_haar_level_kernel+"
                                                   "wtconv_dw_corr_kernel+wtconv_dw_finalize_kernel"
@@ -1081,6 +1372,18 @@ static int run_operator(int B, int C, int H, int W, int L, int k, int dtype, con
                         cudaStream_t s) {
     const FwdChoice fc = choose_fwd(B, C, H, W, L, k, dtype);
     if (fc.status != WTCONV_OK) return fc.status;
+    if (fc.path == FWD_PAIR) {
+        PairArgs a = fc.pr.a;
+        a.x = src;
+        a.out = dst;
+        a.base_w = base_w; a.base_bias = base_bias; a.base_scale = base_scale;
+        a.wavelet_w = wavelet_w; a.wavelet_scale = wavelet_scale;
+        a.flip = flip ? 1 : 0;
+        a.with_bias = flip ? 0 : 1;
+        a.timeout = timeout_flag();
+        if (a.timeout == nullptr) return WTCONV_ERR_CUDA;
+        return cuda_status(launch_pair_fwd(a, dtype, fc.pr.smem, s));
+    }
     if (fc.path == FWD_FUSED) {
         PPlan pp = fc.pp;
         PlaneArgs &a = pp.a;
@@ -1218,6 +1521,22 @@ static int run_dw_fused(FPlan &fp, int dtype, const void *x, const void *dy, flo
     return WTCONV_OK;
 }
 
+// Batch-pair weight-gradient kernel into `partials`; fills what the finalize reads.
+static int run_dw_pair(const PairPlan &pp, int dtype, const void *x, const void *dy, float *partials, LayerArgs &fin,
+                       cudaStream_t s) {
+    PairArgs a = pp.a;
+    a.x = x;
+    a.dy = dy;
+    a.partials = partials;
+    a.timeout = timeout_flag();
+    if (a.timeout == nullptr) return WTCONV_ERR_CUDA;
+    if (launch_pair_dw(a, dtype, pp.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+    fin.B = a.B; fin.C = a.C; fin.H = a.H; fin.W = a.W; fin.L = a.L; fin.K = a.K;
+    fin.nb = a.nb;
+    fin.partials = partials;
+    return WTCONV_OK;
+}
+
 static int backward_common(bool want_dx, int B, int C, int H, int W, int L, int k, int dtype, const void *x,
                            const void *dy, const float *base_w, const float *base_bias, const float *base_scale,
                            const float *wavelet_w, const float *wavelet_scale, void *dx, float *d_base_w,
@@ -1275,6 +1594,9 @@ static int backward_common(bool want_dx, int B, int C, int H, int W, int L, int 
         fin.partials = t.partials;
     } else if (dc.path == DW_FUSED) {
         st = run_dw_fused(dc.f, dtype, x, dy, reinterpret_cast<float *>(wsp), fin, s);
+        if (st != WTCONV_OK) return st;
+    } else if (dc.path == DW_PAIR) {
+        st = run_dw_pair(dc.pr, dtype, x, dy, reinterpret_cast<float *>(wsp), fin, s);
         if (st != WTCONV_OK) return st;
     } else if (dc.path == DW_PYRAMID) {
         Plan &pw = dc.p;
@@ -1370,7 +1692,7 @@ int wtconv_backward_weights_noalloc(int B, int C, int H, int W, int L, int k, in
     // the same kernels as wtconv_backward_weights where they need nothing but the partials
     DwChoice dc = choose_dw(B, C, H, W, L, k, dtype);
     if (dc.status != WTCONV_OK) return dc.status;
-    if ((dc.path != DW_FUSED && dc.path != DW_PLANE) || dc.workspace > sizeof(g_noalloc_scratch))
+    if ((dc.path != DW_FUSED && dc.path != DW_PLANE && dc.path != DW_PAIR) || dc.workspace > sizeof(g_noalloc_scratch))
         return WTCONV_ERR_SCRATCH_LIMIT;
     void *scratch = noalloc_scratch();
     if (scratch == nullptr) return WTCONV_ERR_CUDA;
@@ -1378,6 +1700,9 @@ int wtconv_backward_weights_noalloc(int B, int C, int H, int W, int L, int k, in
     LayerArgs fin{};
     if (dc.path == DW_FUSED) {
         st = run_dw_fused(dc.f, dtype, x, dy, static_cast<float *>(scratch), fin, s);
+        if (st != WTCONV_OK) return st;
+    } else if (dc.path == DW_PAIR) {
+        st = run_dw_pair(dc.pr, dtype, x, dy, static_cast<float *>(scratch), fin, s);
         if (st != WTCONV_OK) return st;
     } else {
         Plan &pw = dc.p;

@@ -37,13 +37,13 @@ def fwd_path(path: str):
 
 def check_layer(shape: LayerShape, inputs: dict, split: bool = True):
     """Forward, fused backward and (if `split`) the separate backward entry points against the
-    oracle, on the default kernels and again with the tiled and the fused whole-plane forward /
-    input-gradient kernels selected (where they apply)."""
+    oracle, on the default kernels and again with each other forward / input-gradient kernel set
+    selected (batch-pair, whole-plane, tiled, fused whole-plane; where they apply)."""
     tol = TOL[shape.dtype]
     d = to_device(inputs)
     y_ref = oracle.forward(inputs["x"], inputs)
     g_ref = oracle.backward(inputs["x"], inputs["dy"], inputs)
-    for path in ("default", "tiles", "fused"):
+    for path in ("default", "pair", "plane", "tiles", "fused"):
         with fwd_path(path):
             y = gpu_forward(d)
             dx, g = gpu_backward(d)
@@ -59,9 +59,9 @@ def check_layer(shape: LayerShape, inputs: dict, split: bool = True):
         assert_close("dx (backward_input)", np64(dx2), g_ref["dx"], tol)
         for n in GRADS:
             assert_close(n + " (backward_weights)", np64(g2[n]), g_ref[n], tol)
-    # the weight gradient's other paths (where they apply): the fused whole-plane kernel, the
-    # staged whole-plane kernel, tiled kernels and workspace pyramids
-    for dpath in ("fused", "plane", "tiles", "pyramid"):
+    # the weight gradient's other paths (where they apply): the batch-pair kernel, the fused
+    # whole-plane kernel, the staged whole-plane kernel, tiled kernels and workspace pyramids
+    for dpath in ("pair", "fused", "plane", "tiles", "pyramid"):
         if dpath == "pyramid" and shape.numel > 20_000_000:
             continue  # the pyramid path already runs by default where planes are too large
         with env_path("WTCONV_DW_PATH", dpath):
@@ -140,7 +140,7 @@ def test_input_gradient_is_forward_with_rotated_kernels():
     assert_close("dx vs rotated forward", np64(dx), np64(y), 1e-6)
 
 
-@pytest.mark.parametrize("path", ["default", "tiles", "fused"])
+@pytest.mark.parametrize("path", ["default", "pair", "plane", "tiles", "fused"])
 def test_outputs_stay_in_bounds_and_inputs_untouched(path):
     """Canary words around every output; inputs byte-identical after the calls."""
     shape = LayerShape(3, 5, 24, 16, 3, 5, "bf16")
