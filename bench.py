@@ -1,25 +1,34 @@
 """Benchmark of the WTConv layer's training step (forward + fused backward) on GB300.
 
 One step = wtconv_forward + wtconv_backward (dx and every parameter gradient) over one batch of
-the seeded synthetic workload, through the C ABI.  Default workload: the ConvNeXt-T stage-1
-shape B=64, C=96, H=W=56, L=3, k=5, fp32 activations (the paper's WTConvNeXt-T setting).
+the seeded synthetic workload, through the C ABI.  Default workload (the headline): four WTConv
+layers back to back, bf16 activations, B = 128, k = 5: (C = 96, 64 x 64, L = 4), (192, 32 x 32,
+L = 3), (384, 16 x 16, L = 2), (768, 8 x 8, L = 1).  `per_config` in the same line repeats the
+device-timed measurement on every workload configuration (tiny, ConvNeXt-T stage 1 and 2 shapes,
+high resolution, four layers).
 
 Prints ONE JSON line (rank 0).  `value` is fwd+bwd throughput in Gpixel*ch/s = B*C*H*W / step
 time over all ranks (replicas: each rank runs its own copy of the workload, "scaling": "weak").
 Timing: W untimed warm-up steps, then K timed steps; L2 is flushed (256 MiB write) before each
 timed step and each step is bracketed by CUDA events on the launching stream (the flush is not
-inside the bracket).  Also reported: per-kernel roofline of the dominant kernel, an end-to-end
-number with host buffers (pinned host -> device copies of x and dy and device -> host copies of
-y, dx and the gradients inside the timed region), the CPU oracle baseline, and SM clocks sampled
-during the timed region.
+inside the bracket).  Also reported: the roofline of the dominant kernel (FP32 packed-FMA pipe:
+algorithmic FLOPs over its event-timed launches, against the peak derived from the device's SM
+count and clock, against the peak measured by the library's packed-FMA probe, and at the sampled
+median clock; HBM: ncu DRAM bytes per launch from the committed profiles over the same time,
+beside the algorithmic bytes), an end-to-end number with host buffers (pinned host -> device
+copies of x and dy and device -> host copies of y, dx and the gradients inside the timed region),
+the CPU oracle baseline, and SM clocks sampled during the timed region.
 
 `--impl reference` times the CPU oracle (the plain fp64 reference pipeline) instead, on the host
 cores, on a bounded sample of the same workload.  `--impl torch-cascade` times the same reference
 cascade written with PyTorch ops on the GPU (grouped convs, autograd): a comparison arm.
+`--impl dwconv7` times a plain depthwise 7x7 conv at the same shapes.  `--peak` prints only the
+packed-FMA probe's result.
 """
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -37,15 +46,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from memory_bound_cnn_gb300 import wtconv as W  # noqa: E402
-from memory_bound_cnn_gb300.inputs import WORKLOADS, LayerShape, make_inputs  # noqa: E402
+from memory_bound_cnn_gb300.inputs import WORKLOAD_ORDER, WORKLOADS, LayerShape, make_inputs  # noqa: E402
 
 PARAMS = ("base_w", "base_bias", "base_scale", "wavelet_w", "wavelet_scale")
 GRADS = ("d_base_w", "d_base_bias", "d_base_scale", "d_wavelet_w", "d_wavelet_scale")
 METRIC = "WTConv fwd+bwd Gpixel·ch/s and achieved HBM GB/s as % of GB300 peak"
 UNIT = "Gpixel·ch/s"
-# FP32 FMA peak from unit counts and the maximum clock: 152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz
-FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
-HBM_FALLBACK_GBS = 6800.0
+HBM_FALLBACK_GBS = 6800.0       # the profiling recipe's fallback (MEASURED_PEAKS.json absent)
+SM_MAX_MHZ_FALLBACK = 2070.0     # GB300's maximum SM clock
+HEADLINE = "four_layers_bf16"
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -67,41 +76,33 @@ def algorithmic(shape: LayerShape) -> dict:
     }
 
 
-# the source files of each reported kernel: a committed ncu traffic figure counts only while
-# these files are unchanged since the capture
-KERNEL_SOURCES = {
-    "wtconv_fwd_kernel": ["wtconv_fwd.cu", "wtconv_analysis.cuh", "wtconv_device.cuh", "wtconv_internal.h"],
-    "wtconv_plane_kernel": ["wtconv_plane.cu", "wtconv_items.cuh", "wtconv_analysis.cuh", "wtconv_device.cuh",
-                            "wtconv_internal.h"],
-    "wtconv_deep_kernel+wtconv_shallow_kernel": ["wtconv_deep.cu", "wtconv_shallow.cu", "wtconv_items.cuh",
-                                                 "wtconv_analysis.cuh", "wtconv_device.cuh", "wtconv_internal.h"],
-    "wtconv_dw_kernel": ["wtconv_bwd.cu", "wtconv_analysis.cuh", "wtconv_device.cuh", "wtconv_internal.h"],
-    "wtconv_dw_plane_kernel": ["wtconv_dw_plane.cu", "wtconv_items.cuh", "wtconv_analysis.cuh", "wtconv_device.cuh",
-                               "wtconv_internal.h"],
-}
-
-
-def source_hash(kernel: str) -> str:
+def source_hash() -> str:
+    """Hash of the library's sources: a committed ncu traffic figure counts only while it matches."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "memory_bound_cnn_gb300", "csrc")
-    for fn in sorted(KERNEL_SOURCES.get(kernel, os.listdir(csrc))):
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(fn.encode() + f.read())
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    with open(os.path.join(ROOT, "include", "wtconv.h"), "rb") as f:
+        h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str, workload: str):
-    """dram bytes per launch from the committed ncu summary, or None if it is missing or was taken
-    on kernel sources other than the current ones."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+def profiled_traffic(workload: str) -> dict:
+    """ncu DRAM bytes per launch, {(layer, op, kernel): bytes}, from the committed profile summary of
+    `workload` (profiles/traffic_<workload>.md); empty if it is missing or was taken on other sources."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.md")
     if not os.path.exists(path):
-        return None
+        return {}
     text = open(path).read()
-    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    s = re.search(r"source_sha:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != source_hash(kernel):
-        return None
-    return float(m.group(1))
+    m = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    if not m or m.group(1) != source_hash():
+        return {}
+    out = {}
+    for layer, op, kernel, b in re.findall(r"traffic: layer=(\d+) op=(\w+) kernel=(\S+) bytes=([0-9.eE+]+)", text):
+        out[(int(layer), op, kernel)] = float(b)
+    return out
 
 
 def measured_peaks() -> dict:
@@ -209,22 +210,20 @@ def dims(s: LayerShape):
                                                      "f16": torch.float16}[s.dtype]]
 
 
-def run_gpu(args, world, rank, local):
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    shapes = WORKLOADS[args.workload]
+def setup_layers(workload: str, dev):
+    """Device inputs, outputs and workspace of every layer of `workload` (seeded host inputs)."""
     layers = []
-    for i, s in enumerate(shapes):
+    for i, s in enumerate(WORKLOADS[workload]):
         host = make_inputs(s, seed=i)
         d = {k: v.to(dev) for k, v in host.items()}
-        ws = torch.empty(max(1, W.wtconv_workspace_size(W.OP_BACKWARD, s.B, s.C, s.H, s.W, s.L, s.k,
-                                                        W.DTYPE_CODE[d["x"].dtype])), dtype=torch.uint8, device=dev)
+        ws = torch.empty(max(1, W.wtconv_workspace_size(W.OP_BACKWARD, *dims(s))), dtype=torch.uint8, device=dev)
         out = {"y": torch.empty_like(d["x"]), "dx": torch.empty_like(d["x"]),
                "grads": {g: torch.empty_like(d[p]) for g, p in zip(GRADS, PARAMS)}}
         layers.append((s, host, d, ws, out))
-    stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    return layers
 
+
+def make_step(layers, stream):
     def step(ev=None):
         for i, (s, _, d, ws, out) in enumerate(layers):
             p = [d[n] for n in PARAMS]
@@ -236,22 +235,113 @@ def run_gpu(args, world, rank, local):
             W.wtconv_backward(d["x"], d["dy"], *p, dx=out["dx"], grads=out["grads"], workspace=ws, stream=stream)
             if ev is not None:
                 ev[i][2].record(stream)
+    return step
 
-    for _ in range(args.warmup):
+
+def time_layers(layers, steps, warmup, stream, flush, dev, world, clk=None):
+    """Per-layer fwd / bwd event times (ms, mean over the timed steps, max over ranks), L2 flushed
+    before every timed step (outside the event bracket)."""
+    step = make_step(layers, stream)
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize(dev)
-
     nl = len(layers)
-    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nl)] for _ in range(args.steps)]
-    with ClockSampler(local) as clk:
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nl)] for _ in range(steps)]
+    with (clk if clk is not None else contextlib.nullcontext()):
         barrier(world)
         torch.cuda.synchronize(dev)
-        for k in range(args.steps):
+        for k in range(steps):
             flush.zero_()
             step(events[k])
         torch.cuda.synchronize(dev)
         barrier(world)
+    fwd = [max_over_ranks(sum(events[k][i][0].elapsed_time(events[k][i][1]) for k in range(steps)) / steps, world)
+           for i in range(nl)]
+    bwd = [max_over_ranks(sum(events[k][i][1].elapsed_time(events[k][i][2]) for k in range(steps)) / steps, world)
+           for i in range(nl)]
+    return fwd, bwd
+
+
+def fp32_peaks(dev, clocks) -> dict:
+    """FP32 packed-FMA peaks: derived from the device's SM count and maximum clock (128 FP32 lanes
+    x 2 FLOP per SM per cycle), at the median SM clock sampled under load, and measured by the
+    library's packed-FMA probe."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peaks = measured_peaks()
+    max_mhz = float(peaks.get("sm_max_mhz") or (clocks or {}).get("sm_max_mhz") or SM_MAX_MHZ_FALLBACK)
+    med_mhz = float((clocks or {}).get("sm_mhz") or max_mhz)
+    derived = sms * 128 * 2 * max_mhz * 1e6 / 1e12
+    with torch.cuda.device(dev):
+        measured = W.wtconv_fp32_fma_peak(20000)
+    return {"derived": round(derived, 2), "at_median_clock": round(sms * 256 * med_mhz * 1e6 / 1e12, 2),
+            "measured": round(measured, 2), "sms": sms, "max_mhz": max_mhz, "median_mhz": med_mhz,
+            "note": f"derived: {sms} SMs x 128 FP32 lanes x 2 FLOP x {max_mhz:.0f} MHz; measured: packed-FMA "
+                    "chains on every SM (wtconv_fp32_fma_peak)"}
+
+
+def layer_roofline(workload, i, s, fwd_ms, fp32, traffic) -> dict:
+    """Roofline of layer i's forward operator kernel (it runs twice per step: y, and dx inside the
+    backward); its launches in wtconv_forward are timed alone by the fwd events."""
+    a = algorithmic(s)
+    kname = "+".join(W.wtconv_plan_kernels(W.OP_FORWARD, *dims(s)))
+    tflops = a["fwd_flop"] / (fwd_ms / 1e3) / 1e12
+    peaks = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", HBM_FALLBACK_GBS))
+    alg_gbs = a["fwd_bytes"] / (fwd_ms / 1e3) / 1e9
+    t = traffic.get((i, "fwd", kname))
+    ncu_gbs = None if t is None else t / (fwd_ms / 1e3) / 1e9
+    return {
+        "bound": "alu", "achieved": round(tflops, 3), "peak": fp32["derived"], "unit": "TFLOP/s",
+        "frac": round(tflops / fp32["derived"], 4), "traffic": t, "kernel": kname, "layer": i,
+        "launch_ms": round(fwd_ms, 5), "algorithmic_flop_per_launch": a["fwd_flop"],
+        "algorithmic_bytes_per_launch": a["fwd_bytes"],
+        "peak_measured": fp32["measured"], "frac_measured": round(tflops / fp32["measured"], 4),
+        "peak_at_median_clock": fp32["at_median_clock"],
+        "frac_at_median_clock": round(tflops / fp32["at_median_clock"], 4),
+        "hbm_achieved_gbs": None if ncu_gbs is None else round(ncu_gbs, 1),
+        "hbm_frac": None if ncu_gbs is None else round(ncu_gbs / hbm_peak, 4),
+        "hbm_achieved_gbs_algorithmic": round(alg_gbs, 1), "hbm_frac_algorithmic": round(alg_gbs / hbm_peak, 4),
+        "hbm_peak_gbs": hbm_peak,
+        "peak_note": "peak: FP32 packed-FMA peak derived from the SM count and maximum clock; hbm_frac: ncu DRAM "
+                     "bytes per launch (committed profile, same sources) over the event time, against the "
+                     "measured copy bandwidth; hbm_frac_algorithmic: one read of x and one write of y",
+    }
+
+
+def workload_summary(workload, layers, fwd, bwd, fp32, world) -> dict:
+    """Throughput and rooflines of one timed workload; the headline roofline is the layer whose
+    forward operator (two launches per step) takes the largest share of the step."""
+    traffic = profiled_traffic(workload)
+    elements = sum(s.numel for s, *_ in layers)
+    step_ms = sum(fwd) + sum(bwd)
+    per_layer = []
+    for i, (s, *_rest) in enumerate(layers):
+        per_layer.append({"layer": i, "fwd_ms": round(fwd[i], 5), "bwd_ms": round(bwd[i], 5),
+                          "value": round(s.numel / ((fwd[i] + bwd[i]) / 1e3) / 1e9, 3),
+                          "roofline": layer_roofline(workload, i, s, fwd[i], fp32, traffic)})
+    top = max(range(len(layers)), key=lambda i: fwd[i])
+    return {"workload": workload, "value": round(whole_job_throughput(elements, world, step_ms / 1e3), 3),
+            "ms_per_step": round(step_ms, 5), "fwd_ms": round(sum(fwd), 5), "bwd_ms": round(sum(bwd), 5),
+            "roofline": per_layer[top]["roofline"], "per_layer": per_layer}
+
+
+def run_gpu(args, world, rank, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    shapes = WORKLOADS[args.workload]
+    layers = setup_layers(args.workload, dev)
+    clk = ClockSampler(local)
+    fwd_ms, bwd_ms = time_layers(layers, args.steps, args.warmup, stream, flush, dev, world, clk)
+    clocks = clk.summary()
+    step_ms = sum(fwd_ms) + sum(bwd_ms)
+    elements = sum(s.numel for s, *_ in layers)
+    value = whole_job_throughput(elements, world, step_ms / 1e3)
+    nl = len(layers)
+
     # warm: the same steps back to back without the L2 flush (small workloads stay in the 129 MB L2)
+    step = make_step(layers, stream)
     w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -261,12 +351,6 @@ def run_gpu(args, world, rank, local):
     w1.record(stream)
     torch.cuda.synchronize(dev)
     warm_ms = max_over_ranks(w0.elapsed_time(w1) / args.steps, world)
-    fwd_ms = [sum(events[k][i][0].elapsed_time(events[k][i][1]) for k in range(args.steps)) / args.steps for i in range(nl)]
-    bwd_ms = [sum(events[k][i][1].elapsed_time(events[k][i][2]) for k in range(args.steps)) / args.steps for i in range(nl)]
-    step_ms_local = sum(fwd_ms) + sum(bwd_ms)
-    step_ms = max_over_ranks(step_ms_local, world)
-    elements = sum(s.numel for s, *_ in layers)
-    value = whole_job_throughput(elements, world, step_ms / 1e3)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region.
     # Every step copies its inputs in and its results out; the copies run on their own streams
@@ -346,35 +430,30 @@ def run_gpu(args, world, rank, local):
     for (s, _, d, ws, out), hp in zip(layers, pinned):
         if not torch.equal(hp["y"], out["y"].cpu()):
             raise RuntimeError("end-to-end results differ from the device-timed run")
+    step_mem = int(sum(out["y"].nbytes + out["dx"].nbytes + ws.nbytes + sum(g.nbytes for g in out["grads"].values())
+                       for _, _, _, ws, out in layers))
+    del sets, pinned, layers
+    torch.cuda.empty_cache()
 
-    # roofline of the dominant kernel: the forward operator's kernel, which runs twice per step
-    # (y in wtconv_forward, dx inside wtconv_backward) and takes the largest share of the step;
-    # its launches in wtconv_forward are timed alone by the fwd events above
-    acc = [algorithmic(s) for s, *_ in layers]
-    fwd_tot, bwd_tot = sum(fwd_ms), sum(bwd_ms)
-    fwd_kernels = {"+".join(W.wtconv_plan_kernels(W.OP_FORWARD, *dims(s))) for s in shapes}
-    kname = fwd_kernels.pop() if len(fwd_kernels) == 1 else "forward kernels (per layer: several)"
-    flop, byt = sum(a["fwd_flop"] for a in acc), sum(a["fwd_bytes"] for a in acc)
-    ms = fwd_tot
-    launches = len(layers)
-    achieved_tflops = flop / (ms / 1e3) / 1e12
-    peaks = measured_peaks()
-    hbm_peak = peaks.get("hbm_gbs", HBM_FALLBACK_GBS)
-    hbm_gbs = byt / (ms / 1e3) / 1e9
-    traffic = profiled_traffic(kname, args.workload)
-    roofline = {
-        "bound": "alu", "achieved": round(achieved_tflops, 3), "peak": round(FP32_PEAK_TFLOPS, 2),
-        "unit": "TFLOP/s", "frac": round(achieved_tflops / FP32_PEAK_TFLOPS, 4),
-        "traffic": None if traffic is None else traffic,
-        "kernel": kname, "launch_ms": round(ms / launches, 5),
-        "algorithmic_flop_per_launch": flop / launches, "algorithmic_bytes_per_launch": byt / launches,
-        "hbm_achieved_gbs": round(hbm_gbs, 1), "hbm_peak_gbs": hbm_peak,
-        "hbm_frac": round(hbm_gbs / hbm_peak, 4),
-        "peak_note": "FP32 FMA peak derived: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz; HBM peak of measured copy",
-    }
+    fp32 = fp32_peaks(dev, clocks)
+    head = workload_summary(args.workload, [(s, None, None, None, None) for s in shapes], fwd_ms, bwd_ms, fp32,
+                            world)
+    # every workload configuration, device-timed the same way (fewer steps for the others)
+    per_config = []
+    for name in WORKLOAD_ORDER:
+        if name == args.workload:
+            entry = dict(head)
+        else:
+            lay = setup_layers(name, dev)
+            f, b = time_layers(lay, max(3, min(args.steps, 100)), args.warmup, stream, flush, dev, world)
+            entry = workload_summary(name, lay, f, b, fp32, world)
+            del lay
+            torch.cuda.empty_cache()
+        entry["layers"] = [s.as_dict() for s in WORKLOADS[name]]
+        per_config.append(entry)
+
     per_step = sum(W.wtconv_launch_count(W.OP_FORWARD, *dims(s)) + W.wtconv_launch_count(W.OP_BACKWARD, *dims(s))
                    for s in shapes)
-
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
@@ -382,24 +461,23 @@ def run_gpu(args, world, rank, local):
         "config": {"workload": args.workload, "layers": [s.as_dict() for s in shapes],
                    "l2": "flushed before every timed step (256 MiB write, outside the event bracket)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "fwd_ms": round(fwd_tot, 5), "bwd_ms": round(bwd_tot, 5),
-        # every layer on its own (this rank's event times): fwd + bwd throughput of the layer
-        "per_layer": [{"layer": i, "fwd_ms": round(fwd_ms[i], 5), "bwd_ms": round(bwd_ms[i], 5),
-                       "value": round(layers[i][0].numel / ((fwd_ms[i] + bwd_ms[i]) / 1e3) / 1e9, 3)}
-                      for i in range(nl)],
+        "fwd_ms": round(sum(fwd_ms), 5), "bwd_ms": round(sum(bwd_ms), 5),
+        # every layer on its own (event times): fwd + bwd throughput and roofline of the layer
+        "per_layer": head["per_layer"],
         "warm": {"value": round(whole_job_throughput(elements, world, warm_ms / 1e3), 3), "unit": UNIT,
                  "ms_per_step": round(warm_ms, 5), "note": "same steps back to back, L2 not flushed"},
-        "roofline": roofline,
+        "roofline": head["roofline"],
+        "fp32_peak": fp32,
         "e2e": {"value": round(whole_job_throughput(elements, world, e2e_ms / 1e3), 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "note": "pinned host buffers; uploads, compute and downloads on three streams, overlapping "
                         "neighbouring steps (two device copies of every activation)"},
         "gpu_launches": per_step * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         # device memory a step needs beyond the inputs and parameters: y, dx, the gradients and
         # the workspace of every layer (the autograd arms report the same quantity)
-        "step_mem_bytes": int(sum(out["y"].nbytes + out["dx"].nbytes + ws.nbytes +
-                                  sum(g.nbytes for g in out["grads"].values()) for _, _, _, ws, out in layers)),
+        "step_mem_bytes": step_mem,
+        "per_config": per_config,
     }
     return line
 
@@ -643,8 +721,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("cuda", "reference", "torch-cascade", "dwconv7"), default="cuda")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stage1_f32")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--peak", action="store_true", help="print only the packed-FMA peak probe's result")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_env()
@@ -659,6 +738,10 @@ def main(argv=None):
             line = run_torch_cascade(args, world, rank, local)
         elif args.impl == "dwconv7":
             line = run_dwconv(args, world, rank, local, k=7)
+        elif args.peak:
+            W.load()
+            torch.cuda.set_device(local)
+            line = {"fp32_peak": fp32_peaks(torch.device("cuda", local), None)}
         else:
             W.load()
             line = run_gpu(args, world, rank, local)

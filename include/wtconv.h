@@ -105,20 +105,30 @@ int wtconv_version(void);
 /* Human-readable name of a status code (static storage; never NULL). */
 const char *wtconv_strerror(int status);
 
-/* Device-side status of the calls made so far on the current device.  Kernels that hand work
- * between their warps wait on shared-memory barriers for a bounded number of tries; a wait that
- * gives up (never expected: it would mean a broken handshake, not a slow GPU) raises a sticky
- * per-device flag and ends its warp, leaving that call's outputs incomplete.  This call
+/* Device-side status of the calls made so far on the current device.  Kernels that wait for
+ * their input copies (or hand work between warps) on shared-memory barriers wait at most half a
+ * second of elapsed time; a wait that gives up (never expected: it would mean a broken copy or
+ * handshake, not a slow GPU) raises a sticky per-device flag and ends its CTA.  The forward and
+ * input-gradient outputs of that CTA stay unwritten and the weight gradients it contributes to
+ * come out as NaN.  The compute calls themselves cannot report this (they return at launch):
+ * a caller that must know its results are valid polls this function after synchronising.  It
  * synchronises the device, returns WTCONV_ERR_DEVICE_TIMEOUT if the flag was raised (and clears
  * it), WTCONV_ERR_CUDA if the synchronisation or the read failed, else WTCONV_OK. */
 int wtconv_device_status(void);
 
 /* Diagnostic of the failure path above, with no fault: launches one kernel on `stream` whose
  * single waiting thread waits on a shared-memory barrier that nothing ever completes.  The wait
- * gives up after its bounded number of tries (about half a second) and raises the flag, so the
- * next wtconv_device_status() returns WTCONV_ERR_DEVICE_TIMEOUT (and clears it).  Returns
- * WTCONV_OK once launched, WTCONV_ERR_CUDA if the launch failed. */
+ * gives up after half a second and raises the flag, so the next wtconv_device_status() returns
+ * WTCONV_ERR_DEVICE_TIMEOUT (and clears it).  Returns WTCONV_OK once launched, WTCONV_ERR_CUDA if
+ * the launch failed. */
 int wtconv_selftest_wait_timeout(wtconv_stream_t stream);
+
+/* Diagnostic: the packed-FMA (fma.rn.f32x2) throughput of the current device in TFLOP/s, the
+ * ceiling of the layer's conv arithmetic and the denominator of its ALU roofline.  Runs
+ * independent FMA chains of `iters` steps in 8 CTAs of 256 threads per SM on the legacy default
+ * stream, timed with CUDA events; synchronises the device.  Writes *tflops; returns WTCONV_OK,
+ * WTCONV_ERR_INVALID_ARG (iters <= 0 or tflops NULL) or WTCONV_ERR_CUDA. */
+int wtconv_fp32_fma_peak(int iters, double *tflops);
 
 /* Bytes of device workspace `op` needs for this shape on the current device (0 if none).
  * FORWARD and BACKWARD_INPUT need, for L >= 2, one fp32 per level-1 position

@@ -1269,6 +1269,11 @@ int wtconv_selftest_wait_timeout(wtconv_stream_t stream) {
     return cuda_status(launch_wait_selftest(flag, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int wtconv_fp32_fma_peak(int iters, double *tflops) {
+    if (iters <= 0 || tflops == nullptr) return WTCONV_ERR_INVALID_ARG;
+    return cuda_status(measure_fma_peak(iters, tflops));
+}
+
 int wtconv_device_status(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return WTCONV_ERR_CUDA;
     int v = 0;

@@ -191,13 +191,21 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"((uint32_t)__cvta_generic_to_shared(bar))
                  : "memory");
 }
-// Wait until the phase with parity `parity` has completed.  Bounded: each try suspends the
-// thread for at most kWaitHintNs; after kMaxWaitTries unsuccessful tries (about half a second)
-// it raises *timeout (if given) and returns false.
-constexpr uint32_t kMaxWaitTries = 1u << 19;
+// Wait until the phase with parity `parity` has completed.  Bounded by elapsed time: after
+// kMaxWaitNs of %globaltimer time (half a second; a copy or handshake that takes that long is
+// broken, not slow) it raises *timeout (if given) and returns false.  Each try suspends the thread
+// for at most kWaitHintNs; kMaxWaitTries is only a backstop should the timer not advance.
+constexpr uint64_t kMaxWaitNs = 500000000ull;
+constexpr uint32_t kMaxWaitTries = 1u << 24;
 constexpr uint32_t kWaitHintNs = 1000;
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *timeout) {
     const uint32_t addr = (uint32_t)__cvta_generic_to_shared(bar);
+    uint64_t t0 = 0;
     for (uint32_t i = 0; i < kMaxWaitTries; ++i) {
         uint32_t done;
         asm volatile(
@@ -208,6 +216,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *t
             : "r"(addr), "r"(parity), "n"(kWaitHintNs)
             : "memory");
         if (done) return true;
+        if ((i & 15) == 0) {
+            const uint64_t now = global_ns();
+            if (i == 0) t0 = now;
+            else if (now - t0 > kMaxWaitNs) break;
+        }
     }
     if (timeout) atomicExch(timeout, 1);
     return false;

@@ -179,7 +179,14 @@ __global__ void __launch_bounds__(kDwPlaneMaxThreads, (K <= 5 ? 2 : 1))
         const uint32_t parity = (uint32_t)(nbuf == 2 ? k >> 1 : k) & 1u;
         // warp 0 waits for the copies, the others at the barrier; all leave together if the wait gave up
         const bool gave_up = tid < 32 && !mbar_wait(&bar[bf], parity, a.timeout);
-        if (__syncthreads_or(gave_up)) break;
+        if (__syncthreads_or(gave_up)) {
+            // the flag is raised: this CTA's partials become NaN (the gradients show it), and the
+            // CTA leaves without touching the buffers a copy may still target
+            const int ns = 1 + 4 * L;
+            float *part = a.partials + ((size_t)nbi * a.C + c) * ns * NA;
+            for (int i = tid; i < ns * NA; i += nt) part[i] = __int_as_float(0x7fc00000);
+            return;
+        }
         // the other buffer was last read before the barrier that ended the previous plane
         if (nbuf == 2 && tid == 0 && k + 1 < n_planes) issue(k + 1);
         float *X = reinterpret_cast<float *>(base + (bf ? lay.x[1] : lay.x[0]));

@@ -102,7 +102,14 @@ __global__ void __launch_bounds__(32, (K <= 5 ? 12 : 8)) wtconv_dw_tile_kernel(c
 
     if (u_begin < u_end) issue(u_begin);
     for (int u = u_begin; u < u_end; ++u) {
-        if (!mbar_wait(&bar, (uint32_t)(u - u_begin) & 1, a.timeout)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar, (uint32_t)(u - u_begin) & 1, a.timeout))) {
+            // the flag is raised: this CTA's partials become NaN (the gradients show it), and the
+            // CTA leaves without touching the buffers a copy may still target
+            const int ns = 1 + 4 * a.L;
+            float *part = a.partials + ((size_t)nbi * a.C + c) * ns * (KK + 1);
+            for (int i = lane; i < ns * (KK + 1); i += 32) part[i] = __int_as_float(0x7fc00000);
+            return;
+        }
         __syncwarp();
         if constexpr (kConvert) {
             // raw tiles -> fp32, loads first, then the stores

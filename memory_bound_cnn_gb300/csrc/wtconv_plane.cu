@@ -163,7 +163,10 @@ __global__ void __launch_bounds__(kPlaneThreads, (K <= 5 ? 4 : 2)) wtconv_plane_
     const int l2_drow = nt / w2c, l2_dcol = nt - l2_drow * w2c;
 
     for (int b = b_begin; b < b_end; ++b) {
-        if (!mbar_wait(&bar, (uint32_t)(b - b_begin) & 1, a.timeout)) break;
+        // thread 0 waits for the copy, the others at the barrier; all leave together if it gave
+        // up (the flag is raised and this CTA's remaining outputs stay unwritten)
+        const bool gave_up = tid == 0 && !mbar_wait(&bar, (uint32_t)(b - b_begin) & 1, a.timeout);
+        if (__syncthreads_or(gave_up)) return;
         if constexpr (kConvert) {
             const uint2 *r2 = reinterpret_cast<const uint2 *>(raw);
             float4 *x4 = reinterpret_cast<float4 *>(X);

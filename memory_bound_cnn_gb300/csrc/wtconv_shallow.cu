@@ -212,8 +212,9 @@ __global__ void __launch_bounds__(32, (K <= 5 ? 16 : 8)) wtconv_shallow_kernel(c
         // 1. this unit's tiles have landed
         const uint32_t parity = (uint32_t)(u - u_begin) & 1;
         cp_async_wait_all();
-        if (tma_x && !mbar_wait(&bar_x, parity, a.timeout)) break;
-        if (tma_d && !mbar_wait(&bar_d, parity, a.timeout)) break;
+        // a wait that gave up raised the flag: this CTA's remaining outputs stay unwritten
+        if (tma_x && !mbar_wait(&bar_x, parity, a.timeout)) return;
+        if (tma_d && !mbar_wait(&bar_d, parity, a.timeout)) return;
         __syncthreads();
         const float *X;
         if constexpr (kConvert) {

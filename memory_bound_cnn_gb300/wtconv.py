@@ -8,11 +8,15 @@ call raises.
 Functions carry the C names: ``wtconv_forward``, ``wtconv_backward_input``,
 ``wtconv_backward_weights``, ``wtconv_backward``, ``wtconv_backward_weights_noalloc``,
 ``wtconv_workspace_size``, ``wtconv_launch_count``, ``wtconv_plan_kernels``, ``wtconv_device_status``,
-``wtconv_selftest_wait_timeout``, ``wtconv_strerror``, ``wtconv_version``.  ``WTConvFunction`` wraps forward and the fused
-backward as a ``torch.autograd.Function``.
+``wtconv_selftest_wait_timeout``, ``wtconv_fp32_fma_peak``, ``wtconv_strerror``, ``wtconv_version``.
+``WTConvFunction`` wraps forward and the fused backward as a ``torch.autograd.Function``.
+
+Every call runs with the activations' device current (the library plans, looks up its device
+symbols and launches on the current device), and rejects a stream or workspace on another device.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -31,7 +35,7 @@ DTYPE_CODE = {v: k for k, v in TORCH_DTYPE.items()}
 EXPORTED = ("wtconv_version", "wtconv_strerror", "wtconv_workspace_size", "wtconv_forward",
             "wtconv_backward_input", "wtconv_backward_weights", "wtconv_backward",
             "wtconv_backward_weights_noalloc", "wtconv_launch_count", "wtconv_device_status",
-            "wtconv_plan_kernels", "wtconv_selftest_wait_timeout")
+            "wtconv_plan_kernels", "wtconv_selftest_wait_timeout", "wtconv_fp32_fma_peak")
 
 _lib = None
 
@@ -55,9 +59,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     if build_if_missing:
         try:
             path = _build.build()
-        except (OSError, RuntimeError) as e:  # no nvcc here: use what is built, if anything
+        except OSError as e:  # no nvcc here: use what is built, if anything
             if not os.path.exists(path):
                 raise RuntimeError(f"libwtconv.so is not built and cannot be built: {e}") from e
+        # a compile error (RuntimeError) propagates: a stale library must not stand in for it
     lib = ctypes.CDLL(path)
     i, vp, sz, fp = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
     lib.wtconv_version.restype = i
@@ -74,6 +79,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.wtconv_selftest_wait_timeout.argtypes = [ctypes.c_void_p]
     lib.wtconv_launch_count.restype = i
     lib.wtconv_launch_count.argtypes = [i] * 8
+    lib.wtconv_fp32_fma_peak.restype = i
+    lib.wtconv_fp32_fma_peak.argtypes = [i, ctypes.POINTER(ctypes.c_double)]
     shape = [i] * 7
     params = [fp] * 5
     lib.wtconv_forward.restype = i
@@ -121,6 +128,14 @@ def wtconv_selftest_wait_timeout(stream=None) -> None:
 
 def wtconv_launch_count(op: int, B: int, C: int, H: int, W: int, L: int, k: int, dtype: int) -> int:
     return load().wtconv_launch_count(op, B, C, H, W, L, k, dtype)
+
+
+def wtconv_fp32_fma_peak(iters: int = 20000, device=None) -> float:
+    """Packed-FMA throughput of the device in TFLOP/s (synchronises it)."""
+    out = ctypes.c_double(0.0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _raise(load().wtconv_fp32_fma_peak(iters, ctypes.byref(out)), "wtconv_fp32_fma_peak")
+    return out.value
 
 
 # ------------------------------------------------------------------------------- marshalling
@@ -189,6 +204,23 @@ def _raise(status: int, where: str):
         raise WTConvError(status, where)
 
 
+def check_devices(device: torch.device, stream=None, workspace: torch.Tensor | None = None):
+    """Raise ValueError if an explicit stream or workspace lives on another device than `device`
+    (the activations' device): the library would launch on one device with another's memory."""
+    if stream is not None and getattr(stream, "device", device) != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
+    if workspace is not None and workspace.device != device:
+        raise ValueError(f"workspace is on {workspace.device}, the tensors on {device}")
+
+
+@contextlib.contextmanager
+def _on(device: torch.device, stream, workspace):
+    """The activations' device made current for the call (checked against stream and workspace)."""
+    check_devices(device, stream, workspace)
+    with torch.cuda.device(device):
+        yield
+
+
 def wtconv_forward(x, base_w, base_bias, base_scale, wavelet_w, wavelet_scale, y=None, workspace=None,
                    stream=None) -> torch.Tensor:
     """y = WTConv(x); x (B, C, H, W) fp32 / bf16 / fp16 on CUDA, parameters fp32."""
@@ -198,8 +230,9 @@ def wtconv_forward(x, base_w, base_bias, base_scale, wavelet_w, wavelet_scale, y
     if y is None:
         y = torch.empty_like(x)
     _check_out(y, "y", x)
-    ws, nbytes = _workspace(OP_FORWARD, shape, x.device, workspace)
-    rc = load().wtconv_forward(*shape, _ptr(x), *p, _ptr(y), _ptr(ws), nbytes, _stream(stream))
+    with _on(x.device, stream, workspace):
+        ws, nbytes = _workspace(OP_FORWARD, shape, x.device, workspace)
+        rc = load().wtconv_forward(*shape, _ptr(x), *p, _ptr(y), _ptr(ws), nbytes, _stream(stream))
     _raise(rc, "wtconv_forward")
     return y
 
@@ -213,8 +246,9 @@ def wtconv_backward_input(dy, base_w, base_bias, base_scale, wavelet_w, wavelet_
     if dx is None:
         dx = torch.empty_like(dy)
     _check_out(dx, "dx", dy)
-    ws, nbytes = _workspace(OP_BACKWARD_INPUT, shape, dy.device, workspace)
-    rc = load().wtconv_backward_input(*shape, *p, _ptr(dy), _ptr(dx), _ptr(ws), nbytes, _stream(stream))
+    with _on(dy.device, stream, workspace):
+        ws, nbytes = _workspace(OP_BACKWARD_INPUT, shape, dy.device, workspace)
+        rc = load().wtconv_backward_input(*shape, *p, _ptr(dy), _ptr(dx), _ptr(ws), nbytes, _stream(stream))
     _raise(rc, "wtconv_backward_input")
     return dx
 
@@ -243,8 +277,10 @@ def wtconv_backward_weights(x, dy, base_w, base_bias, base_scale, wavelet_w, wav
     shape = _shape(x, wavelet_w, base_w)
     p = _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, x)
     grads, gp = _grad_buffers(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, grads)
-    ws, nbytes = _workspace(OP_BACKWARD_WEIGHTS, shape, x.device, workspace)
-    rc = load().wtconv_backward_weights(*shape, _ptr(x), _ptr(dy), *p, *gp, _ptr(ws), nbytes, _stream(stream))
+    with _on(x.device, stream, workspace):
+        ws, nbytes = _workspace(OP_BACKWARD_WEIGHTS, shape, x.device, workspace)
+        rc = load().wtconv_backward_weights(*shape, _ptr(x), _ptr(dy), *p, *gp, _ptr(ws), nbytes,
+                                            _stream(stream))
     _raise(rc, "wtconv_backward_weights")
     return grads
 
@@ -263,7 +299,8 @@ def wtconv_backward_weights_noalloc(x, dy, base_w, base_bias, base_scale, wavele
     shape = _shape(x, wavelet_w, base_w)
     p = _params(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, x)
     grads, gp = _grad_buffers(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, grads)
-    rc = load().wtconv_backward_weights_noalloc(*shape, _ptr(x), _ptr(dy), *p, *gp, _stream(stream))
+    with _on(x.device, stream, None):
+        rc = load().wtconv_backward_weights_noalloc(*shape, _ptr(x), _ptr(dy), *p, *gp, _stream(stream))
     _raise(rc, "wtconv_backward_weights_noalloc")
     return grads
 
@@ -280,9 +317,10 @@ def wtconv_backward(x, dy, base_w, base_bias, base_scale, wavelet_w, wavelet_sca
     _check_out(dx, "dx", x)
     _check_out(dy, "dy", x)
     grads, gp = _grad_buffers(base_w, base_bias, base_scale, wavelet_w, wavelet_scale, grads)
-    ws, nbytes = _workspace(OP_BACKWARD, shape, x.device, workspace)
-    rc = load().wtconv_backward(*shape, _ptr(x), _ptr(dy), *p, _ptr(dx), *gp, _ptr(ws), nbytes,
-                                _stream(stream))
+    with _on(x.device, stream, workspace):
+        ws, nbytes = _workspace(OP_BACKWARD, shape, x.device, workspace)
+        rc = load().wtconv_backward(*shape, _ptr(x), _ptr(dy), *p, _ptr(dx), *gp, _ptr(ws), nbytes,
+                                    _stream(stream))
     _raise(rc, "wtconv_backward")
     return dx, grads
 
@@ -292,8 +330,9 @@ class WTConvFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, x, base_w, base_bias, base_scale, wavelet_w, wavelet_scale):
-        ctx.save_for_backward(x, base_w, base_bias, base_scale, wavelet_w, wavelet_scale)
-        return wtconv_forward(x.contiguous(), base_w, base_bias, base_scale, wavelet_w, wavelet_scale)
+        xc = x.contiguous()  # the backward reads the same contiguous copy
+        ctx.save_for_backward(xc, base_w, base_bias, base_scale, wavelet_w, wavelet_scale)
+        return wtconv_forward(xc, base_w, base_bias, base_scale, wavelet_w, wavelet_scale)
 
     @staticmethod
     def backward(ctx, dy):

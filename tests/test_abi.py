@@ -99,3 +99,22 @@ def test_fault_injection_returns_before_launch(monkeypatch):
     assert lib.wtconv_backward_weights_noalloc(2, 3, 16, 16, 2, 5, 0, FAKE, FAKE, *p5, *p5, None) == W.ERR_INJECTED
     monkeypatch.setenv("WTCONV_INJECT_FAULT", "0")
     assert _fwd(lib, k=4) == W.ERR_INVALID_ARG
+
+
+def test_binding_rejects_stream_or_workspace_on_another_device():
+    """The binding makes the activations' device current for every call; an explicit stream or
+    workspace on another device is rejected before the library is called."""
+    import torch
+
+    d0, d1 = torch.device("cuda", 0), torch.device("cuda", 1)
+
+    class Stream:
+        def __init__(self, device):
+            self.device = device
+
+    W.check_devices(d0)
+    W.check_devices(d0, stream=Stream(d0))
+    with pytest.raises(ValueError, match="stream"):
+        W.check_devices(d0, stream=Stream(d1))
+    with pytest.raises(ValueError, match="workspace"):
+        W.check_devices(d0, workspace=torch.empty(16, dtype=torch.uint8))  # host memory

@@ -104,6 +104,9 @@ SWEEP = [
     (1, 2, 3, 3, 2, 5, "f32"),
     (1, 1, 1, 1, 1, 3, "f32"),       # a single pixel: every level pads
     (2, 2, 1, 37, 3, 5, "bf16"),     # one row, odd width
+    # large fp32 planes on the planner's own choice (tiled kernels)
+    (1, 2, 256, 256, 5, 5, "f32"),
+    (1, 2, 128, 192, 4, 7, "f32"),
 ]
 
 
@@ -182,6 +185,23 @@ def test_autograd_function_matches_oracle():
     y.backward(d["dy"])
     g_ref = oracle.backward(inputs["x"], inputs["dy"], inputs)
     assert_close("autograd dx", np64(leaves["x"].grad), g_ref["dx"], 1e-5)
+    for gname, p in zip(GRADS, PARAMS):
+        assert_close("autograd " + gname, np64(leaves[p].grad), g_ref[gname], 1e-5)
+
+
+def test_autograd_on_a_non_contiguous_input():
+    """A transposed view as input: the forward and the backward read the same contiguous copy."""
+    shape = LayerShape(2, 3, 16, 24, 2, 5, "f32")
+    inputs = make_inputs(shape, seed=4)
+    d = to_device(inputs)
+    xt = d["x"].transpose(2, 3).contiguous().transpose(2, 3)  # same values, non-contiguous
+    assert not xt.is_contiguous()
+    leaves = {k: d[k].clone().requires_grad_(True) for k in PARAMS}
+    xl = xt.clone().requires_grad_(True)
+    y = W.WTConvFunction.apply(xl, *[leaves[p] for p in PARAMS])
+    y.backward(d["dy"])
+    g_ref = oracle.backward(inputs["x"], inputs["dy"], inputs)
+    assert_close("autograd dx (non-contiguous x)", np64(xl.grad), g_ref["dx"], 1e-5)
     for gname, p in zip(GRADS, PARAMS):
         assert_close("autograd " + gname, np64(leaves[p].grad), g_ref[gname], 1e-5)
 
