@@ -440,7 +440,7 @@ def run_gpu(args, world, rank, local):
                             world)
     # every workload configuration, device-timed the same way (fewer steps for the others)
     per_config = []
-    for name in WORKLOAD_ORDER:
+    for name in ([] if args.no_per_config else WORKLOAD_ORDER):
         if name == args.workload:
             entry = dict(head)
         else:
@@ -477,8 +477,9 @@ def run_gpu(args, world, rank, local):
         # device memory a step needs beyond the inputs and parameters: y, dx, the gradients and
         # the workspace of every layer (the autograd arms report the same quantity)
         "step_mem_bytes": step_mem,
-        "per_config": per_config,
     }
+    if per_config:
+        line["per_config"] = per_config
     return line
 
 
@@ -724,7 +725,17 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--peak", action="store_true", help="print only the packed-FMA peak probe's result")
+    ap.add_argument("--no-per-config", action="store_true", help="time the chosen workload only")
+    ap.add_argument("--shape", help="one custom layer B,C,H,W,L,k,dtype instead of a named workload "
+                                    "(e.g. 32,96,64,64,4,5,bf16)")
     args = ap.parse_args(argv)
+    if args.shape:
+        f = args.shape.split(",")
+        if len(f) != 7:
+            ap.error("--shape wants B,C,H,W,L,k,dtype")
+        WORKLOADS["custom"] = [LayerShape(*(int(v) for v in f[:6]), f[6])]
+        args.workload = "custom"
+        args.no_per_config = True
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_env()
     if world > 1:
