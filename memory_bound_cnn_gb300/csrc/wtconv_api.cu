@@ -848,7 +848,7 @@ PairPlan plan_pair_fwd_uncached(int B, int C, int H, int W, int L, int k, int dt
     const int npairs = (B + 1) / 2;
     const int KK = k * k;
     for (const PairShape &sh : kPairShapes) {
-        for (int T : {128, 256}) {
+        for (int T : {64, 128, 256}) {
             for (int G = 1; G <= std::min(npairs, kPairMaxSlots); ++G) {
                 PairArgs a{};
                 a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
@@ -902,7 +902,7 @@ PairPlan plan_pair_dw_uncached(int B, int C, int H, int W, int L, int k, int dty
     const int npairs = (B + 1) / 2;
     const int KK = k * k, nsig = 1 + 4 * L;
     for (const PairShape &sh : kPairShapes) {
-        for (int T : {128, 256}) {
+        for (int T : {64, 128, 256}) {
             for (int G = 1; G <= std::min(npairs, kPairMaxSlots); ++G) {
                 PairArgs a{};
                 a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;

@@ -19,7 +19,7 @@
 
 namespace wtconv {
 
-constexpr int kPairMaxThreads = 256;  // threads per CTA of the batch-pair kernels: 128 or 256
+constexpr int kPairMaxThreads = 256;  // threads per CTA of the batch-pair kernels: 64, 128 or 256
 constexpr int kPairMaxSlots = 64;     // pair slots per CTA group
 
 // Shared-memory geometry of one pair slot, in packed pairs (f2, 8 bytes).
@@ -89,7 +89,7 @@ struct PairArgs {
     int nchunks;            // work units per channel: ceil(ngroups / chunk_groups)
     int units;              // C * nchunks; unit u is channel u / nchunks, chunk u % nchunks
     int grid;               // CTAs (persistent): CTA i takes units [i*units/grid, (i+1)*units/grid)
-    int nthreads;           // CTA size: 128 or 256
+    int nthreads;           // CTA size: 64, 128 or 256
     int nb;                 // partials per (channel, signal, tap) = nchunks
     int tma;                // 1: planes arrive by bulk copies into the raw staging area
     int raw_pair_bytes;     // raw bytes of one pair slot (two planes, or four for the weight gradient)
@@ -115,6 +115,12 @@ struct PairArgs {
     FastDiv dv_xn, dv_xw;   // X build: two-pixel steps per plane, per row
     PairGeo geo;
 };
+
+// Per activation type T (float, __nv_bfloat16, __half), defined in that type's translation unit.
+template <typename T> cudaError_t launch_pair_fwd_typed(const PairArgs &a, size_t smem, cudaStream_t st);
+template <typename T> int occupancy_pair_fwd_typed(int K, size_t smem, int nthreads);
+template <typename T> cudaError_t launch_pair_dw_typed(const PairArgs &a, size_t smem, cudaStream_t st);
+template <typename T> int occupancy_pair_dw_typed(int K, size_t smem, int nthreads);
 
 size_t pair_fwd_smem_bytes(const PairArgs &a, int elem_bytes);
 cudaError_t launch_pair_fwd(const PairArgs &a, int dtype, size_t smem, cudaStream_t st);

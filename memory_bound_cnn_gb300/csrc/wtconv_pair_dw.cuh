@@ -12,6 +12,8 @@
 // k*k tap sums (packed pairs: partial sums of the two planes) in registers across all groups.  At
 // the end the tap sums are reduced in a fixed thread order into one partial per (channel,
 // signal, tap): deterministic, no atomics.
+#pragma once
+
 #include "wtconv_pair.cuh"
 
 namespace wtconv {
@@ -188,13 +190,8 @@ __device__ __forceinline__ void dw_pass1_block(const PairGeo &g, f2_t *slot, con
 
 }  // namespace
 
-size_t pair_dw_smem_bytes(const PairArgs &a, int elem_bytes) {
-    (void)elem_bytes;
-    return pair_dw_layout(a).total;
-}
-
 template <int K, typename T, int NT>
-__global__ void __launch_bounds__(NT, NT == 128 ? (K <= 3 ? 4 : (K == 5 ? 3 : 2)) : 1)
+__global__ void __launch_bounds__(NT, NT == 64 ? (K <= 5 ? 6 : 4) : NT == 128 ? (K <= 3 ? 4 : (K == 5 ? 3 : 2)) : 1)
     wtconv_pair_dw_kernel(const __grid_constant__ PairArgs a) {
     constexpr int P = K / 2, KK = K * K, NA = KK + 1;
     extern __shared__ __align__(128) unsigned char pair_smem[];
@@ -366,8 +363,10 @@ __global__ void __launch_bounds__(NT, NT == 128 ? (K <= 3 ? 4 : (K == 5 ? 3 : 2)
 }
 
 template <int K, typename T>
-static cudaError_t launch_pair_dw_t(const PairArgs &a, size_t smem, cudaStream_t st) {
-    auto kern = a.nthreads == 256 ? wtconv_pair_dw_kernel<K, T, 256> : wtconv_pair_dw_kernel<K, T, 128>;
+cudaError_t launch_pair_dw_t(const PairArgs &a, size_t smem, cudaStream_t st) {
+    auto kern = a.nthreads == 256  ? wtconv_pair_dw_kernel<K, T, 256>
+                : a.nthreads == 64 ? wtconv_pair_dw_kernel<K, T, 64>
+                                   : wtconv_pair_dw_kernel<K, T, 128>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<dim3((unsigned)a.grid), (unsigned)a.nthreads, smem, st>>>(a);
@@ -375,36 +374,14 @@ static cudaError_t launch_pair_dw_t(const PairArgs &a, size_t smem, cudaStream_t
 }
 
 template <int K, typename T>
-static int occ_pair_dw_t(size_t smem, int nthreads) {
-    auto kern = nthreads == 256 ? wtconv_pair_dw_kernel<K, T, 256> : wtconv_pair_dw_kernel<K, T, 128>;
+int occ_pair_dw_t(size_t smem, int nthreads) {
+    auto kern = nthreads == 256  ? wtconv_pair_dw_kernel<K, T, 256>
+                : nthreads == 64 ? wtconv_pair_dw_kernel<K, T, 64>
+                                 : wtconv_pair_dw_kernel<K, T, 128>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, nthreads, smem) != cudaSuccess) return 0;
     return n;
-}
-
-#define WTCONV_PAIRDW_DISPATCH(K_, DT_, FN, ...)                                          \
-    switch ((K_) * 4 + (DT_)) {                                                           \
-    case 3 * 4 + 0: return FN<3, float>(__VA_ARGS__);                                     \
-    case 3 * 4 + 1: return FN<3, __nv_bfloat16>(__VA_ARGS__);                             \
-    case 3 * 4 + 2: return FN<3, __half>(__VA_ARGS__);                                    \
-    case 5 * 4 + 0: return FN<5, float>(__VA_ARGS__);                                     \
-    case 5 * 4 + 1: return FN<5, __nv_bfloat16>(__VA_ARGS__);                             \
-    case 5 * 4 + 2: return FN<5, __half>(__VA_ARGS__);                                    \
-    case 7 * 4 + 0: return FN<7, float>(__VA_ARGS__);                                     \
-    case 7 * 4 + 1: return FN<7, __nv_bfloat16>(__VA_ARGS__);                             \
-    case 7 * 4 + 2: return FN<7, __half>(__VA_ARGS__);                                    \
-    default: break;                                                                       \
-    }
-
-cudaError_t launch_pair_dw(const PairArgs &a, int dtype, size_t smem, cudaStream_t st) {
-    WTCONV_PAIRDW_DISPATCH(a.K, dtype, launch_pair_dw_t, a, smem, st);
-    return cudaErrorInvalidValue;
-}
-
-int occupancy_pair_dw(int dtype, int K, size_t smem, int nthreads) {
-    WTCONV_PAIRDW_DISPATCH(K, dtype, occ_pair_dw_t, smem, nthreads);
-    return 0;
 }
 
 }  // namespace wtconv

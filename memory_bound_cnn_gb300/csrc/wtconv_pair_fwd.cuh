@@ -16,6 +16,8 @@
 //      each pair of output rows completes, add the level-1 inverse butterflies of Z^1 and store
 //      the two planes' pixels.
 // x is read once from HBM and y written once; nothing else leaves the chip.
+#pragma once
+
 #include "wtconv_pair.cuh"
 
 namespace wtconv {
@@ -356,13 +358,8 @@ __device__ __forceinline__ void pass1(const PairArgs &a, const PairGeo &g, f2_t 
 
 }  // namespace
 
-size_t pair_fwd_smem_bytes(const PairArgs &a, int elem_bytes) {
-    (void)elem_bytes;
-    return pair_fwd_layout(a).total;
-}
-
 template <int K, typename T, int NT>
-__global__ void __launch_bounds__(NT, NT == 128 ? (K <= 3 ? 4 : (K == 5 ? 3 : 2)) : 1)
+__global__ void __launch_bounds__(NT, NT == 64 ? (K <= 5 ? 6 : 4) : NT == 128 ? (K <= 3 ? 4 : (K == 5 ? 3 : 2)) : 1)
     wtconv_pair_fwd_kernel(const __grid_constant__ PairArgs a) {
     extern __shared__ __align__(128) unsigned char pair_smem[];
     __shared__ __align__(8) uint64_t bar;
@@ -507,8 +504,10 @@ __global__ void __launch_bounds__(NT, NT == 128 ? (K <= 3 ? 4 : (K == 5 ? 3 : 2)
 }
 
 template <int K, typename T>
-static cudaError_t launch_pair_fwd_t(const PairArgs &a, size_t smem, cudaStream_t st) {
-    auto kern = a.nthreads == 256 ? wtconv_pair_fwd_kernel<K, T, 256> : wtconv_pair_fwd_kernel<K, T, 128>;
+cudaError_t launch_pair_fwd_t(const PairArgs &a, size_t smem, cudaStream_t st) {
+    auto kern = a.nthreads == 256  ? wtconv_pair_fwd_kernel<K, T, 256>
+                : a.nthreads == 64 ? wtconv_pair_fwd_kernel<K, T, 64>
+                                   : wtconv_pair_fwd_kernel<K, T, 128>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<dim3((unsigned)a.grid), (unsigned)a.nthreads, smem, st>>>(a);
@@ -516,36 +515,14 @@ static cudaError_t launch_pair_fwd_t(const PairArgs &a, size_t smem, cudaStream_
 }
 
 template <int K, typename T>
-static int occ_pair_fwd_t(size_t smem, int nthreads) {
-    auto kern = nthreads == 256 ? wtconv_pair_fwd_kernel<K, T, 256> : wtconv_pair_fwd_kernel<K, T, 128>;
+int occ_pair_fwd_t(size_t smem, int nthreads) {
+    auto kern = nthreads == 256  ? wtconv_pair_fwd_kernel<K, T, 256>
+                : nthreads == 64 ? wtconv_pair_fwd_kernel<K, T, 64>
+                                 : wtconv_pair_fwd_kernel<K, T, 128>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, nthreads, smem) != cudaSuccess) return 0;
     return n;
-}
-
-#define WTCONV_PAIR_DISPATCH(K_, DT_, FN, ...)                                            \
-    switch ((K_) * 4 + (DT_)) {                                                           \
-    case 3 * 4 + 0: return FN<3, float>(__VA_ARGS__);                                     \
-    case 3 * 4 + 1: return FN<3, __nv_bfloat16>(__VA_ARGS__);                             \
-    case 3 * 4 + 2: return FN<3, __half>(__VA_ARGS__);                                    \
-    case 5 * 4 + 0: return FN<5, float>(__VA_ARGS__);                                     \
-    case 5 * 4 + 1: return FN<5, __nv_bfloat16>(__VA_ARGS__);                             \
-    case 5 * 4 + 2: return FN<5, __half>(__VA_ARGS__);                                    \
-    case 7 * 4 + 0: return FN<7, float>(__VA_ARGS__);                                     \
-    case 7 * 4 + 1: return FN<7, __nv_bfloat16>(__VA_ARGS__);                             \
-    case 7 * 4 + 2: return FN<7, __half>(__VA_ARGS__);                                    \
-    default: break;                                                                       \
-    }
-
-cudaError_t launch_pair_fwd(const PairArgs &a, int dtype, size_t smem, cudaStream_t st) {
-    WTCONV_PAIR_DISPATCH(a.K, dtype, launch_pair_fwd_t, a, smem, st);
-    return cudaErrorInvalidValue;
-}
-
-int occupancy_pair_fwd(int dtype, int K, size_t smem, int nthreads) {
-    WTCONV_PAIR_DISPATCH(K, dtype, occ_pair_fwd_t, smem, nthreads);
-    return 0;
 }
 
 }  // namespace wtconv
