@@ -786,6 +786,9 @@ const PairShape kPairShapes[] = {
     {4, 4, 4, 4, 4, 4, 0.76}, {2, 4, 2, 4, 2, 4, 0.70},
 };
 
+// Relative speed of a shape-specialised forward instantiation over the generic one (GB300).
+constexpr double kSpecGain = 1.4;
+
 struct PairPlan {
     int status = WTCONV_ERR_UNSUPPORTED;
     PairArgs a{};
@@ -794,6 +797,17 @@ struct PairPlan {
     double score = 0.0;
     size_t workspace = 0;  // weight gradient: partials
 };
+
+// Planner restrictions for tuning runs: WTCONV_PAIR_THREADS (64, 128 or 256) keeps one CTA
+// size, WTCONV_PAIR_SHAPE (an index into kPairShapes) one item shape.
+bool pair_threads_allowed(int T) {
+    const char *v = getenv("WTCONV_PAIR_THREADS");
+    return !(v && v[0]) || atoi(v) == T;
+}
+bool pair_shape_allowed(int i) {
+    const char *v = getenv("WTCONV_PAIR_SHAPE");
+    return !(v && v[0]) || atoi(v) == i;
+}
 
 void pair_counts(PairArgs &a) {
     const PairGeo &g = a.geo;
@@ -847,9 +861,20 @@ PairPlan plan_pair_fwd_uncached(int B, int C, int H, int W, int L, int k, int dt
     if (sms <= 0) { best.status = WTCONV_ERR_CUDA; return best; }
     const int npairs = (B + 1) / 2;
     const int KK = k * k;
-    for (const PairShape &sh : kPairShapes) {
+    // a shape with a specialised instantiation takes the CTA size and slots that measured fastest
+    PairSpecPref pref{};
+    const char *knob_t = getenv("WTCONV_PAIR_THREADS"), *knob_s = getenv("WTCONV_PAIR_SHAPE");
+    const bool tuned = pair_spec_measured(H, W, L, k, dtype, &pref) && !(knob_t && knob_t[0]) && !(knob_s && knob_s[0]);
+    for (int si = 0; si < (int)(sizeof(kPairShapes) / sizeof(kPairShapes[0])); ++si) {
+        const PairShape &sh = kPairShapes[si];
+        if (!pair_shape_allowed(si)) continue;
+        const int shp0[6] = {sh.q0, sh.s0, sh.ql, sh.sl, sh.qd, sh.sd};
+        if (tuned && !std::equal(shp0, shp0 + 6, pref.shape)) continue;
         for (int T : {64, 128, 256}) {
+            if (!pair_threads_allowed(T)) continue;
+            if (tuned && pref.threads && T != pref.threads) continue;
             for (int G = 1; G <= std::min(npairs, kPairMaxSlots); ++G) {
+                if (tuned && pref.slots && G != std::min(pref.slots, npairs)) continue;
                 PairArgs a{};
                 a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
                 a.npairs = npairs;
@@ -860,10 +885,13 @@ PairPlan plan_pair_fwd_uncached(int B, int C, int H, int W, int L, int k, int dt
                 a.tma = ((size_t)H * W * eb) % 16 == 0;
                 a.raw_pair_bytes = (int)(((size_t)2 * H * W * eb + 15) / 16 * 16);
                 a.vec_st = (W % 4) == 0;
+                const int shp[6] = {sh.q0, sh.s0, sh.ql, sh.sl, sh.qd, sh.sd};
+                a.spec = pair_spec_index(H, W, L, k, dtype, shp);
                 pair_counts(a);
                 const size_t smem = pair_fwd_smem_bytes(a, eb);
                 if (smem + kStaticSmemMargin > (size_t)kMaxSmem) break;
-                const int occ = occupancy_pair_fwd(dtype, k, smem, T);
+                const int occ = a.spec >= 0 ? occupancy_pair_fwd_spec(a.spec, smem, T)
+                                            : occupancy_pair_fwd(dtype, k, smem, T);
                 if (occ <= 0) break;
                 const PairGeo &g = a.geo;
                 double work = 0.0, tim = 0.0;
@@ -878,7 +906,8 @@ PairPlan plan_pair_fwd_uncached(int B, int C, int H, int W, int L, int k, int dt
                 // resident warps (beyond 16 per SM more warps no longer help); a single resident
                 // CTA also loses its phases' barrier waits, which other CTAs would fill
                 const double warps = std::min((double)occ * T / 32.0, 16.0) * (occ >= 2 ? 1.0 : 0.8);
-                const double score = work / tim * warps;
+                // a shape-specialised instantiation issues far fewer index instructions
+                const double score = work / tim * warps * (a.spec >= 0 ? kSpecGain : 1.0);
                 if (score > best.score * 1.02) {
                     best.status = WTCONV_OK;
                     best.a = a;
@@ -901,8 +930,11 @@ PairPlan plan_pair_dw_uncached(int B, int C, int H, int W, int L, int k, int dty
     if (sms <= 0) { best.status = WTCONV_ERR_CUDA; return best; }
     const int npairs = (B + 1) / 2;
     const int KK = k * k, nsig = 1 + 4 * L;
-    for (const PairShape &sh : kPairShapes) {
+    for (int si = 0; si < (int)(sizeof(kPairShapes) / sizeof(kPairShapes[0])); ++si) {
+        const PairShape &sh = kPairShapes[si];
+        if (!pair_shape_allowed(si)) continue;
         for (int T : {64, 128, 256}) {
+            if (!pair_threads_allowed(T)) continue;
             for (int G = 1; G <= std::min(npairs, kPairMaxSlots); ++G) {
                 PairArgs a{};
                 a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
@@ -911,6 +943,7 @@ PairPlan plan_pair_dw_uncached(int B, int C, int H, int W, int L, int k, int dty
                 a.ngroups = (npairs + G - 1) / G;
                 a.nthreads = T;
                 a.geo = make_pair_geo(H, W, L, k, 1, sh.q0, sh.s0, sh.ql, sh.sl, sh.qd, sh.sd);
+                a.spec = -1;
                 a.tma = ((size_t)H * W * eb) % 16 == 0;
                 a.raw_pair_bytes = (int)(((size_t)4 * H * W * eb + 15) / 16 * 16);
                 pair_counts(a);
@@ -1001,7 +1034,10 @@ PairPlan cached_pair_plan(int kind, int B, int C, int H, int W, int L, int k, in
         p.status = WTCONV_ERR_CUDA;
         return p;
     }
-    const PlanKey key(kind, B, C, H, W, L, k, dtype, dev);
+    // the tuning restrictions are part of the key: a restricted plan is a different plan
+    const char *vt = getenv("WTCONV_PAIR_THREADS"), *vs = getenv("WTCONV_PAIR_SHAPE");
+    const int knobs = (vt && vt[0] ? atoi(vt) : 0) * 16 + (vs && vs[0] ? atoi(vs) + 1 : 0);
+    const PlanKey key(kind + 1000 * knobs, B, C, H, W, L, k, dtype, dev);
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = cache.find(key);
@@ -1012,9 +1048,10 @@ PairPlan cached_pair_plan(int kind, int B, int C, int H, int W, int L, int k, in
     const char *verbose = getenv("WTCONV_VERBOSE");
     if (verbose && verbose[0] == '1')
         fprintf(stderr, "wtconv plan pair-%s B=%d C=%d H=%d W=%d L=%d k=%d dtype=%d: status %d G=%d items %dx%d/%dx%d "
-                        "threads=%d grid=%d units=%d chunk=%d smem=%zu occ=%d tma=%d d=%d score=%.2f\n",
+                        "qd=%d sd=%d spec=%d threads=%d grid=%d units=%d chunk=%d smem=%zu occ=%d tma=%d d=%d score=%.2f\n",
                 kind == 10 ? "fwd" : "dw", B, C, H, W, L, k, dtype, p.status, p.a.G, p.a.geo.Q[0], p.a.geo.S[0],
-                p.a.geo.Q[1], p.a.geo.S[1], p.a.nthreads, p.a.grid, p.a.units, p.a.chunk_groups, p.smem, p.occ,
+                p.a.geo.Q[1], p.a.geo.S[1], L >= 2 ? p.a.geo.Q[2] : 0, L >= 2 ? p.a.geo.S[2] : 0, p.a.spec,
+                p.a.nthreads, p.a.grid, p.a.units, p.a.chunk_groups, p.smem, p.occ,
                 p.a.tma, p.a.per_thread, p.score);
     if (p.status == WTCONV_OK || p.status == WTCONV_ERR_UNSUPPORTED) {
         std::lock_guard<std::mutex> lock(mu);
@@ -1030,16 +1067,18 @@ PairPlan plan_pair_dw(int B, int C, int H, int W, int L, int k, int dtype) {
     return cached_pair_plan(11, B, C, H, W, L, k, dtype);
 }
 
-// Whether the batch-pair kernels run by default.  Measured on GB300 (bf16, k = 5, B = 128): they
-// win on small planes, where the whole-plane kernels' per-plane setup does not amortise (8 x 8
-// planes: forward 56 vs 79 us, weight gradient 138 vs 208 us; 16 x 16: weight gradient 201 vs 208
-// us, forward 93 vs 85 us), and lose on larger ones (32 x 32 forward 203 vs 154 us).
-// WTCONV_PAIR=0 turns them off, =1 makes them the default wherever they apply.
-bool pair_default(bool weight_gradient, int H, int W) {
+// Whether the batch-pair kernels run by default.  For the shapes with a specialised instantiation
+// the choice measured on GB300 decides (wtconv_pair_specs.h); elsewhere the generic batch-pair
+// forward wins only on the smallest planes (8 x 8: 56 vs 79 us, where the whole-plane kernels'
+// per-plane setup does not amortise), the weight gradient up to 28 x 28 planes.  WTCONV_PAIR=0
+// turns them off, =1 makes them the default wherever they apply.
+bool pair_default(bool weight_gradient, int H, int W, int L, int k, int dtype) {
     const char *v = getenv("WTCONV_PAIR");
     if (v && strcmp(v, "0") == 0) return false;
     if (v && strcmp(v, "1") == 0) return true;
-    return (long long)H * W <= (weight_gradient ? 256 : 64);
+    PairSpecPref pref{};
+    if (pair_spec_measured(H, W, L, k, dtype, &pref)) return weight_gradient ? pref.dw_default : pref.fwd_default;
+    return (long long)H * W <= (weight_gradient ? 784 : 64);
 }
 
 // Forward / input-gradient path of a shape (WTCONV_FWD_PATH=fused / tiles / plane selects a path
@@ -1065,7 +1104,7 @@ FwdChoice choose_fwd(int B, int C, int H, int W, int L, int k, int dtype) {
     if (!want_tiles && !want_plane && !want_fused) {
         f.pr = plan_pair_fwd(B, C, H, W, L, k, dtype);
         if (f.pr.status != WTCONV_OK && f.pr.status != WTCONV_ERR_UNSUPPORTED) { f.status = f.pr.status; return f; }
-        if (f.pr.status == WTCONV_OK && (want_pair || pair_default(false, H, W))) {
+        if (f.pr.status == WTCONV_OK && (want_pair || pair_default(false, H, W, L, k, dtype))) {
             f.path = FWD_PAIR;
             return f;
         }
@@ -1123,7 +1162,7 @@ DwChoice choose_dw(int B, int C, int H, int W, int L, int k, int dtype) {
     if (!want_tiles && !want_pyramid && !want_plane && !want_fused) {
         d.pr = plan_pair_dw(B, C, H, W, L, k, dtype);
         if (d.pr.status != WTCONV_OK && d.pr.status != WTCONV_ERR_UNSUPPORTED) { d.status = d.pr.status; return d; }
-        if (d.pr.status == WTCONV_OK && (want_pair || pair_default(true, H, W))) {
+        if (d.pr.status == WTCONV_OK && (want_pair || pair_default(true, H, W, L, k, dtype))) {
             d.path = DW_PAIR;
             d.workspace = d.pr.workspace;
             return d;

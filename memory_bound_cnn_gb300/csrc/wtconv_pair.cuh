@@ -44,11 +44,11 @@ struct PairGeo {
     int slot;                                       // pairs per slot (even)
 };
 
-__host__ __device__ inline int pg_round2(int v) { return (v + 1) & ~1; }
+__host__ __device__ constexpr inline int pg_round2(int v) { return (v + 1) & ~1; }
 
 // q0 / s0: item shape of the base path; ql / sl: of level 1; qd / sd: of the levels >= 2 (rows per
 // item drop to 4 on images of at most 4 rows).
-__host__ __device__ inline PairGeo make_pair_geo(int H, int W, int L, int K, int kind, int q0, int s0, int ql,
+__host__ __device__ constexpr inline PairGeo make_pair_geo(int H, int W, int L, int K, int kind, int q0, int s0, int ql,
                                                  int sl, int qd, int sd) {
     PairGeo g = {};
     g.H = H; g.W = W; g.L = L; g.K = K; g.P = K / 2; g.kind = kind;
@@ -94,6 +94,7 @@ struct PairArgs {
     int tma;                // 1: planes arrive by bulk copies into the raw staging area
     int raw_pair_bytes;     // raw bytes of one pair slot (two planes, or four for the weight gradient)
     int vec_st;             // 1: rows allow 4-element vector stores / loads of activations
+    int spec;               // >= 0: the shape-specialised instantiation of this index runs (else -1)
     const void *x;          // forward: x; input gradient: dy; weight gradient: x
     const void *dy;         // weight gradient: dy
     void *out;              // y or dx
@@ -121,6 +122,20 @@ template <typename T> cudaError_t launch_pair_fwd_typed(const PairArgs &a, size_
 template <typename T> int occupancy_pair_fwd_typed(int K, size_t smem, int nthreads);
 template <typename T> cudaError_t launch_pair_dw_typed(const PairArgs &a, size_t smem, cudaStream_t st);
 template <typename T> int occupancy_pair_dw_typed(int K, size_t smem, int nthreads);
+
+// Index of the shape-specialised instantiation for this layer shape and item shapes (q0, s0, ql,
+// sl, qd, sd), or -1; and its occupancy.
+int pair_spec_index(int H, int W, int L, int K, int dtype, const int (&shape)[6]);
+int occupancy_pair_fwd_spec(int spec, size_t smem, int nthreads);
+
+// What measured fastest on GB300 for a layer shape that has a specialised instantiation: its item
+// shapes, the forward's CTA size and pair slots per group (0: the planner's choice), and whether
+// the batch-pair forward / weight gradient is the default for the shape.
+struct PairSpecPref {
+    int shape[6];
+    int threads, slots, fwd_default, dw_default;
+};
+bool pair_spec_measured(int H, int W, int L, int K, int dtype, PairSpecPref *pref);
 
 size_t pair_fwd_smem_bytes(const PairArgs &a, int elem_bytes);
 cudaError_t launch_pair_fwd(const PairArgs &a, int dtype, size_t smem, cudaStream_t st);

@@ -155,10 +155,18 @@ __device__ __forceinline__ void pair_out_item(const f2_t *__restrict__ in, int p
     }
 }
 
+// n / d for an index decode: with a compile-time geometry (FIX) d is a constant after inlining
+// and the division becomes a multiply-shift; otherwise the planner's fast divisor of d.
+template <bool FIX>
+__device__ __forceinline__ int divq(int n, int d, const FastDiv &f) {
+    if constexpr (FIX) return n / d;
+    else return (int)fdiv(f, (uint32_t)n);
+}
+
 // Conv items of level l of every slot (every subband image), in the order of a flat item list
 // whose first `base` entries went to the threads before: thread tid takes items e with
 // (base + e) % nt == tid.  The level's geometry sits in registers for the whole loop.
-template <int K, int Q, int S>
+template <int K, int Q, int S, bool FIX>
 __device__ __forceinline__ void conv_level(const PairArgs &a, const PairGeo &g, f2_t *slots, const f2_t *wts, int np,
                                            int l, int base) {
     constexpr int WP = wpairs(K), KK = K * K;
@@ -171,8 +179,8 @@ __device__ __forceinline__ void conv_level(const PairArgs &a, const PairGeo &g, 
     int e = (int)threadIdx.x - base % nt;
     if (e < 0) e += nt;
     for (; e < n; e += nt) {
-        const int img = (int)fdiv(dpi, (uint32_t)e), rem = e - img * per_img;
-        const int seg = (int)fdiv(dns, (uint32_t)rem), strip = rem - seg * ns;
+        const int img = divq<FIX>(e, per_img, dpi), rem = e - img * per_img;
+        const int seg = divq<FIX>(rem, ns, dns), strip = rem - seg * ns;
         const int gs = img >> 2, s = img & 3;
         f2_t w[KK];
         load_weights<K>(wts + (1 + 4 * (l - 1) + s) * WP, w);
@@ -237,20 +245,20 @@ __device__ __forceinline__ void analysis_deep_pass(const PairGeo &g, f2_t *slots
 }
 
 // Output items of every slot with item shape Q x S (the base kernel in registers for the loop).
-template <int K, int Q, int S, typename T>
+template <int K, int Q, int S, typename T, bool FIX>
 __device__ __forceinline__ void out_phase(const PairArgs &a, const PairGeo &g, const f2_t *slots, const f2_t *wts,
                                           int np, int p0, int c, f2_t bias2, T *out) {
     constexpr int KK = K * K;
     f2_t w[KK];
     load_weights<K>(wts, w);
     const int ns0 = g.ns[0], ip0 = g.ipitch[0], zp1 = g.zpitch[1], zi1 = g.zimg[1];
-    const int ox = g.off_x, oz1 = g.off_z[1], slot = g.slot, n_out = a.n_out;
-    const int B = a.B, C = a.C, H = a.H, W = a.W;
+    const int ox = g.off_x, oz1 = g.off_z[1], slot = g.slot, n_out = g.ns[0] * g.ng[0];
+    const int B = a.B, C = a.C, H = g.H, W = g.W;
     const size_t HW = (size_t)H * W;
     const bool vec = a.vec_st != 0;
     for (int t = threadIdx.x; t < np * n_out; t += blockDim.x) {
-        const int gs = (int)fdiv(a.dv_nout, (uint32_t)t), e = t - gs * n_out;
-        const int seg = (int)fdiv(a.dv_out_ns, (uint32_t)e), strip = e - seg * ns0;
+        const int gs = divq<FIX>(t, n_out, a.dv_nout), e = t - gs * n_out;
+        const int seg = divq<FIX>(e, ns0, a.dv_out_ns), strip = e - seg * ns0;
         const int r0 = seg * S, c0 = strip * Q;
         const f2_t *sl = slots + (size_t)gs * slot;
         const int b0 = 2 * (p0 + gs);
@@ -264,14 +272,14 @@ __device__ __forceinline__ void out_phase(const PairArgs &a, const PairGeo &g, c
 // First analysis pass: 4x4 (L >= 2) or 2x2 (L == 1) blocks of the raw planes -> the interleaved
 // padded copy X and the Haar level 1 (and level 2) quads of every slot.  plane(gs, q) gives the raw
 // plane q of slot gs, or null past B.
-template <int BS, typename T, typename PlaneFn>
+template <int BS, typename T, bool FIX, typename PlaneFn>
 __device__ __forceinline__ void pass1(const PairArgs &a, const PairGeo &g, f2_t *slots, int np, PlaneFn plane) {
-    const int P = g.P, W = a.W, bw = W / BS;
+    const int P = g.P, W = g.W, bw = W / BS, n_a = (g.H / BS) * bw;
     const int p1 = g.ipitch[1], i1 = g.iimg[1], oy1 = g.off_y[1];
     const int p2 = BS == 4 ? g.ipitch[2] : 0, i2 = BS == 4 ? g.iimg[2] : 0, oy2 = BS == 4 ? g.off_y[2] : 0;
-    for (int t = threadIdx.x; t < np * a.n_a; t += blockDim.x) {
-        const int gs = (int)fdiv(a.dv_na, (uint32_t)t), blk = t - gs * a.n_a;
-        const int bi = (int)fdiv(a.dv_naw, (uint32_t)blk), bj = blk - bi * bw;
+    for (int t = threadIdx.x; t < np * n_a; t += blockDim.x) {
+        const int gs = divq<FIX>(t, n_a, a.dv_na), blk = t - gs * n_a;
+        const int bi = divq<FIX>(blk, bw, a.dv_naw), bj = blk - bi * bw;
         f2_t *slot = slots + (size_t)gs * g.slot;
         f2_t X[BS][BS];
         {
@@ -358,20 +366,21 @@ __device__ __forceinline__ void pass1(const PairArgs &a, const PairGeo &g, f2_t 
 
 }  // namespace
 
-template <int K, typename T, int NT>
-__global__ void __launch_bounds__(NT, NT == 64 ? (K <= 5 ? 6 : 4) : NT == 128 ? (K <= 3 ? 4 : (K == 5 ? 3 : 2)) : 1)
-    wtconv_pair_fwd_kernel(const __grid_constant__ PairArgs a) {
+// The forward kernel's body, for a geometry `g` that is either the plan's (runtime values) or,
+// with FIX, a compile-time constant of a specialised instantiation: then every pitch and offset is
+// an immediate, the level loops unroll and index decodes divide by constants.
+template <int K, typename T, bool FIX>
+__device__ __forceinline__ void pair_fwd_body(const PairArgs &a, const PairGeo &g) {
     extern __shared__ __align__(128) unsigned char pair_smem[];
     __shared__ __align__(8) uint64_t bar;
     __shared__ int copy_ok;
     const uint32_t s0 = (uint32_t)__cvta_generic_to_shared(pair_smem);
     unsigned char *base = pair_smem + (((s0 + 127u) & ~127u) - s0);
     const PairFwdLayout lay = pair_fwd_layout(a);
-    const PairGeo &g = a.geo;
     f2_t *slots = reinterpret_cast<f2_t *>(base + lay.slots);
     f2_t *wts = reinterpret_cast<f2_t *>(base + lay.wts);
     const int tid = threadIdx.x, nt = blockDim.x;
-    const int B = a.B, C = a.C, H = a.H, W = a.W, L = a.L;
+    const int B = a.B, C = a.C, H = g.H, W = g.W, L = g.L;
     const size_t HW = (size_t)H * W;
     const T *x = static_cast<const T *>(a.x);
     T *out = static_cast<T *>(a.out);
@@ -432,25 +441,31 @@ __global__ void __launch_bounds__(NT, NT == 64 ? (K <= 5 ? 6 : 4) : NT == 128 ? 
             return a.tma ? raw + (size_t)gs * raw_pair + q * HW : x + ((size_t)b * C + c) * HW;
         };
         // ---- pass 1: X and Haar levels 1 (and 2)
-        if (L >= 2) pass1<4, T>(a, g, slots, np, plane);
-        else pass1<2, T>(a, g, slots, np, plane);
+        if (L >= 2) pass1<4, T, FIX>(a, g, slots, np, plane);
+        else pass1<2, T, FIX>(a, g, slots, np, plane);
         __syncthreads();
         if (a.tma && tid == 0 && u + 1 < u1) issue(u + 1);  // the raw planes are free
         // ---- deeper passes: levels 3 (and 4), then 5
+#pragma unroll(FIX ? 2 : 1)
         for (int l0 = 3; l0 <= L; l0 += 2) {
             analysis_deep_pass(g, slots, np, l0, L);
             __syncthreads();
         }
         // ---- conv items of every subband image of every level
-        for (int l = 1; l <= L; ++l) {
-            const int base_l = np * a.conv_start[l];
-            const int Ql = g.Q[l], Sl = g.S[l];
-            if (Ql == 4) {
-                if (Sl == 8) conv_level<K, 4, 8>(a, g, slots, wts, np, l, base_l);
-                else conv_level<K, 4, 4>(a, g, slots, wts, np, l, base_l);
-            } else {
-                if (Sl == 8) conv_level<K, 2, 8>(a, g, slots, wts, np, l, base_l);
-                else conv_level<K, 2, 4>(a, g, slots, wts, np, l, base_l);
+        {
+            int first = 0;  // conv items of the levels before l, per slot
+#pragma unroll(FIX ? kMaxLevels : 1)
+            for (int l = 1; l <= L; ++l) {
+                const int base_l = np * first;
+                first += 4 * g.ns[l] * g.ng[l];
+                const int Ql = g.Q[l], Sl = g.S[l];
+                if (Ql == 4) {
+                    if (Sl == 8) conv_level<K, 4, 8, FIX>(a, g, slots, wts, np, l, base_l);
+                    else conv_level<K, 4, 4, FIX>(a, g, slots, wts, np, l, base_l);
+                } else {
+                    if (Sl == 8) conv_level<K, 2, 8, FIX>(a, g, slots, wts, np, l, base_l);
+                    else conv_level<K, 2, 4, FIX>(a, g, slots, wts, np, l, base_l);
+                }
             }
         }
         __syncthreads();
@@ -458,13 +473,15 @@ __global__ void __launch_bounds__(NT, NT == 64 ? (K <= 5 ? 6 : 4) : NT == 128 ? 
         if (L >= 2) {
             const int w2 = g.w[2];
             const int zp1 = g.zpitch[1];
-            for (int t = tid; t < np * a.n_gather; t += nt) {
-                const int gs = (int)fdiv(a.dv_ngather, (uint32_t)t), e = t - gs * a.n_gather;
-                const int i2 = (int)fdiv(a.dv_gw, (uint32_t)e), j2 = e - i2 * w2;
+            const int n_gather = g.h[2] * w2;
+            for (int t = tid; t < np * n_gather; t += nt) {
+                const int gs = divq<FIX>(t, n_gather, a.dv_ngather), e = t - gs * n_gather;
+                const int i2 = divq<FIX>(e, w2, a.dv_gw), j2 = e - i2 * w2;
                 f2_t *slot = slots + (size_t)gs * g.slot;
                 const f2_t *z2 = slot + g.off_z[2] + i2 * g.zpitch[2] + j2;
                 const int zi2 = g.zimg[2];
                 f2_t v = pk2(0.f, 0.f);
+#pragma unroll(FIX ? kMaxLevels : 1)
                 for (int l = 3; l <= L; ++l) {
                     const int sh = l - 2;
                     const f2_t *zl = slot + g.off_z[l] + (i2 >> sh) * g.zpitch[l] + (j2 >> sh);
@@ -493,32 +510,59 @@ __global__ void __launch_bounds__(NT, NT == 64 ? (K <= 5 ? 6 : 4) : NT == 128 ? 
         const f2_t bias2 = pk2(bias, bias);
         const int Q0 = g.Q[0], S0 = g.S[0];
         if (Q0 == 4) {
-            if (S0 == 8) out_phase<K, 4, 8, T>(a, g, slots, wts, np, p0, c, bias2, out);
-            else out_phase<K, 4, 4, T>(a, g, slots, wts, np, p0, c, bias2, out);
+            if (S0 == 8) out_phase<K, 4, 8, T, FIX>(a, g, slots, wts, np, p0, c, bias2, out);
+            else out_phase<K, 4, 4, T, FIX>(a, g, slots, wts, np, p0, c, bias2, out);
         } else {
-            if (S0 == 8) out_phase<K, 2, 8, T>(a, g, slots, wts, np, p0, c, bias2, out);
-            else out_phase<K, 2, 4, T>(a, g, slots, wts, np, p0, c, bias2, out);
+            if (S0 == 8) out_phase<K, 2, 8, T, FIX>(a, g, slots, wts, np, p0, c, bias2, out);
+            else out_phase<K, 2, 4, T, FIX>(a, g, slots, wts, np, p0, c, bias2, out);
         }
         __syncthreads();
     }
 }
 
-template <int K, typename T>
+// Geometry of a kernel instantiation: the plan's at run time, or a shape fixed at compile time.
+// A fixed geometry lives in a device constant the compiler folds wherever the index is known.
+template <int K, int H, int W, int L, int Q0, int S0, int QL, int SL, int QD, int SD, int KIND>
+__device__ constexpr PairGeo kPairSpecGeo = make_pair_geo(H, W, L, K, KIND, Q0, S0, QL, SL, QD, SD);
+
+struct PairDynSpec {
+    static constexpr bool fixed = false;
+};
+template <int H_, int W_, int L_, int Q0, int S0, int QL, int SL, int QD, int SD>
+struct PairShapeSpec {
+    static constexpr bool fixed = true;
+    template <int K, int KIND>
+    static __device__ __forceinline__ const PairGeo &geo() {
+        return kPairSpecGeo<K, H_, W_, L_, Q0, S0, QL, SL, QD, SD, KIND>;
+    }
+};
+
+template <int K, typename T, int NT, class Spec>
+__global__ void __launch_bounds__(NT, NT == 64 ? (K <= 5 ? 6 : 4) : NT == 128 ? (K <= 3 ? 4 : (K == 5 ? 3 : 2)) : 1)
+    wtconv_pair_fwd_kernel(const __grid_constant__ PairArgs a) {
+    if constexpr (Spec::fixed) {
+        pair_fwd_body<K, T, true>(a, Spec::template geo<K, 0>());
+    } else {
+        pair_fwd_body<K, T, false>(a, a.geo);
+    }
+}
+
+template <int K, typename T, class Spec = PairDynSpec>
 cudaError_t launch_pair_fwd_t(const PairArgs &a, size_t smem, cudaStream_t st) {
-    auto kern = a.nthreads == 256  ? wtconv_pair_fwd_kernel<K, T, 256>
-                : a.nthreads == 64 ? wtconv_pair_fwd_kernel<K, T, 64>
-                                   : wtconv_pair_fwd_kernel<K, T, 128>;
+    auto kern = a.nthreads == 256  ? wtconv_pair_fwd_kernel<K, T, 256, Spec>
+                : a.nthreads == 64 ? wtconv_pair_fwd_kernel<K, T, 64, Spec>
+                                   : wtconv_pair_fwd_kernel<K, T, 128, Spec>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<dim3((unsigned)a.grid), (unsigned)a.nthreads, smem, st>>>(a);
     return cudaGetLastError();
 }
 
-template <int K, typename T>
+template <int K, typename T, class Spec = PairDynSpec>
 int occ_pair_fwd_t(size_t smem, int nthreads) {
-    auto kern = nthreads == 256  ? wtconv_pair_fwd_kernel<K, T, 256>
-                : nthreads == 64 ? wtconv_pair_fwd_kernel<K, T, 64>
-                                 : wtconv_pair_fwd_kernel<K, T, 128>;
+    auto kern = nthreads == 256  ? wtconv_pair_fwd_kernel<K, T, 256, Spec>
+                : nthreads == 64 ? wtconv_pair_fwd_kernel<K, T, 64, Spec>
+                                 : wtconv_pair_fwd_kernel<K, T, 128, Spec>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, nthreads, smem) != cudaSuccess) return 0;

@@ -2,8 +2,57 @@
 // type to the per-type translation units.
 #include "wtconv_pair_dw.cuh"
 #include "wtconv_pair_fwd.cuh"
+#include "wtconv_pair_specs.h"
 
 namespace wtconv {
+
+#define WTCONV_DECL_ONE(spec) WTCONV_CALL(WTCONV_PAIR_SPEC_DECL, spec)
+WTCONV_PAIR_SPEC_LIST(WTCONV_DECL_ONE)
+
+namespace {
+
+struct PairSpecEntry {
+    int H, W, L, K, dtype, shape[6];
+    int fwd_threads, fwd_slots, fwd_default, dw_default;
+    cudaError_t (*launch_fwd)(const PairArgs &, size_t, cudaStream_t);
+    int (*occ_fwd)(size_t, int);
+};
+
+#define WTCONV_ENTRY(name, H, W, L, K, T, dt, q0, s0, ql, sl, qd, sd, nt, g, fd, dd)                  \
+    {H, W, L, K, dt, {q0, s0, ql, sl, qd, sd}, nt, g, fd, dd, launch_pair_fwd_spec_##name,           \
+     occupancy_pair_fwd_spec_##name},
+#define WTCONV_ENTRY_ONE(spec) WTCONV_CALL(WTCONV_ENTRY, spec)
+const PairSpecEntry kSpecs[] = {WTCONV_PAIR_SPEC_LIST(WTCONV_ENTRY_ONE)};
+
+}  // namespace
+
+int pair_spec_index(int H, int W, int L, int K, int dtype, const int (&shape)[6]) {
+    for (int i = 0; i < (int)(sizeof(kSpecs) / sizeof(kSpecs[0])); ++i) {
+        const PairSpecEntry &e = kSpecs[i];
+        if (e.H == H && e.W == W && e.L == L && e.K == K && e.dtype == dtype) {
+            bool same = true;
+            for (int j = 0; j < 6; ++j) same = same && e.shape[j] == shape[j];
+            if (same) return i;
+        }
+    }
+    return -1;
+}
+
+int occupancy_pair_fwd_spec(int spec, size_t smem, int nthreads) { return kSpecs[spec].occ_fwd(smem, nthreads); }
+
+bool pair_spec_measured(int H, int W, int L, int K, int dtype, PairSpecPref *pref) {
+    for (const PairSpecEntry &e : kSpecs) {
+        if (e.H == H && e.W == W && e.L == L && e.K == K && e.dtype == dtype) {
+            for (int j = 0; j < 6; ++j) pref->shape[j] = e.shape[j];
+            pref->threads = e.fwd_threads;
+            pref->slots = e.fwd_slots;
+            pref->fwd_default = e.fwd_default;
+            pref->dw_default = e.dw_default;
+            return true;
+        }
+    }
+    return false;
+}
 
 size_t pair_fwd_smem_bytes(const PairArgs &a, int elem_bytes) {
     (void)elem_bytes;
@@ -16,6 +65,7 @@ size_t pair_dw_smem_bytes(const PairArgs &a, int elem_bytes) {
 }
 
 cudaError_t launch_pair_fwd(const PairArgs &a, int dtype, size_t smem, cudaStream_t st) {
+    if (a.spec >= 0) return kSpecs[a.spec].launch_fwd(a, smem, st);
     switch (dtype) {
     case 0: return launch_pair_fwd_typed<float>(a, smem, st);
     case 1: return launch_pair_fwd_typed<__nv_bfloat16>(a, smem, st);
