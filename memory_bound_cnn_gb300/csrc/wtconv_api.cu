@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <map>
 #include <mutex>
 #include <string>
@@ -17,6 +18,7 @@
 #include "wtconv_internal.h"
 #include "wtconv_pad.h"
 #include "wtconv_pair.cuh"
+#include "wtconv_ptile.h"
 #include "wtconv_selftest.h"
 
 using namespace wtconv;
@@ -477,6 +479,20 @@ bool encode_map(CUtensorMap *m, CUtensorMapDataType dt, int eb, const void *base
     if (fn == nullptr) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)C, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)W * eb, (cuuint64_t)H * W * eb, (cuuint64_t)C * H * W * eb};
+    const cuuint32_t box[4] = {(cuuint32_t)bw, (cuuint32_t)bh, 1u, (cuuint32_t)bb};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same for planes stored with a row pitch of `pitch` elements (pitch * eb a multiple of 16).
+bool encode_map_pitched(CUtensorMap *m, CUtensorMapDataType dt, int eb, const void *base, int W, int H, int C, int B,
+                        int pitch, int bw, int bh, int bb) {
+    EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)C, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)pitch * eb, (cuuint64_t)H * pitch * eb, (cuuint64_t)C * H * pitch * eb};
     const cuuint32_t box[4] = {(cuuint32_t)bw, (cuuint32_t)bh, 1u, (cuuint32_t)bb};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1081,6 +1097,250 @@ bool pair_default(bool weight_gradient, int H, int W, int L, int k, int dtype) {
     return (long long)H * W <= (weight_gradient ? 784 : 64);
 }
 
+// ------------------------------------------------------- tiled batch-pair weight gradient plan
+//
+// Launch 0 correlates the base path and levels 1 .. min(L, 2) on tiles of x and dy; while levels
+// remain, it writes the level-2 LL bands of x and dy as fp32 planes and launch i + 1 takes the
+// next (up to) two levels from them (lvl_off = 2 (i + 1)).  All launches write the same rows of
+// partials [nchunks][C][1 + 4L][K*K+1], each its own signals.
+struct PtPlan {
+    int status = WTCONV_ERR_UNSUPPORTED;
+    int nlaunch = 0;
+    PtileArgs a[3];
+    size_t smem[3] = {0, 0, 0};
+    int occ[3] = {0, 0, 0};
+    size_t ll_off[3] = {0, 0, 0};     // workspace offset of launch i's LL planes (x, then dy at + ll_half)
+    size_t ll_half[3] = {0, 0, 0};
+    size_t partial_bytes = 0;
+    size_t workspace = 0;
+};
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Geometry of one launch on B x C planes of H x W elements (row pitch in_pitch, element size eb)
+// with tiles of TH x TW and G pairs per group; false where the bulk tensor copies cannot apply.
+bool pt_make(PtileArgs &a, int B, int C, int H, int W, int in_pitch, int eb, int K, int LT, int base, int lvl_off,
+             int L_total, int TH, int TW, int G, int nt, bool small) {
+    a = PtileArgs{};
+    const int P = K / 2, BS = 1 << LT;
+    a.B = B; a.C = C; a.H = H; a.W = W; a.K = K; a.LT = LT; a.base = base; a.lvl_off = lvl_off;
+    a.L_total = L_total;
+    a.TH = TH; a.TW = TW; a.G = G; a.nthreads = nt;
+    // a tile that covers the whole plane needs no halo: outside the plane every level is zero,
+    // which the zeroed slots already hold
+    const bool whole = TH >= H && TW >= W;
+    a.HX = whole ? 0 : BS * P;
+    const int al = 16 / eb;
+    a.HXL = (a.HX + al - 1) / al * al;
+    a.RXR = TH + 2 * a.HX;
+    a.RXW = TW + 2 * a.HXL;
+    a.in_pitch = in_pitch;
+    if (TH % BS != 0 || TW % BS != 0 || TH <= 0 || TW <= 0) return false;
+    if (((size_t)TW * eb) % 16 != 0 || ((size_t)in_pitch * eb) % 16 != 0) return false;
+    if (a.RXW > 256 || a.RXR > 256 || 2 * G > 256 || TW > 256 || TH > 256) return false;
+    a.tiles_r = (H + TH - 1) / TH;
+    a.tiles_c = (W + TW - 1) / TW;
+    a.tiles = a.tiles_r * a.tiles_c;
+    int off = 0;
+    for (int l = 0; l <= LT; ++l) {
+        PtLevel &v = a.lv[l];
+        v.h = TH >> l;
+        v.w = TW >> l;
+        v.Q = small ? 2 : 4;  // one item width per launch (levels narrower than Q round up)
+        v.S = v.h >= 8 ? 8 : 4;
+        v.ns = (v.w + v.Q - 1) / v.Q;
+        v.ng = (v.h + v.S - 1) / v.S;
+        v.ipitch = pg_round2(v.Q * v.ns + K - 1);
+        v.irows = v.ng * v.S + K - 1;
+        v.iimg = v.ipitch * v.irows;
+        v.zpitch = pg_round2(v.Q * v.ns);
+        v.zrows = v.ng * v.S;
+        v.zimg = v.zpitch * v.zrows;
+        v.items = v.ns * v.ng;
+    }
+    if (base) {
+        a.lv[0].off_y = off; off += a.lv[0].iimg;
+        a.lv[0].off_z = off; off += a.lv[0].zimg;
+    }
+    for (int l = 1; l <= LT; ++l) { a.lv[l].off_y = off; off += 4 * a.lv[l].iimg; }
+    for (int l = 1; l <= LT; ++l) { a.lv[l].off_z = off; off += 4 * a.lv[l].zimg; }
+    a.slot = pg_round2(off);
+    a.n0 = base ? a.lv[0].items : 0;
+    a.n1 = a.lv[1].items;
+    a.n2 = LT >= 2 ? a.lv[2].items : 0;
+    a.per_pair = a.n0 + 4 * a.n1 + 4 * a.n2;
+    a.raw_x_bytes = (int)(((size_t)2 * G * a.RXR * a.RXW * eb + 127) / 128 * 128);
+    a.raw_dy_bytes = (int)(((size_t)2 * G * TH * TW * eb + 127) / 128 * 128);
+    a.npairs = (B + 1) / 2;
+    a.ngroups = (a.npairs + G - 1) / G;
+    a.work = a.tiles * a.ngroups;
+    a.ll_out = L_total - lvl_off > LT ? 1 : 0;
+    if (a.ll_out && LT != 2) return false;
+    a.ll_h = H / 4;
+    a.ll_w = W / 4;
+    a.ll_pitch = (a.ll_w + 3) / 4 * 4;
+    a.dv_pp = make_fastdiv(a.per_pair);
+    a.dv_n1 = make_fastdiv(std::max(1, a.n1));
+    a.dv_n2 = make_fastdiv(std::max(1, a.n2));
+    for (int l = 0; l <= kPtMaxLevels; ++l) a.dv_ns[l] = make_fastdiv(l <= LT ? a.lv[l].ns : 1);
+    a.dv_ngroups = make_fastdiv(a.ngroups);
+    a.dv_tiles_c = make_fastdiv(a.tiles_c);
+    const int xbw = (TW + 2 * a.HX) / BS, xbh = (TH + 2 * a.HX) / BS;
+    a.dv_xbw = make_fastdiv(xbw);
+    a.dv_xb = make_fastdiv(xbw * xbh);
+    a.dv_dbw = make_fastdiv(TW / BS);
+    a.dv_db = make_fastdiv((TW / BS) * (TH / BS));
+    return true;
+}
+
+// Tuning restrictions (0: planner's choice): WTCONV_PTILE=TH,TW,G,threads[,small items 0/1].
+void pt_knobs(int &th, int &tw, int &g, int &nt, int &sm) {
+    th = tw = g = nt = 0;
+    sm = -1;
+    const char *v = getenv("WTCONV_PTILE");
+    if (v && v[0]) sscanf(v, "%d,%d,%d,%d,%d", &th, &tw, &g, &nt, &sm);
+}
+
+// Best geometry of one launch: for each tile and CTA size, the largest G that keeps two CTAs per
+// SM resident, scored by how evenly a group's items fill the CTA's threads and by resident warps.
+bool pt_choose(PtileArgs &best, size_t &best_smem, int &best_occ, int B, int C, int H, int W, int in_pitch, int eb,
+               int dtype, int K, int LT, int base, int lvl_off, int L_total) {
+    int kth = 0, ktw = 0, kg = 0, knt = 0, ksm = -1;
+    if (base) pt_knobs(kth, ktw, kg, knt, ksm);  // the restrictions apply to the first launch
+    const int BS = 1 << LT, al = 16 / eb;
+    const int Hr = (H + BS - 1) / BS * BS;
+    const int Wr = (W + std::max(BS, al) - 1) / std::max(BS, al) * std::max(BS, al);
+    const int sms = device_sms();
+    if (sms <= 0) return false;
+    double best_score = -1.0;
+    for (int th0 : {16, 32, 64}) {
+        const int TH = std::min(th0, Hr);
+        if (kth && TH != kth) continue;
+        for (int tw0 : {32, 64}) {
+            const int TW = std::min(tw0, Wr);
+            if (ktw && TW != ktw) continue;
+            if (th0 > 16 && TH < th0 && TH == std::min(th0 / 2, Hr)) continue;  // same tile as a smaller th0
+            if (tw0 > 32 && TW < tw0 && TW == std::min(tw0 / 2, Wr)) continue;
+            for (int nt : {128, 256})
+            for (int small = 0; small < 2; ++small) {
+                if (knt && nt != knt) continue;
+                if (ksm >= 0 && small != ksm) continue;
+                for (int G = 1; G <= 16; ++G) {
+                    if (kg && G != kg) continue;
+                    PtileArgs a;
+                    if (!pt_make(a, B, C, H, W, in_pitch, eb, K, LT, base, lvl_off, L_total, TH, TW, G, nt, small))
+                        break;
+                    if (G > a.npairs) break;
+                    const size_t smem = ptile_smem_bytes(a, eb);
+                    if (smem + kStaticSmemMargin > (size_t)kMaxSmem) break;
+                    const int occ = occupancy_ptile_dw(base ? dtype : WTCONV_F32, K, LT, base, smem, nt, a.lv[0].Q);
+                    if (occ <= 0) break;
+                    // Measured on GB300 (256 x 256 bf16 planes, L = 5): resident threads decide
+                    // first (the kernel is latency-bound: 4 x 128 threads ran 1.26x faster than
+                    // 3 x 128), CTAs of 128 beat 256 at equal residency (one barrier spans fewer
+                    // warps), then how evenly a group's items fill the threads (a group takes as
+                    // long as its busiest thread) and the share of the x tile that is halo.
+                    const long long items = (long long)a.per_pair * G;
+                    const double fill = (double)items / ((double)((items + nt - 1) / nt) * nt);
+                    const double resident = std::min(512.0, (double)occ * nt) / 512.0;
+                    const double cta = nt == 128 ? 1.0 : 0.7;
+                    const double load = small ? 0.9 : 1.0;  // narrower items: more loads per FMA
+                    const double halo = (double)(TH * TW) / ((double)a.RXR * (TW + 2 * a.HX));
+                    const double tiles_used = (double)H * W / ((double)a.tiles * TH * TW);
+                    const double score =
+                        resident * cta * std::sqrt(fill) * load * std::sqrt(std::sqrt(halo)) * tiles_used;
+                    const char *vb = getenv("WTCONV_VERBOSE");
+                    if (vb && vb[0] == '2')
+                        fprintf(stderr, "  ptile candidate %dx%d q=%d G=%d nt=%d smem=%zu occ=%d fill=%.3f halo=%.3f score=%.4f\n",
+                                TH, TW, a.lv[0].Q, G, nt, smem, occ, fill, halo, score);
+                    if (score > best_score) {
+                        best_score = score;
+                        best = a;
+                        best_smem = smem;
+                        best_occ = occ;
+                    }
+                }
+            }
+        }
+    }
+    return best_score > 0.0;
+}
+
+PtPlan plan_ptile_dw_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
+    PtPlan p;
+    const int eb = elem_bytes(dtype);
+    if (B < 1 || L < 1 || H % (1 << L) != 0 || W % (1 << L) != 0) return p;
+    const int sms = device_sms();
+    if (sms <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
+    int h = H, w = W, pitch = W, e = eb, lvl = 0;
+    for (int i = 0; lvl < L; ++i) {
+        const int LT = std::min(2, L - lvl);
+        if (!pt_choose(p.a[i], p.smem[i], p.occ[i], B, C, h, w, pitch, e, dtype, k, LT, i == 0 ? 1 : 0, lvl, L)) return p;
+        lvl += LT;
+        if (p.a[i].ll_out) {
+            h = p.a[i].ll_h;
+            w = p.a[i].ll_w;
+            pitch = p.a[i].ll_pitch;
+            e = 4;
+        }
+        p.nlaunch = i + 1;
+    }
+    // partial rows per channel: enough units to keep every resident CTA of launch 0 busy
+    const PtileArgs &a0 = p.a[0];
+    const long long slots = (long long)sms * p.occ[0];
+    int nchunks = (int)std::min<long long>(a0.work, std::max<long long>(1, (2 * slots + C - 1) / C));
+    size_t off = 0;
+    const int nsig = 1 + 4 * L, NA = k * k + 1;
+    p.partial_bytes = round256((size_t)nchunks * C * nsig * NA * sizeof(float));
+    off = p.partial_bytes;
+    for (int i = 0; i < p.nlaunch; ++i) {
+        PtileArgs &a = p.a[i];
+        a.nchunks = nchunks;
+        a.units = C * nchunks;
+        a.grid = (int)std::min<long long>(a.units, (long long)sms * p.occ[i]);
+        if (a.ll_out) {
+            p.ll_half[i] = round256((size_t)B * C * a.ll_h * a.ll_pitch * sizeof(float));
+            p.ll_off[i] = off;
+            off += 2 * p.ll_half[i];
+        }
+    }
+    p.workspace = off;
+    p.status = WTCONV_OK;
+    return p;
+}
+
+PtPlan plan_ptile_dw(int B, int C, int H, int W, int L, int k, int dtype) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int, int, int, int, int, std::string>, PtPlan> cache;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        PtPlan p;
+        p.status = WTCONV_ERR_CUDA;
+        return p;
+    }
+    const char *kn = getenv("WTCONV_PTILE");
+    const auto key = std::make_tuple(B, C, H, W, L, k, dtype, dev, std::string(kn ? kn : ""));
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    PtPlan p = plan_ptile_dw_uncached(B, C, H, W, L, k, dtype);
+    const char *verbose = getenv("WTCONV_VERBOSE");
+    if (verbose && verbose[0] == '1')
+        for (int i = 0; i < p.nlaunch; ++i)
+            fprintf(stderr, "wtconv plan ptile-dw[%d] B=%d C=%d H=%d W=%d L=%d k=%d dtype=%d: status %d LT=%d base=%d "
+                            "tile=%dx%d halo=%d G=%d threads=%d items/pair=%d (%dx%d) grid=%d units=%d chunks=%d smem=%zu occ=%d\n",
+                    i, B, C, p.a[i].H, p.a[i].W, L, k, dtype, p.status, p.a[i].LT, p.a[i].base, p.a[i].TH, p.a[i].TW,
+                    p.a[i].HX, p.a[i].G, p.a[i].nthreads, p.a[i].per_pair, p.a[i].lv[1].Q, p.a[i].lv[1].S, p.a[i].grid,
+                    p.a[i].units, p.a[i].nchunks, p.smem[i], p.occ[i]);
+    if (p.status == WTCONV_OK || p.status == WTCONV_ERR_UNSUPPORTED) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache.emplace(key, p);
+    }
+    return p;
+}
+
 // Forward / input-gradient path of a shape (WTCONV_FWD_PATH=fused / tiles / plane selects a path
 // where it applies).  By default the fused whole-plane kernel runs where it measured fastest on
 // GB300: fp32 planes with at least 64 output items and three or more resident CTAs per SM; else
@@ -1129,11 +1389,12 @@ FwdChoice choose_fwd(int B, int C, int H, int W, int L, int k, int dtype) {
     return f;
 }
 
-// Which weight-gradient path a call takes: the fused whole-plane kernel where it applies and
-// measured fastest, else the whole-plane kernel where a plane fits, else the tiled kernels where
-// they apply, else the workspace pyramids.  WTCONV_DW_PATH=fused, =tiles, =plane or =pyramid
+// Which weight-gradient path a call takes: the batch-pair kernel where it measured fastest, the
+// fused whole-plane kernel where it applies and measured fastest, else the whole-plane kernel
+// where a plane fits, else the tiled batch-pair kernel, else the tiled kernels where they apply,
+// else the workspace pyramids.  WTCONV_DW_PATH=pair, =fused, =plane, =ptile, =tiles or =pyramid
 // selects a path where it applies (for testing and comparison).
-enum DwPath { DW_TILE, DW_PLANE, DW_PYRAMID, DW_FUSED, DW_PAIR };
+enum DwPath { DW_TILE, DW_PLANE, DW_PYRAMID, DW_FUSED, DW_PAIR, DW_PTILE };
 struct DwChoice {
     int status = WTCONV_OK;
     DwPath path = DW_PLANE;
@@ -1141,6 +1402,7 @@ struct DwChoice {
     Plan p;
     FPlan f;
     PairPlan pr;
+    PtPlan pt;
     size_t workspace = 0;
 };
 
@@ -1159,6 +1421,16 @@ DwChoice choose_dw(int B, int C, int H, int W, int L, int k, int dtype) {
     const bool want_fused = env && strcmp(env, "fused") == 0;
     const bool want_plane = env && strcmp(env, "plane") == 0;
     const bool want_pair = env && strcmp(env, "pair") == 0;
+    const bool want_ptile = env && strcmp(env, "ptile") == 0;
+    if (want_ptile) {
+        d.pt = plan_ptile_dw(B, C, H, W, L, k, dtype);
+        if (d.pt.status != WTCONV_OK && d.pt.status != WTCONV_ERR_UNSUPPORTED) { d.status = d.pt.status; return d; }
+        if (d.pt.status == WTCONV_OK) {
+            d.path = DW_PTILE;
+            d.workspace = d.pt.workspace;
+            return d;
+        }
+    }
     if (!want_tiles && !want_pyramid && !want_plane && !want_fused) {
         d.pr = plan_pair_dw(B, C, H, W, L, k, dtype);
         if (d.pr.status != WTCONV_OK && d.pr.status != WTCONV_ERR_UNSUPPORTED) { d.status = d.pr.status; return d; }
@@ -1183,6 +1455,17 @@ DwChoice choose_dw(int B, int C, int H, int W, int L, int k, int dtype) {
         if (!d.p.dw_pyramid) {
             d.path = DW_PLANE;
             d.workspace = d.p.workspace;
+            return d;
+        }
+    }
+    // planes too large for the whole-plane kernels: the tiled batch-pair kernel where its bulk
+    // copies apply (256 x 256 bf16 planes, L = 5: 582 vs 882 us), else the tiled kernels
+    if (!want_tiles && !want_pyramid) {
+        d.pt = plan_ptile_dw(B, C, H, W, L, k, dtype);
+        if (d.pt.status != WTCONV_OK && d.pt.status != WTCONV_ERR_UNSUPPORTED) { d.status = d.pt.status; return d; }
+        if (d.pt.status == WTCONV_OK) {
+            d.path = DW_PTILE;
+            d.workspace = d.pt.workspace;
             return d;
         }
     }
@@ -1341,7 +1624,8 @@ static const char *plan_kernels_inner(int op, int B, int C, int H, int W, int L,
     const DwChoice d = choose_dw(B, C, H, W, L, k, dtype);
     if (d.status != WTCONV_OK) return "";
     if (dw) {
-        return d.path == DW_PAIR ? "wtconv_pair_dw_kernel+wtconv_dw_finalize_kernel"
+        return d.path == DW_PTILE ? "wtconv_ptile_dw_kernel+wtconv_dw_finalize_kernel"
+             : d.path == DW_PAIR ? "wtconv_pair_dw_kernel+wtconv_dw_finalize_kernel"
              : d.path == DW_FUSED ? "wtconv_dw_plane_kernel+wtconv_dw_finalize_kernel"
              : d.path == DW_PLANE ? "wtconv_dw_kernel+wtconv_dw_finalize_kernel"
              : d.path == DW_TILE ? "wtconv_dw_tile_kernel+wtconv_level2_kernel+wtconv_haar_level_kernel+"
@@ -1352,7 +1636,8 @@ static const char *plan_kernels_inner(int op, int B, int C, int H, int W, int L,
     // combination; static storage)
     static std::mutex mu;
     static std::map<std::string, std::string> names;
-    const std::string dws = d.path == DW_PAIR ? "wtconv_pair_dw_kernel+wtconv_dw_finalize_kernel"
+    const std::string dws = d.path == DW_PTILE ? "wtconv_ptile_dw_kernel+wtconv_dw_finalize_kernel"
+                            : d.path == DW_PAIR ? "wtconv_pair_dw_kernel+wtconv_dw_finalize_kernel"
                             : d.path == DW_FUSED ? "wtconv_dw_plane_kernel+wtconv_dw_finalize_kernel"
                             : d.path == DW_PLANE ? "wtconv_dw_kernel+wtconv_dw_finalize_kernel"
                             : d.path == DW_TILE ? "wtconv_dw_tile_kernel+wtconv_level2_kernel+wtconv_haar_level_kernel+"
@@ -1402,6 +1687,7 @@ static int launch_count_inner(int op, int B, int C, int H, int W, int L, int k, 
         const DwChoice d = choose_dw(B, C, H, W, L, k, dtype);
         if (d.status != WTCONV_OK) return 0;
         if (d.path == DW_TILE) n += 2 + (L >= 2 ? 1 + (L - 2) + (L - 1) : 0);  // tiles, level 2, levels, corr, finalize
+        else if (d.path == DW_PTILE) n += d.pt.nlaunch + 1;                       // tile launches, finalize
         else n += d.path == DW_PYRAMID ? 2 * L + 2 : 2;
     }
     return n;
@@ -1565,6 +1851,43 @@ static int run_dw_fused(FPlan &fp, int dtype, const void *x, const void *dy, flo
     return WTCONV_OK;
 }
 
+// Tiled batch-pair weight-gradient launches: partials at the start of `wsp`, the LL planes of the
+// deeper launches after them; fills what the finalize reads.
+static int run_dw_ptile(const PtPlan &pt, int dtype, const void *x, const void *dy, char *wsp, LayerArgs &fin,
+                        cudaStream_t s) {
+    float *partials = reinterpret_cast<float *>(wsp);
+    const void *in_x = x, *in_dy = dy;
+    int in_dtype = dtype;
+    int *timeout = timeout_flag();
+    if (timeout == nullptr) return WTCONV_ERR_CUDA;
+    for (int i = 0; i < pt.nlaunch; ++i) {
+        PtileArgs a = pt.a[i];
+        a.x = in_x;
+        a.dy = in_dy;
+        a.partials = partials;
+        a.timeout = timeout;
+        if (a.ll_out) {
+            a.ll_x = reinterpret_cast<float *>(wsp + pt.ll_off[i]);
+            a.ll_dy = reinterpret_cast<float *>(wsp + pt.ll_off[i] + pt.ll_half[i]);
+        }
+        const int eb = elem_bytes(in_dtype);
+        if (!encode_map_pitched(&a.tmap_x, tma_dtype(in_dtype), eb, in_x, a.W, a.H, a.C, a.B, a.in_pitch, a.RXW, a.RXR,
+                                2 * a.G) ||
+            !encode_map_pitched(&a.tmap_dy, tma_dtype(in_dtype), eb, in_dy, a.W, a.H, a.C, a.B, a.in_pitch, a.TW, a.TH,
+                                2 * a.G))
+            return WTCONV_ERR_CUDA;
+        if (launch_ptile_dw(a, in_dtype, pt.smem[i], s) != cudaSuccess) return WTCONV_ERR_CUDA;
+        in_x = a.ll_x;
+        in_dy = a.ll_dy;
+        in_dtype = WTCONV_F32;
+    }
+    const PtileArgs &a0 = pt.a[0];
+    fin.B = a0.B; fin.C = a0.C; fin.H = a0.H; fin.W = a0.W; fin.L = a0.L_total; fin.K = a0.K;
+    fin.nb = a0.nchunks;
+    fin.partials = partials;
+    return WTCONV_OK;
+}
+
 // Batch-pair weight-gradient kernel into `partials`; fills what the finalize reads.
 static int run_dw_pair(const PairPlan &pp, int dtype, const void *x, const void *dy, float *partials, LayerArgs &fin,
                        cudaStream_t s) {
@@ -1641,6 +1964,9 @@ static int backward_common(bool want_dx, int B, int C, int H, int W, int L, int 
         if (st != WTCONV_OK) return st;
     } else if (dc.path == DW_PAIR) {
         st = run_dw_pair(dc.pr, dtype, x, dy, reinterpret_cast<float *>(wsp), fin, s);
+        if (st != WTCONV_OK) return st;
+    } else if (dc.path == DW_PTILE) {
+        st = run_dw_ptile(dc.pt, dtype, x, dy, wsp, fin, s);
         if (st != WTCONV_OK) return st;
     } else if (dc.path == DW_PYRAMID) {
         Plan &pw = dc.p;

@@ -3,6 +3,7 @@
 #include "wtconv_pair_dw.cuh"
 #include "wtconv_pair_fwd.cuh"
 #include "wtconv_pair_specs.h"
+#include "wtconv_ptile_dw.cuh"
 
 namespace wtconv {
 
@@ -97,6 +98,38 @@ int occupancy_pair_dw(int dtype, int K, size_t smem, int nthreads) {
     case 0: return occupancy_pair_dw_typed<float>(K, smem, nthreads);
     case 1: return occupancy_pair_dw_typed<__nv_bfloat16>(K, smem, nthreads);
     case 2: return occupancy_pair_dw_typed<__half>(K, smem, nthreads);
+    default: return 0;
+    }
+}
+
+// ---------------------------------------------------------------- tiled batch-pair weight gradient
+
+cudaError_t launch_ptile_dw_f32(const PtileArgs &a, size_t smem, cudaStream_t st);
+cudaError_t launch_ptile_dw_bf16(const PtileArgs &a, size_t smem, cudaStream_t st);
+cudaError_t launch_ptile_dw_f16(const PtileArgs &a, size_t smem, cudaStream_t st);
+int occupancy_ptile_dw_f32(int K, int LT, int base, size_t smem, int nthreads, int iq);
+int occupancy_ptile_dw_bf16(int K, int LT, int base, size_t smem, int nthreads, int iq);
+int occupancy_ptile_dw_f16(int K, int LT, int base, size_t smem, int nthreads, int iq);
+
+size_t ptile_smem_bytes(const PtileArgs &a, int elem_bytes) {
+    (void)elem_bytes;  // the raw tile sizes already count the element size
+    return ptile_layout(a).total;
+}
+
+cudaError_t launch_ptile_dw(const PtileArgs &a, int dtype, size_t smem, cudaStream_t st) {
+    switch (dtype) {
+    case 0: return launch_ptile_dw_f32(a, smem, st);
+    case 1: return launch_ptile_dw_bf16(a, smem, st);
+    case 2: return launch_ptile_dw_f16(a, smem, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int occupancy_ptile_dw(int dtype, int K, int LT, int base, size_t smem, int nthreads, int iq) {
+    switch (dtype) {
+    case 0: return occupancy_ptile_dw_f32(K, LT, base, smem, nthreads, iq);
+    case 1: return occupancy_ptile_dw_bf16(K, LT, base, smem, nthreads, iq);
+    case 2: return occupancy_ptile_dw_f16(K, LT, base, smem, nthreads, iq);
     default: return 0;
     }
 }

@@ -59,9 +59,10 @@ def check_layer(shape: LayerShape, inputs: dict, split: bool = True):
         assert_close("dx (backward_input)", np64(dx2), g_ref["dx"], tol)
         for n in GRADS:
             assert_close(n + " (backward_weights)", np64(g2[n]), g_ref[n], tol)
-    # the weight gradient's other paths (where they apply): the batch-pair kernel, the fused
+    # the weight gradient's other paths (where they apply): the tiled batch-pair kernel, the
+    # batch-pair kernel, the fused
     # whole-plane kernel, the staged whole-plane kernel, tiled kernels and workspace pyramids
-    for dpath in ("pair", "fused", "plane", "tiles", "pyramid"):
+    for dpath in ("ptile", "pair", "fused", "plane", "tiles", "pyramid"):
         if dpath == "pyramid" and shape.numel > 20_000_000:
             continue  # the pyramid path already runs by default where planes are too large
         with env_path("WTCONV_DW_PATH", dpath):
@@ -125,6 +126,20 @@ def test_backward_is_deterministic(case):
     dx2, g2 = gpu_backward(d)
     torch.cuda.synchronize()
     assert torch.equal(dx1, dx2)
+    for n in GRADS:
+        assert torch.equal(g1[n], g2[n]), n
+
+
+@pytest.mark.parametrize("case", [(6, 8, 64, 64, 4, 5, "bf16"), (3, 4, 96, 64, 5, 3, "f32")],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_tiled_pair_weight_gradient_is_deterministic(case):
+    """The tiled batch-pair weight gradient (three launches for L = 5) reduces in a fixed order."""
+    shape = LayerShape(*case)
+    d = to_device(make_inputs(shape, seed=4))
+    with env_path("WTCONV_DW_PATH", "ptile"):
+        g1 = W.wtconv_backward_weights(d["x"], d["dy"], *[d[p] for p in PARAMS])
+        g2 = W.wtconv_backward_weights(d["x"], d["dy"], *[d[p] for p in PARAMS])
+    torch.cuda.synchronize()
     for n in GRADS:
         assert torch.equal(g1[n], g2[n]), n
 
