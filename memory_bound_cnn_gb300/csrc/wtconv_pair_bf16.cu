@@ -1,6 +1,5 @@
-// Batch-pair kernels instantiated for __nv_bfloat16 activations (one translation unit per activation type,
+// Batch-pair forward kernels instantiated for __nv_bfloat16 activations (one translation unit per activation type,
 // so the three compile in parallel).
-#include "wtconv_pair_dw.cuh"
 #include "wtconv_pair_fwd.cuh"
 
 namespace wtconv {
@@ -21,26 +20,6 @@ int occupancy_pair_fwd_typed<__nv_bfloat16>(int K, size_t smem, int nthreads) {
     case 3: return occ_pair_fwd_t<3, __nv_bfloat16>(smem, nthreads);
     case 5: return occ_pair_fwd_t<5, __nv_bfloat16>(smem, nthreads);
     case 7: return occ_pair_fwd_t<7, __nv_bfloat16>(smem, nthreads);
-    default: return 0;
-    }
-}
-
-template <>
-cudaError_t launch_pair_dw_typed<__nv_bfloat16>(const PairArgs &a, size_t smem, cudaStream_t st) {
-    switch (a.K) {
-    case 3: return launch_pair_dw_t<3, __nv_bfloat16>(a, smem, st);
-    case 5: return launch_pair_dw_t<5, __nv_bfloat16>(a, smem, st);
-    case 7: return launch_pair_dw_t<7, __nv_bfloat16>(a, smem, st);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
-template <>
-int occupancy_pair_dw_typed<__nv_bfloat16>(int K, size_t smem, int nthreads) {
-    switch (K) {
-    case 3: return occ_pair_dw_t<3, __nv_bfloat16>(smem, nthreads);
-    case 5: return occ_pair_dw_t<5, __nv_bfloat16>(smem, nthreads);
-    case 7: return occ_pair_dw_t<7, __nv_bfloat16>(smem, nthreads);
     default: return 0;
     }
 }
