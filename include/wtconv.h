@@ -134,7 +134,10 @@ int wtconv_fp32_fma_peak(int iters, double *tflops);
  * FORWARD and BACKWARD_INPUT need, for L >= 2, one fp32 per level-1 position
  * (B*C*(H/2)*(W/2)*4 bytes, rounded up to 256): the contribution of the Haar levels >= 2, which a
  * first kernel computes per plane and the second kernel adds to every output pixel.  The weight
- * gradients need one fp32 partial per (CTA, channel, subband, tap); BACKWARD needs both.
+ * gradients need one fp32 partial per (CTA, channel, subband, tap), and for planes too large
+ * for the whole-plane kernels with L >= 3 also the level-2 (and level-4) low bands of x and dy as
+ * fp32 planes (2 * B*C*(H/4)*(W/4 rounded up to 4)*4 bytes, then the same for H/16, W/16);
+ * BACKWARD needs both.
  * Sides that are not multiples of 2^L add the padded activations (each B*C*Hp*Wp elements,
  * rounded up to 256 bytes): two for FORWARD, BACKWARD_INPUT and BACKWARD_WEIGHTS, three for
  * BACKWARD.
@@ -149,10 +152,11 @@ const char *wtconv_plan_kernels(int op, int B, int C, int H, int W, int L, int k
  * or unsupported shape).  Planes whose Haar pyramid fits in shared memory take one launch for
  * the forward and the input gradient and two for the weight gradients (correlations +
  * finalize); larger planes take two for the forward / input gradient (levels >= 2, then the
- * base conv and level 1) and 2L + 2 for the weight gradients (L pyramid levels, L + 1
- * correlations, finalize).  BACKWARD is the sum of BACKWARD_INPUT and BACKWARD_WEIGHTS.
- * Sides that are not multiples of 2^L add the pads and the crop: two launches for
- * FORWARD, BACKWARD_INPUT and BACKWARD_WEIGHTS, three for BACKWARD. */
+ * base conv and level 1) and, for the weight gradients, one tiled launch per two Haar levels
+ * plus the finalize (ceil(L / 2) + 1; with WTCONV_DW_PATH=tiles the older tiled chain, 2L + 2).
+ * BACKWARD is the sum of BACKWARD_INPUT and BACKWARD_WEIGHTS.  Sides that are not multiples of
+ * 2^L add the pads and the crop: two launches for FORWARD, BACKWARD_INPUT and
+ * BACKWARD_WEIGHTS, three for BACKWARD. */
 int wtconv_launch_count(int op, int B, int C, int H, int W, int L, int k, int dtype);
 
 /* Forward pass (Metodologia: fused on-chip Haar analysis, folded scales, closed-form
@@ -162,9 +166,12 @@ int wtconv_forward(int B, int C, int H, int W, int L, int k, int dtype, const vo
                    const float *wavelet_w, const float *wavelet_scale, void *y, void *workspace,
                    size_t workspace_bytes, wtconv_stream_t stream);
 
-/* Gradient with respect to the input: dx = sum_l Synth_l(s_l * corr(Analysis_l(dy), flip(w_l)))
- * + s_b * corr(dy, flip(w_b)), the transpose of the forward's linear part (the bias drops out).
- * Reads dy, writes dx, both [B][C][H][W]. */
+/* Gradient with respect to the input (gist.science pt, Resumo Tecnico / Resultados: the timed
+ * training step is forward plus backward; Metodologia: the reformulation leaves the operator
+ * unchanged, so its transpose is the same three reformulations run in reverse roles):
+ * dx = sum_l Synth_l(s_l * corr(Analysis_l(dy), flip(w_l))) + s_b * corr(dy, flip(w_b)), the
+ * transpose of the forward's linear part (the bias drops out), computed by the forward's kernels
+ * on dy with every kernel rotated by 180 degrees.  Reads dy, writes dx, both [B][C][H][W]. */
 int wtconv_backward_input(int B, int C, int H, int W, int L, int k, int dtype,
                           const float *base_w, const float *base_bias, const float *base_scale,
                           const float *wavelet_w, const float *wavelet_scale, const void *dy,
@@ -182,8 +189,12 @@ int wtconv_backward_weights(int B, int C, int H, int W, int L, int k, int dtype,
                             float *d_base_scale, float *d_wavelet_w, float *d_wavelet_scale,
                             void *workspace, size_t workspace_bytes, wtconv_stream_t stream);
 
-/* Fused backward: dx and every parameter gradient in one pass that reads x and dy once.
- * Same results as wtconv_backward_input followed by wtconv_backward_weights. */
+/* Whole backward in one call (gist.science pt, Resumo Tecnico / Principais Contribuicoes: the
+ * reformulated layer is validated on the forward outputs and on all parameter gradients;
+ * Resultados: a training step is forward plus backward): dx and every parameter gradient.  It
+ * launches the input gradient's kernels and then the weight gradients' on `stream` (each reads
+ * dy), with one workspace for both.  Same results as wtconv_backward_input followed by
+ * wtconv_backward_weights. */
 int wtconv_backward(int B, int C, int H, int W, int L, int k, int dtype, const void *x,
                     const void *dy, const float *base_w, const float *base_bias,
                     const float *base_scale, const float *wavelet_w, const float *wavelet_scale,
