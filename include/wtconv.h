@@ -56,10 +56,16 @@
  *   - The weight gradients run the batch-pair kernel on small planes, else the fused
  *     whole-plane kernel (x and dy planes moved by bulk tensor copies, both pyramids on chip; fp32
  *     planes of at least 64 base items where both copies fit one box of at most 256 x 256), else a
- *     staged whole-plane kernel where both planes' pyramids fit in shared memory, else tiled
- *     kernels (tiles with bulk tensor copies, levels >= 2 on their pyramids in the workspace),
- *     else workspace pyramids for every level.  WTCONV_DW_PATH=pair, =fused, =plane, =tiles or
- *     =pyramid selects a path where it applies (same results within fp32 rounding).
+ *     staged whole-plane kernel where both planes' pyramids fit in shared memory, else the tiled
+ *     batch-pair kernel (tiles of x with halo and of dy by bulk tensor copies, two Haar levels per
+ *     launch, deeper levels from the level-2 low bands the previous launch writes), else older
+ *     tiled kernels (levels >= 2 on their pyramids in the workspace), else workspace pyramids for
+ *     every level.  WTCONV_DW_PATH=pair, =fused, =plane, =ptile, =tiles or =pyramid selects a path
+ *     where it applies (same results within fp32 rounding).
+ *   - Tuning restrictions for measurement runs (the plans they give are valid, only slower or
+ *     faster): WTCONV_PAIR_THREADS, WTCONV_PAIR_SHAPE and WTCONV_PAIR_SLOTS fix the batch-pair
+ *     kernels' CTA size, item shapes and pair slots per group; WTCONV_PTILE=TH,TW,G,threads[,narrow]
+ *     fixes the first tiled batch-pair launch's tile, pair slots, CTA size and item width.
  *   - Setting the environment variable WTCONV_INJECT_FAULT=1 makes every compute entry point
  *     return WTCONV_ERR_INJECTED before launching anything (host-side fault injection).
  */

@@ -880,6 +880,8 @@ PairPlan plan_pair_fwd_uncached(int B, int C, int H, int W, int L, int k, int dt
     // a shape with a specialised instantiation takes the CTA size and slots that measured fastest
     PairSpecPref pref{};
     const char *knob_t = getenv("WTCONV_PAIR_THREADS"), *knob_s = getenv("WTCONV_PAIR_SHAPE");
+    const char *knob_gs = getenv("WTCONV_PAIR_SLOTS");  // tuning: pair slots per group
+    const int knob_g = knob_gs && knob_gs[0] ? atoi(knob_gs) : 0;
     const bool tuned = pair_spec_measured(H, W, L, k, dtype, &pref) && !(knob_t && knob_t[0]) && !(knob_s && knob_s[0]);
     for (int si = 0; si < (int)(sizeof(kPairShapes) / sizeof(kPairShapes[0])); ++si) {
         const PairShape &sh = kPairShapes[si];
@@ -891,6 +893,7 @@ PairPlan plan_pair_fwd_uncached(int B, int C, int H, int W, int L, int k, int dt
             if (tuned && pref.threads && T != pref.threads) continue;
             for (int G = 1; G <= std::min(npairs, kPairMaxSlots); ++G) {
                 if (tuned && pref.slots && G != std::min(pref.slots, npairs)) continue;
+                if (knob_g > 0 && G != std::min(knob_g, npairs)) continue;
                 PairArgs a{};
                 a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
                 a.npairs = npairs;
@@ -1051,8 +1054,8 @@ PairPlan cached_pair_plan(int kind, int B, int C, int H, int W, int L, int k, in
         return p;
     }
     // the tuning restrictions are part of the key: a restricted plan is a different plan
-    const char *vt = getenv("WTCONV_PAIR_THREADS"), *vs = getenv("WTCONV_PAIR_SHAPE");
-    const int knobs = (vt && vt[0] ? atoi(vt) : 0) * 16 + (vs && vs[0] ? atoi(vs) + 1 : 0);
+    const char *vt = getenv("WTCONV_PAIR_THREADS"), *vs = getenv("WTCONV_PAIR_SHAPE"), *vg = getenv("WTCONV_PAIR_SLOTS");
+    const int knobs = ((vg && vg[0] ? atoi(vg) : 0) * 512 + (vt && vt[0] ? atoi(vt) : 0)) * 16 + (vs && vs[0] ? atoi(vs) + 1 : 0);
     const PlanKey key(kind + 1000 * knobs, B, C, H, W, L, k, dtype, dev);
     {
         std::lock_guard<std::mutex> lock(mu);

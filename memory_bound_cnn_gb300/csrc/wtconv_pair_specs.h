@@ -9,14 +9,14 @@
 // batch-pair forward / weight gradient beat the whole-plane kernels there (1) or not (0).
 //   64x64 L4 bf16: forward 293.5 vs 316 us (256 threads, 1 pair); weight gradient 424 vs 340 us
 //   32x32 L3 bf16: forward 144.0 vs 154 us (256 threads, 4 pairs); weight gradient 191 vs 176 us
-//   16x16 L2 bf16: forward 80.5 vs 84.6 us; weight gradient 106 vs 122 us
-//   8x8 L1 bf16: forward 51.8 vs 78.5 us; weight gradient 74 vs 134 us
+//   16x16 L2 bf16: forward 76.4 vs 84.6 us (64 threads, 4 pairs); weight gradient 106 vs 122 us
+//   8x8 L1 bf16: forward 49.8 vs 78.5 us (64 threads, 8 pairs); weight gradient 74 vs 134 us
 //   28x28 L2 bf16: forward 76.4 vs 74.4 us; weight gradient 84 vs 94 us
 //   56x56 L3 fp32: forward 154 vs 117 us; weight gradient 169 vs 156 us
 #define WTCONV_SPEC_b64l4 b64l4, 64, 64, 4, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 256, 1, 1, 0
 #define WTCONV_SPEC_b32l3 b32l3, 32, 32, 3, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 256, 4, 1, 0
-#define WTCONV_SPEC_b16l2 b16l2, 16, 16, 2, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 0, 0, 1, 1
-#define WTCONV_SPEC_b8l1 b8l1, 8, 8, 1, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 0, 0, 1, 1
+#define WTCONV_SPEC_b16l2 b16l2, 16, 16, 2, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 64, 4, 1, 1
+#define WTCONV_SPEC_b8l1 b8l1, 8, 8, 1, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 64, 8, 1, 1
 #define WTCONV_SPEC_b28l2 b28l2, 28, 28, 2, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 0, 0, 0, 1
 #define WTCONV_SPEC_f56l3 f56l3, 56, 56, 3, 5, float, 0, 2, 8, 2, 8, 2, 8, 0, 0, 0, 0
 
