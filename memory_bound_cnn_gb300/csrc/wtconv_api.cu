@@ -13,6 +13,7 @@
 #include <mutex>
 #include <string>
 #include <tuple>
+#include <vector>
 
 #include "wtconv.h"
 #include "wtconv_internal.h"
@@ -883,11 +884,16 @@ PairPlan plan_pair_fwd_uncached(int B, int C, int H, int W, int L, int k, int dt
     const char *knob_gs = getenv("WTCONV_PAIR_SLOTS");  // tuning: pair slots per group
     const int knob_g = knob_gs && knob_gs[0] ? atoi(knob_gs) : 0;
     const bool tuned = pair_spec_measured(H, W, L, k, dtype, &pref) && !(knob_t && knob_t[0]) && !(knob_s && knob_s[0]);
-    for (int si = 0; si < (int)(sizeof(kPairShapes) / sizeof(kPairShapes[0])); ++si) {
-        const PairShape &sh = kPairShapes[si];
-        if (!pair_shape_allowed(si)) continue;
-        const int shp0[6] = {sh.q0, sh.s0, sh.ql, sh.sl, sh.qd, sh.sd};
-        if (tuned && !std::equal(shp0, shp0 + 6, pref.shape)) continue;
+    // candidate item shapes: the instantiation's own (which may lie outside the run-time menu)
+    // for a tuned shape, else the menu
+    std::vector<PairShape> shapes;
+    if (tuned) {
+        shapes.push_back({pref.shape[0], pref.shape[1], pref.shape[2], pref.shape[3], pref.shape[4], pref.shape[5], 1.0});
+    } else {
+        for (int si = 0; si < (int)(sizeof(kPairShapes) / sizeof(kPairShapes[0])); ++si)
+            if (pair_shape_allowed(si)) shapes.push_back(kPairShapes[si]);
+    }
+    for (const PairShape &sh : shapes) {
         for (int T : {64, 128, 256}) {
             if (!pair_threads_allowed(T)) continue;
             if (tuned && pref.threads && T != pref.threads) continue;
@@ -906,6 +912,7 @@ PairPlan plan_pair_fwd_uncached(int B, int C, int H, int W, int L, int k, int dt
                 a.vec_st = (W % 4) == 0;
                 const int shp[6] = {sh.q0, sh.s0, sh.ql, sh.sl, sh.qd, sh.sd};
                 a.spec = pair_spec_index(H, W, L, k, dtype, shp);
+                if (a.spec < 0 && tuned) break;  // only the instantiation runs its own shapes
                 pair_counts(a);
                 const size_t smem = pair_fwd_smem_bytes(a, eb);
                 if (smem + kStaticSmemMargin > (size_t)kMaxSmem) break;
@@ -949,12 +956,23 @@ PairPlan plan_pair_dw_uncached(int B, int C, int H, int W, int L, int k, int dty
     if (sms <= 0) { best.status = WTCONV_ERR_CUDA; return best; }
     const int npairs = (B + 1) / 2;
     const int KK = k * k, nsig = 1 + 4 * L;
-    for (int si = 0; si < (int)(sizeof(kPairShapes) / sizeof(kPairShapes[0])); ++si) {
-        const PairShape &sh = kPairShapes[si];
+    const char *knob_gs = getenv("WTCONV_PAIR_SLOTS");  // tuning: pair slots per group
+    const int knob_g = knob_gs && knob_gs[0] ? atoi(knob_gs) : 0;
+    // the menu, plus 7-row items (exact on planes of 7 * 2^l rows; correlation items only); a
+    // shape with a measured preference keeps to it unless a tuning restriction is set
+    constexpr int kMenu = (int)(sizeof(kPairShapes) / sizeof(kPairShapes[0]));
+    PairSpecPref pref{};
+    const char *knob_t = getenv("WTCONV_PAIR_THREADS"), *knob_s = getenv("WTCONV_PAIR_SHAPE");
+    const bool tuned = pair_spec_measured(H, W, L, k, dtype, &pref) && !(knob_t && knob_t[0]) && !(knob_s && knob_s[0]);
+    for (int si = 0; si <= kMenu; ++si) {
+        const PairShape sh = si < kMenu ? kPairShapes[si] : PairShape{2, 7, 2, 7, 2, 7, 1.10};
         if (!pair_shape_allowed(si)) continue;
+        if (tuned && pref.dw_shape >= 0 && si != pref.dw_shape) continue;
         for (int T : {64, 128, 256}) {
             if (!pair_threads_allowed(T)) continue;
+            if (tuned && pref.dw_threads && T != pref.dw_threads) continue;
             for (int G = 1; G <= std::min(npairs, kPairMaxSlots); ++G) {
+                if (knob_g > 0 && G != std::min(knob_g, npairs)) continue;
                 PairArgs a{};
                 a.B = B; a.C = C; a.H = H; a.W = W; a.L = L; a.K = k;
                 a.npairs = npairs;

@@ -129,11 +129,12 @@ int pair_spec_index(int H, int W, int L, int K, int dtype, const int (&shape)[6]
 int occupancy_pair_fwd_spec(int spec, size_t smem, int nthreads);
 
 // What measured fastest on GB300 for a layer shape that has a specialised instantiation: its item
-// shapes, the forward's CTA size and pair slots per group (0: the planner's choice), and whether
-// the batch-pair forward / weight gradient is the default for the shape.
+// shapes, the forward's CTA size and pair slots per group (0: the planner's choice), whether
+// the batch-pair forward / weight gradient is the default for the shape, and the weight
+// gradient's CTA size (0: planner) and item-shape index (-1: planner).
 struct PairSpecPref {
     int shape[6];
-    int threads, slots, fwd_default, dw_default;
+    int threads, slots, fwd_default, dw_default, dw_threads, dw_shape;
 };
 bool pair_spec_measured(int H, int W, int L, int K, int dtype, PairSpecPref *pref);
 

@@ -48,6 +48,7 @@ __device__ __forceinline__ void corr_item_dispatch(int q, int s, const f2_t *y, 
         else pair_corr_strip<K, 4, 4>(y, ypitch, g, gpitch, acc);
     } else {
         if (s == 8) pair_corr_strip<K, 2, 8>(y, ypitch, g, gpitch, acc);
+        else if (s == 7) pair_corr_strip<K, 2, 7>(y, ypitch, g, gpitch, acc);  // planes of 7 * 2^l rows
         else pair_corr_strip<K, 2, 4>(y, ypitch, g, gpitch, acc);
     }
 }

@@ -369,8 +369,23 @@ __device__ __forceinline__ void pass1(const PairArgs &a, const PairGeo &g, f2_t 
 // The forward kernel's body, for a geometry `g` that is either the plan's (runtime values) or,
 // with FIX, a compile-time constant of a specialised instantiation: then every pitch and offset is
 // an immediate, the level loops unroll and index decodes divide by constants.
-template <int K, typename T, bool FIX>
+// Conv items of levels LV .. L of an instantiation with a compile-time geometry: each level's
+// item shape is a constant (rows drop to 4 on images of at most 4 rows), so shapes outside the
+// run-time menu (e.g. 7-row items on 28 x 28 planes) work as well.
+template <int K, class Spec, int LV>
+__device__ __forceinline__ void conv_levels_fixed(const PairArgs &a, const PairGeo &g, f2_t *slots, const f2_t *wts,
+                                                  int np, int first) {
+    if constexpr (LV <= Spec::kL) {
+        constexpr int Q = LV == 1 ? Spec::kQL : Spec::kQD;
+        constexpr int S = (Spec::kH >> LV) <= 4 ? 4 : (LV == 1 ? Spec::kSL : Spec::kSD);
+        conv_level<K, Q, S, true>(a, g, slots, wts, np, LV, np * first);
+        conv_levels_fixed<K, Spec, LV + 1>(a, g, slots, wts, np, first + 4 * g.ns[LV] * g.ng[LV]);
+    }
+}
+
+template <int K, typename T, class Spec>
 __device__ __forceinline__ void pair_fwd_body(const PairArgs &a, const PairGeo &g) {
+    constexpr bool FIX = Spec::fixed;
     extern __shared__ __align__(128) unsigned char pair_smem[];
     __shared__ __align__(8) uint64_t bar;
     __shared__ int copy_ok;
@@ -452,7 +467,9 @@ __device__ __forceinline__ void pair_fwd_body(const PairArgs &a, const PairGeo &
             __syncthreads();
         }
         // ---- conv items of every subband image of every level
-        {
+        if constexpr (FIX) {
+            conv_levels_fixed<K, Spec, 1>(a, g, slots, wts, np, 0);
+        } else {
             int first = 0;  // conv items of the levels before l, per slot
 #pragma unroll(FIX ? kMaxLevels : 1)
             for (int l = 1; l <= L; ++l) {
@@ -509,7 +526,10 @@ __device__ __forceinline__ void pair_fwd_body(const PairArgs &a, const PairGeo &
         // ---- output items: base conv + level-1 synthesis, one store per pixel
         const f2_t bias2 = pk2(bias, bias);
         const int Q0 = g.Q[0], S0 = g.S[0];
-        if (Q0 == 4) {
+        if constexpr (FIX) {
+            constexpr int kS0 = Spec::kH <= 4 ? 4 : Spec::kS0;
+            out_phase<K, Spec::kQ0, kS0, T, true>(a, g, slots, wts, np, p0, c, bias2, out);
+        } else if (Q0 == 4) {
             if (S0 == 8) out_phase<K, 4, 8, T, FIX>(a, g, slots, wts, np, p0, c, bias2, out);
             else out_phase<K, 4, 4, T, FIX>(a, g, slots, wts, np, p0, c, bias2, out);
         } else {
@@ -531,6 +551,8 @@ struct PairDynSpec {
 template <int H_, int W_, int L_, int Q0, int S0, int QL, int SL, int QD, int SD>
 struct PairShapeSpec {
     static constexpr bool fixed = true;
+    static constexpr int kH = H_, kW = W_, kL = L_;
+    static constexpr int kQ0 = Q0, kS0 = S0, kQL = QL, kSL = SL, kQD = QD, kSD = SD;
     template <int K, int KIND>
     static __device__ __forceinline__ const PairGeo &geo() {
         return kPairSpecGeo<K, H_, W_, L_, Q0, S0, QL, SL, QD, SD, KIND>;
@@ -541,9 +563,9 @@ template <int K, typename T, int NT, class Spec>
 __global__ void __launch_bounds__(NT, NT == 64 ? (K <= 5 ? 6 : 4) : NT == 128 ? (K <= 3 ? 4 : (K == 5 ? 3 : 2)) : 1)
     wtconv_pair_fwd_kernel(const __grid_constant__ PairArgs a) {
     if constexpr (Spec::fixed) {
-        pair_fwd_body<K, T, true>(a, Spec::template geo<K, 0>());
+        pair_fwd_body<K, T, Spec>(a, Spec::template geo<K, 0>());
     } else {
-        pair_fwd_body<K, T, false>(a, a.geo);
+        pair_fwd_body<K, T, Spec>(a, a.geo);
     }
 }
 

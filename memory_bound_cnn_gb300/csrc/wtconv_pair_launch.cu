@@ -14,13 +14,13 @@ namespace {
 
 struct PairSpecEntry {
     int H, W, L, K, dtype, shape[6];
-    int fwd_threads, fwd_slots, fwd_default, dw_default;
+    int fwd_threads, fwd_slots, fwd_default, dw_default, dw_threads, dw_shape;
     cudaError_t (*launch_fwd)(const PairArgs &, size_t, cudaStream_t);
     int (*occ_fwd)(size_t, int);
 };
 
-#define WTCONV_ENTRY(name, H, W, L, K, T, dt, q0, s0, ql, sl, qd, sd, nt, g, fd, dd)                  \
-    {H, W, L, K, dt, {q0, s0, ql, sl, qd, sd}, nt, g, fd, dd, launch_pair_fwd_spec_##name,           \
+#define WTCONV_ENTRY(name, H, W, L, K, T, dt, q0, s0, ql, sl, qd, sd, nt, g, fd, dd, dnt, dsh)        \
+    {H, W, L, K, dt, {q0, s0, ql, sl, qd, sd}, nt, g, fd, dd, dnt, dsh, launch_pair_fwd_spec_##name, \
      occupancy_pair_fwd_spec_##name},
 #define WTCONV_ENTRY_ONE(spec) WTCONV_CALL(WTCONV_ENTRY, spec)
 const PairSpecEntry kSpecs[] = {WTCONV_PAIR_SPEC_LIST(WTCONV_ENTRY_ONE)};
@@ -49,6 +49,8 @@ bool pair_spec_measured(int H, int W, int L, int K, int dtype, PairSpecPref *pre
             pref->slots = e.fwd_slots;
             pref->fwd_default = e.fwd_default;
             pref->dw_default = e.dw_default;
+            pref->dw_threads = e.dw_threads;
+            pref->dw_shape = e.dw_shape;
             return true;
         }
     }

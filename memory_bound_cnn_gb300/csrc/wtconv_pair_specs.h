@@ -5,20 +5,25 @@
 //
 // Each spec: name, H, W, L, K, activation type, dtype code, q0, s0, ql, sl, qd, sd (item shapes as
 // in make_pair_geo), then what measured fastest on GB300 for the layer (B = 128 or 64, k = 5):
-// the forward's CTA size and pair slots per group (0: the planner's choice), and whether the
-// batch-pair forward / weight gradient beat the whole-plane kernels there (1) or not (0).
+// the forward's CTA size and pair slots per group (0: the planner's choice), whether the
+// batch-pair forward / weight gradient beat the whole-plane kernels there (1) or not (0), and the
+// weight gradient's CTA size and item-shape index (planner menu; 6: 7-row items; -1: the
+// planner's choice).
 //   64x64 L4 bf16: forward 293.5 vs 316 us (256 threads, 1 pair); weight gradient 424 vs 340 us
 //   32x32 L3 bf16: forward 144.0 vs 154 us (256 threads, 4 pairs); weight gradient 191 vs 176 us
 //   16x16 L2 bf16: forward 76.4 vs 84.6 us (64 threads, 4 pairs); weight gradient 106 vs 122 us
 //   8x8 L1 bf16: forward 49.8 vs 78.5 us (64 threads, 8 pairs); weight gradient 74 vs 134 us
-//   28x28 L2 bf16: forward 76.4 vs 74.4 us; weight gradient 84 vs 94 us
-//   56x56 L3 fp32: forward 154 vs 117 us; weight gradient 169 vs 156 us
-#define WTCONV_SPEC_b64l4 b64l4, 64, 64, 4, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 256, 1, 1, 0
-#define WTCONV_SPEC_b32l3 b32l3, 32, 32, 3, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 256, 4, 1, 0
-#define WTCONV_SPEC_b16l2 b16l2, 16, 16, 2, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 64, 4, 1, 1
-#define WTCONV_SPEC_b8l1 b8l1, 8, 8, 1, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 64, 8, 1, 1
-#define WTCONV_SPEC_b28l2 b28l2, 28, 28, 2, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 0, 0, 0, 1
-#define WTCONV_SPEC_f56l3 f56l3, 56, 56, 3, 5, float, 0, 2, 8, 2, 8, 2, 8, 0, 0, 0, 0
+//   28x28 L2 bf16 (14-row output items, 7-row conv items: no rows past the plane): forward
+//   60.1 vs 74.4 us (76.4 with 8-row items); weight gradient 80.5 us with 7-row items (64
+//   threads) vs 85.7 with the planner's 8-row items and 94 on the whole-plane kernel
+//   56x56 L3 fp32: forward 131 with 7-row items at levels >= 1 (154 with 8-row) vs 119 us on the
+//   fused whole-plane kernel; weight gradient 169 vs 156 us
+#define WTCONV_SPEC_b64l4 b64l4, 64, 64, 4, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 256, 1, 1, 0, 0, -1
+#define WTCONV_SPEC_b32l3 b32l3, 32, 32, 3, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 256, 4, 1, 0, 0, -1
+#define WTCONV_SPEC_b16l2 b16l2, 16, 16, 2, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 64, 4, 1, 1, 0, -1
+#define WTCONV_SPEC_b8l1 b8l1, 8, 8, 1, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 64, 8, 1, 1, 0, -1
+#define WTCONV_SPEC_b28l2 b28l2, 28, 28, 2, 5, __nv_bfloat16, 1, 2, 14, 2, 7, 2, 7, 0, 0, 1, 1, 64, 6
+#define WTCONV_SPEC_f56l3 f56l3, 56, 56, 3, 5, float, 0, 2, 8, 2, 7, 2, 7, 0, 0, 0, 0, 0, -1
 
 #define WTCONV_PAIR_SPEC_LIST(X)                                                                    \
     X(WTCONV_SPEC_b64l4) X(WTCONV_SPEC_b32l3) X(WTCONV_SPEC_b16l2) X(WTCONV_SPEC_b8l1)             \
@@ -28,11 +33,11 @@
 #define WTCONV_CALL(M, ...) M(__VA_ARGS__)
 
 // The functions one specialised translation unit defines.
-#define WTCONV_PAIR_SPEC_DECL(name, H, W, L, K, T, dt, q0, s0, ql, sl, qd, sd, nt, g, fd, dd)                      \
+#define WTCONV_PAIR_SPEC_DECL(name, H, W, L, K, T, dt, q0, s0, ql, sl, qd, sd, nt, g, fd, dd, dnt, dsh)                      \
     cudaError_t launch_pair_fwd_spec_##name(const PairArgs &a, size_t smem, cudaStream_t st);       \
     int occupancy_pair_fwd_spec_##name(size_t smem, int nthreads);
 
-#define WTCONV_PAIR_SPEC_DEF(name, H, W, L, K, T, dt, q0, s0, ql, sl, qd, sd, nt, g, fd, dd)                       \
+#define WTCONV_PAIR_SPEC_DEF(name, H, W, L, K, T, dt, q0, s0, ql, sl, qd, sd, nt, g, fd, dd, dnt, dsh)                       \
     cudaError_t launch_pair_fwd_spec_##name(const PairArgs &a, size_t smem, cudaStream_t st) {      \
         return launch_pair_fwd_t<K, T, PairShapeSpec<H, W, L, q0, s0, ql, sl, qd, sd>>(a, smem, st); \
     }                                                                                               \
