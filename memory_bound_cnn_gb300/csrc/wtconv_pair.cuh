@@ -184,13 +184,23 @@ __device__ __forceinline__ void stage_pair_weights(const PairArgs &a, int c, f2_
 // origin 16-byte aligned), `out` at the compact output (pitch even).  The window slides down one
 // input row at a time; each loaded row feeds the (up to K) output rows whose window contains it,
 // so only about K x Q accumulators are live at once.
-template <int K, int Q, int S>
+//
+// SKIP: the first zt and the last zb window rows are known to be zero padding (small planes,
+// where they are a large share of the window): those rows are neither loaded nor multiplied.
+template <int K, int Q, int S, bool SKIP = false>
 __device__ __forceinline__ void pair_conv_strip(const f2_t *__restrict__ in, int pitch, const f2_t (&w)[K * K],
-                                                f2_t *__restrict__ out, int opitch) {
+                                                f2_t *__restrict__ out, int opitch, int zt = 0, int zb = 0) {
     constexpr int NW = Q + K - 1, NL = (NW + 1) / 2;
     f2_t acc[S][Q];
+    if constexpr (SKIP) {
+#pragma unroll
+        for (int j = 0; j < S; ++j)
+#pragma unroll
+            for (int q = 0; q < Q; ++q) acc[j][q] = 0ull;
+    }
 #pragma unroll
     for (int i = 0; i < S + K - 1; ++i) {
+        if (!SKIP || (i >= zt && i < S + K - 1 - zb)) {
         f2_t x[2 * NL];
         const ulonglong2 *p = reinterpret_cast<const ulonglong2 *>(in + i * pitch);
 #pragma unroll
@@ -207,11 +217,12 @@ __device__ __forceinline__ void pair_conv_strip(const f2_t *__restrict__ in, int
                 if (j >= 0 && j < S) {
 #pragma unroll
                     for (int q = 0; q < Q; ++q) {
-                        if (u == 0 && v == 0) acc[j][q] = fmul2(w[0], x[q]);
+                        if (!SKIP && u == 0 && v == 0) acc[j][q] = fmul2(w[0], x[q]);
                         else ffma2_acc(acc[j][q], w[u * K + v], x[q + v]);
                     }
                 }
             }
+        }
         const int jd = i - (K - 1);
         if (jd >= 0) {
             ulonglong2 *o = reinterpret_cast<ulonglong2 *>(out + jd * opitch);
@@ -229,9 +240,11 @@ __device__ __forceinline__ void pair_conv_strip(const f2_t *__restrict__ in, int
 // Correlation strip of the weight gradient: acc[u*K+v] += sum_{j<S, q<Q} g[j][q] * y[j + u][q + v]
 // (elementwise on the pair: the two halves are partial sums over the two planes).  `y` points at
 // the window origin of the padded image, `g` at the matching interior origin of the compact image.
+// The first zt and the last zb window rows of y may be declared zero padding (rows outside the
+// plane): they are neither loaded nor multiplied, which leaves the sums exact.
 template <int K, int Q, int S>
 __device__ __forceinline__ void pair_corr_strip(const f2_t *__restrict__ y, int ypitch, const f2_t *__restrict__ g,
-                                                int gpitch, f2_t (&acc)[K * K]) {
+                                                int gpitch, f2_t (&acc)[K * K], int zt = 0, int zb = 0) {
     constexpr int NW = Q + K - 1, NL = (NW + 1) / 2;
     f2_t gr[S][Q];
 #pragma unroll
@@ -245,6 +258,7 @@ __device__ __forceinline__ void pair_corr_strip(const f2_t *__restrict__ y, int 
                 gr[r][2 * t + 1] = v.y;
             }
         }
+        if (r < zt || r >= S + K - 1 - zb) continue;
         f2_t x[2 * NL];
         const ulonglong2 *p = reinterpret_cast<const ulonglong2 *>(y + r * ypitch);
 #pragma unroll

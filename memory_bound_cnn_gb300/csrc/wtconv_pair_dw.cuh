@@ -42,14 +42,14 @@ __host__ __device__ inline PairDwLayout pair_dw_layout(const PairArgs &a) {
 
 template <int K>
 __device__ __forceinline__ void corr_item_dispatch(int q, int s, const f2_t *y, int ypitch, const f2_t *g, int gpitch,
-                                                   f2_t (&acc)[K * K]) {
+                                                   f2_t (&acc)[K * K], int zt, int zb) {
     if (q == 4) {
-        if (s == 8) pair_corr_strip<K, 4, 8>(y, ypitch, g, gpitch, acc);
-        else pair_corr_strip<K, 4, 4>(y, ypitch, g, gpitch, acc);
+        if (s == 8) pair_corr_strip<K, 4, 8>(y, ypitch, g, gpitch, acc, zt, zb);
+        else pair_corr_strip<K, 4, 4>(y, ypitch, g, gpitch, acc, zt, zb);
     } else {
-        if (s == 8) pair_corr_strip<K, 2, 8>(y, ypitch, g, gpitch, acc);
-        else if (s == 7) pair_corr_strip<K, 2, 7>(y, ypitch, g, gpitch, acc);  // planes of 7 * 2^l rows
-        else pair_corr_strip<K, 2, 4>(y, ypitch, g, gpitch, acc);
+        if (s == 8) pair_corr_strip<K, 2, 8>(y, ypitch, g, gpitch, acc, zt, zb);
+        else if (s == 7) pair_corr_strip<K, 2, 7>(y, ypitch, g, gpitch, acc, zt, zb);  // planes of 7 * 2^l rows
+        else pair_corr_strip<K, 2, 4>(y, ypitch, g, gpitch, acc, zt, zb);
     }
 }
 
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(NT, NT == 64 ? (K <= 5 ? 6 : 4) : NT == 128 ? 
     const int nthr = sig < 0 ? 1 : a.sig_start[sig + 1] - a.sig_start[sig];
     const int per_pair = g.ns[lvl] * g.ng[lvl];
     const int ipitch = g.ipitch[lvl], zpitch = g.zpitch[lvl];
-    const int Ql = g.Q[lvl], Sl = g.S[lvl];
+    const int Ql = g.Q[lvl], Sl = g.S[lvl], hl = g.h[lvl];
     const int yoff = lvl == 0 ? g.off_x : g.off_y[lvl] + sub * g.iimg[lvl];
     const int goff = lvl == 0 ? g.off_dy : g.off_z[lvl] + sub * g.zimg[lvl];
     const FastDiv dv_pp = a.dv_lvl[lvl], dv_ns = a.dv_lvl_ns[lvl];
@@ -331,7 +331,9 @@ __global__ void __launch_bounds__(NT, NT == 64 ? (K <= 5 ? 6 : 4) : NT == 128 ? 
                     const f2_t *slot = slots + (size_t)gs * g.slot;
                     const f2_t *yw = slot + yoff + seg * Sl * ipitch + strip * Ql;
                     const f2_t *gw = slot + goff + seg * Sl * zpitch + strip * Ql;
-                    corr_item_dispatch<K>(Ql, Sl, yw, ipitch, gw, zpitch, acc);
+                    // window rows of y outside the plane: zero padding, skipped
+                    const int zt = max(0, P - seg * Sl), zb = max(0, (seg + 1) * Sl + P - hl);
+                    corr_item_dispatch<K>(Ql, Sl, yw, ipitch, gw, zpitch, acc, zt, zb);
                 }
             }
             __syncthreads();

@@ -93,15 +93,23 @@ __device__ __forceinline__ void store_row(const f2_t (&acc)[Q], T *d0, T *d1, in
 // soon as its window is complete: an even row 2m adds the level-1 inverse butterflies of row m of
 // Z^1 (LL already holding the deeper levels) for a = 0 and keeps those for a = 1 until row 2m+1:
 // pixel (a, b) of position (m, p) gains LL + (-1)^b LH + (-1)^a HL + (-1)^(a+b) HH.
-template <int K, int Q, int S, typename T>
+// SKIP: as in pair_conv_strip, the first zt and last zb window rows are zero padding.
+template <int K, int Q, int S, typename T, bool SKIP = false>
 __device__ __forceinline__ void pair_out_item(const f2_t *__restrict__ in, int pitch, const f2_t (&w)[K * K],
                                               f2_t bias2, const f2_t *__restrict__ z1, int zpitch, int zimg, T *d0,
-                                              T *d1, int W, int nrows, int ncols, bool vec) {
+                                              T *d1, int W, int nrows, int ncols, bool vec, int zt = 0, int zb = 0) {
     constexpr int NW = Q + K - 1, NL = (NW + 1) / 2, QL = Q / 2;
     f2_t acc[S][Q];
     f2_t pend[Q];  // the odd row's synthesis terms
+    if constexpr (SKIP) {
+#pragma unroll
+        for (int j = 0; j < S; ++j)
+#pragma unroll
+            for (int q = 0; q < Q; ++q) acc[j][q] = bias2;
+    }
 #pragma unroll
     for (int i = 0; i < S + K - 1; ++i) {
+        if (!SKIP || (i >= zt && i < S + K - 1 - zb)) {
         f2_t x[2 * NL];
         const ulonglong2 *p = reinterpret_cast<const ulonglong2 *>(in + i * pitch);
 #pragma unroll
@@ -118,11 +126,12 @@ __device__ __forceinline__ void pair_out_item(const f2_t *__restrict__ in, int p
                 if (j >= 0 && j < S) {
 #pragma unroll
                     for (int q = 0; q < Q; ++q) {
-                        if (u == 0 && v == 0) acc[j][q] = ffma2(w[0], x[q], bias2);
+                        if (!SKIP && u == 0 && v == 0) acc[j][q] = ffma2(w[0], x[q], bias2);
                         else ffma2_acc(acc[j][q], w[u * K + v], x[q + v]);
                     }
                 }
             }
+        }
         const int jd = i - (K - 1);
         if (jd < 0) continue;
         if ((jd & 1) == 0) {
@@ -166,7 +175,7 @@ __device__ __forceinline__ int divq(int n, int d, const FastDiv &f) {
 // Conv items of level l of every slot (every subband image), in the order of a flat item list
 // whose first `base` entries went to the threads before: thread tid takes items e with
 // (base + e) % nt == tid.  The level's geometry sits in registers for the whole loop.
-template <int K, int Q, int S, bool FIX>
+template <int K, int Q, int S, bool FIX, bool SKIP = false>
 __device__ __forceinline__ void conv_level(const PairArgs &a, const PairGeo &g, f2_t *slots, const f2_t *wts, int np,
                                            int l, int base) {
     constexpr int WP = wpairs(K), KK = K * K;
@@ -185,8 +194,10 @@ __device__ __forceinline__ void conv_level(const PairArgs &a, const PairGeo &g, 
         f2_t w[KK];
         load_weights<K>(wts + (1 + 4 * (l - 1) + s) * WP, w);
         f2_t *sl = slots + (size_t)gs * slot;
-        pair_conv_strip<K, Q, S>(sl + oy + s * ii + seg * S * ip + strip * Q, ip, w,
-                                 sl + oz + s * zi + seg * S * zp + strip * Q, zp);
+        // window rows above the plane / at or below its last row (SKIP only)
+        const int zt = max(0, K / 2 - seg * S), zb = max(0, (seg + 1) * S + K / 2 - g.h[l]);
+        pair_conv_strip<K, Q, S, SKIP>(sl + oy + s * ii + seg * S * ip + strip * Q, ip, w,
+                                       sl + oz + s * zi + seg * S * zp + strip * Q, zp, zt, zb);
     }
 }
 
@@ -245,7 +256,7 @@ __device__ __forceinline__ void analysis_deep_pass(const PairGeo &g, f2_t *slots
 }
 
 // Output items of every slot with item shape Q x S (the base kernel in registers for the loop).
-template <int K, int Q, int S, typename T, bool FIX>
+template <int K, int Q, int S, typename T, bool FIX, bool SKIP = false>
 __device__ __forceinline__ void out_phase(const PairArgs &a, const PairGeo &g, const f2_t *slots, const f2_t *wts,
                                           int np, int p0, int c, f2_t bias2, T *out) {
     constexpr int KK = K * K;
@@ -264,8 +275,9 @@ __device__ __forceinline__ void out_phase(const PairArgs &a, const PairGeo &g, c
         const int b0 = 2 * (p0 + gs);
         T *d0 = out + ((size_t)b0 * C + c) * HW + (size_t)r0 * W + c0;
         T *d1 = b0 + 1 < B ? d0 + (size_t)C * HW : nullptr;
-        pair_out_item<K, Q, S, T>(sl + ox + r0 * ip0 + c0, ip0, w, bias2, sl + oz1 + (r0 >> 1) * zp1 + (c0 >> 1), zp1,
-                                  zi1, d0, d1, W, min(S, H - r0), min(Q, W - c0), vec);
+        const int zt = max(0, K / 2 - r0), zb = max(0, r0 + S + K / 2 - H);
+        pair_out_item<K, Q, S, T, SKIP>(sl + ox + r0 * ip0 + c0, ip0, w, bias2, sl + oz1 + (r0 >> 1) * zp1 + (c0 >> 1),
+                                        zp1, zi1, d0, d1, W, min(S, H - r0), min(Q, W - c0), vec, zt, zb);
     }
 }
 
@@ -378,7 +390,7 @@ __device__ __forceinline__ void conv_levels_fixed(const PairArgs &a, const PairG
     if constexpr (LV <= Spec::kL) {
         constexpr int Q = LV == 1 ? Spec::kQL : Spec::kQD;
         constexpr int S = (Spec::kH >> LV) <= 4 ? 4 : (LV == 1 ? Spec::kSL : Spec::kSD);
-        conv_level<K, Q, S, true>(a, g, slots, wts, np, LV, np * first);
+        conv_level<K, Q, S, true, Spec::kSkip>(a, g, slots, wts, np, LV, np * first);
         conv_levels_fixed<K, Spec, LV + 1>(a, g, slots, wts, np, first + 4 * g.ns[LV] * g.ng[LV]);
     }
 }
@@ -528,7 +540,7 @@ __device__ __forceinline__ void pair_fwd_body(const PairArgs &a, const PairGeo &
         const int Q0 = g.Q[0], S0 = g.S[0];
         if constexpr (FIX) {
             constexpr int kS0 = Spec::kH <= 4 ? 4 : Spec::kS0;
-            out_phase<K, Spec::kQ0, kS0, T, true>(a, g, slots, wts, np, p0, c, bias2, out);
+            out_phase<K, Spec::kQ0, kS0, T, true, Spec::kSkip>(a, g, slots, wts, np, p0, c, bias2, out);
         } else if (Q0 == 4) {
             if (S0 == 8) out_phase<K, 4, 8, T, FIX>(a, g, slots, wts, np, p0, c, bias2, out);
             else out_phase<K, 4, 4, T, FIX>(a, g, slots, wts, np, p0, c, bias2, out);
@@ -553,6 +565,9 @@ struct PairShapeSpec {
     static constexpr bool fixed = true;
     static constexpr int kH = H_, kW = W_, kL = L_;
     static constexpr int kQ0 = Q0, kS0 = S0, kQL = QL, kSL = SL, kQD = QD, kSD = SD;
+    // planes of at most 16 x 16: the zero-padding rows of each window are a large share of it
+    // (8 x 8, k = 5: 4 of 12 rows), so the items skip them
+    static constexpr bool kSkip = H_ <= 16 && W_ <= 16;
     template <int K, int KIND>
     static __device__ __forceinline__ const PairGeo &geo() {
         return kPairSpecGeo<K, H_, W_, L_, Q0, S0, QL, SL, QD, SD, KIND>;
