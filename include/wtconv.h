@@ -65,7 +65,9 @@
  *   - Tuning restrictions for measurement runs (the plans they give are valid, only slower or
  *     faster): WTCONV_PAIR_THREADS, WTCONV_PAIR_SHAPE and WTCONV_PAIR_SLOTS fix the batch-pair
  *     kernels' CTA size, item shapes and pair slots per group; WTCONV_PTILE=TH,TW,G,threads[,narrow]
- *     fixes the first tiled batch-pair launch's tile, pair slots, CTA size and item width.
+ *     fixes the first tiled batch-pair launch's tile, pair slots, CTA size and item width;
+ *     WTCONV_STAGED=G,threads fixes the planes per slot group and CTA size of the whole-plane and
+ *     deep kernels.
  *   - Setting the environment variable WTCONV_INJECT_FAULT=1 makes every compute entry point
  *     return WTCONV_ERR_INJECTED before launching anything (host-side fault injection).
  */

@@ -166,6 +166,10 @@ bool choose_launch(LayerArgs &a, int dtype, SmemFn smem_fn, BalFn bal_fn, OccFn 
     const int eb = elem_bytes(dtype);
     const bool can_stage = a.stage != 0;
     const char *force = getenv("WTCONV_STAGE");
+    // tuning restriction: WTCONV_STAGED=G,threads fixes the planes per slot group and CTA size
+    int kg = 0, kt = 0;
+    const char *kn = getenv("WTCONV_STAGED");
+    if (kn && kn[0]) sscanf(kn, "%d,%d", &kg, &kt);
     double best = -1.0;
     int bestG = 0, bestT = 0, bestS = 0;
     for (int stage : {1, 0}) {
@@ -173,7 +177,9 @@ bool choose_launch(LayerArgs &a, int dtype, SmemFn smem_fn, BalFn bal_fn, OccFn 
         if (force && force[0] == '0' && stage) continue;
         if (force && force[0] == '1' && !stage && can_stage) continue;
         for (int T : {256, 128}) {
+            if (kt && T != kt) continue;
             for (int G = 1; G <= a.B && G <= 64; ++G) {
+                if (kg && G != kg) continue;
                 const size_t smem = smem_fn(a.geo, G, a.L, a.K, eb, stage != 0, nullptr);
                 if (smem + kStaticSmemMargin > (size_t)kMaxSmem) break;
                 const int occ = occ_fn(dtype, a.K, T, smem);
@@ -383,7 +389,12 @@ Plan cached_plan(int kind, int B, int C, int H, int W, int L, int k, int dtype) 
         p.status = WTCONV_ERR_CUDA;
         return p;
     }
-    const PlanKey key(kind, B, C, H, W, L, k, dtype, dev);
+    // the tuning restrictions are part of the key
+    int kg = 0, kt = 0;
+    const char *kn = getenv("WTCONV_STAGED"), *ks = getenv("WTCONV_STAGE");
+    if (kn && kn[0]) sscanf(kn, "%d,%d", &kg, &kt);
+    const int knobs = (kg * 512 + kt) * 4 + (ks && ks[0] ? (ks[0] == '1' ? 1 : 2) : 0);
+    const PlanKey key(kind + 16 * knobs, B, C, H, W, L, k, dtype, dev);
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = cache.find(key);

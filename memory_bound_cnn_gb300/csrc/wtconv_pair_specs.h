@@ -9,8 +9,10 @@
 // batch-pair forward / weight gradient beat the whole-plane kernels there (1) or not (0), and the
 // weight gradient's CTA size and item-shape index (planner menu; 6: 7-row items; -1: the
 // planner's choice).
-//   64x64 L4 bf16: forward 293.5 vs 316 us (256 threads, 1 pair); weight gradient 424 vs 340 us
-//   32x32 L3 bf16: forward 144.0 vs 154 us (256 threads, 4 pairs); weight gradient 191 vs 176 us
+//   64x64 L4 bf16: forward 252 vs 316 us (256 threads, 1 pair; 4-column level-1 items: 261 with
+//   2-column, 281 with 4-column level 0, 331 with 4 columns everywhere); weight gradient 424 vs 340 us
+//   32x32 L3 bf16: forward 127.6 vs 154 us (256 threads, 4 pairs; 4-column level-1 items);
+//   weight gradient 191 vs 176 us
 //   16x16 L2 bf16: forward 64.1 vs 84.6 us (128 threads, 4 pairs; window rows outside the plane
 //   skipped); weight gradient 106 vs 122 us
 //   8x8 L1 bf16: forward 43.6 vs 78.5 us (64 threads, 8 pairs; window rows outside the plane
@@ -20,8 +22,8 @@
 //   threads) vs 85.7 with the planner's 8-row items and 94 on the whole-plane kernel
 //   56x56 L3 fp32: forward 131 with 7-row items at levels >= 1 (154 with 8-row) vs 119 us on the
 //   fused whole-plane kernel; weight gradient 169 vs 156 us
-#define WTCONV_SPEC_b64l4 b64l4, 64, 64, 4, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 256, 1, 1, 0, 0, -1
-#define WTCONV_SPEC_b32l3 b32l3, 32, 32, 3, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 256, 4, 1, 0, 0, -1
+#define WTCONV_SPEC_b64l4 b64l4, 64, 64, 4, 5, __nv_bfloat16, 1, 2, 8, 4, 8, 2, 8, 256, 1, 1, 0, 0, -1
+#define WTCONV_SPEC_b32l3 b32l3, 32, 32, 3, 5, __nv_bfloat16, 1, 2, 8, 4, 8, 2, 8, 256, 4, 1, 0, 0, -1
 #define WTCONV_SPEC_b16l2 b16l2, 16, 16, 2, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 128, 4, 1, 1, 0, -1
 #define WTCONV_SPEC_b8l1 b8l1, 8, 8, 1, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 64, 8, 1, 1, 0, -1
 #define WTCONV_SPEC_b28l2 b28l2, 28, 28, 2, 5, __nv_bfloat16, 1, 2, 14, 2, 7, 2, 7, 0, 0, 1, 1, 64, 6
