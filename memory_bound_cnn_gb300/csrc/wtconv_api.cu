@@ -978,6 +978,7 @@ PairPlan plan_pair_dw_uncached(int B, int C, int H, int W, int L, int k, int dty
     for (int si = 0; si <= kMenu; ++si) {
         const PairShape sh = si < kMenu ? kPairShapes[si] : PairShape{2, 7, 2, 7, 2, 7, 1.10};
         if (!pair_shape_allowed(si)) continue;
+        if (si == kMenu && H % 7 != 0 && !(knob_s && knob_s[0])) continue;  // 7-row items: planes of 7 * 2^l rows
         if (tuned && pref.dw_shape >= 0 && si != pref.dw_shape) continue;
         for (int T : {64, 128, 256}) {
             if (!pair_threads_allowed(T)) continue;
@@ -1061,12 +1062,21 @@ PairPlan plan_pair_dw_uncached(int B, int C, int H, int W, int L, int k, int dty
         }
     }
     if (best.status == WTCONV_OK) {
-        // units of several groups (one partial each): few enough partials to keep the flush and
-        // the finalize small, enough units to keep every resident CTA busy
+        // units of several groups (one partial each): enough items per thread in a unit that its
+        // flush (tap sums to shared memory, the reduction, the partial's store) stays small
+        // against its correlations, which matters on small planes (8 x 8: 77 -> 71 us at 8 groups
+        // per unit instead of 2), and enough units to keep every resident CTA busy
         PairArgs &a = best.a;
         const long long slots = (long long)sms * best.occ;
+        long long items_pair = 0;
+        for (int l = 0; l <= L; ++l) items_pair += (l == 0 ? 1 : 4) * (long long)a.geo.ns[l] * a.geo.ng[l];
+        const double per_thread_group = (double)a.G * items_pair / a.nthreads;
         int cg = 1;
-        while (cg < a.ngroups && (long long)C * ((a.ngroups + 2 * cg - 1) / (2 * cg)) >= 2 * slots) cg *= 2;
+        while (cg < a.ngroups && cg * per_thread_group < 8.0 &&
+               (long long)C * ((a.ngroups + 2 * cg - 1) / (2 * cg)) >= slots)
+            cg *= 2;
+        const char *kc = getenv("WTCONV_PAIR_CHUNK");  // tuning: groups per work unit
+        if (kc && kc[0] && atoi(kc) > 0) cg = std::min(atoi(kc), a.ngroups);
         pair_grid(a, sms, best.occ, cg);
         best.workspace = ((size_t)a.nchunks * C * nsig * (KK + 1) * sizeof(float) + 255) / 256 * 256;
     }
@@ -1084,7 +1094,9 @@ PairPlan cached_pair_plan(int kind, int B, int C, int H, int W, int L, int k, in
     }
     // the tuning restrictions are part of the key: a restricted plan is a different plan
     const char *vt = getenv("WTCONV_PAIR_THREADS"), *vs = getenv("WTCONV_PAIR_SHAPE"), *vg = getenv("WTCONV_PAIR_SLOTS");
-    const int knobs = ((vg && vg[0] ? atoi(vg) : 0) * 512 + (vt && vt[0] ? atoi(vt) : 0)) * 16 + (vs && vs[0] ? atoi(vs) + 1 : 0);
+    const char *vc = getenv("WTCONV_PAIR_CHUNK");
+    const int knobs = (((vc && vc[0] ? atoi(vc) : 0) * 128 + (vg && vg[0] ? atoi(vg) : 0)) * 512 +
+                       (vt && vt[0] ? atoi(vt) : 0)) * 16 + (vs && vs[0] ? atoi(vs) + 1 : 0);
     const PlanKey key(kind + 1000 * knobs, B, C, H, W, L, k, dtype, dev);
     {
         std::lock_guard<std::mutex> lock(mu);
