@@ -144,6 +144,29 @@ def test_tiled_pair_weight_gradient_is_deterministic(case):
         assert torch.equal(g1[n], g2[n]), n
 
 
+@pytest.mark.parametrize("case,launches", [((16, 64, 256, 256, 5, 5, "bf16"), 3), ((1, 2, 256, 256, 5, 5, "f32"), 3),
+                                           ((2, 3, 128, 128, 4, 5, "bf16"), 2)],
+                         ids=lambda c: "x".join(map(str, c)) if isinstance(c, tuple) else str(c))
+def test_large_planes_run_the_tiled_pair_weight_gradient(case, launches):
+    """Planes beyond the whole-plane kernels take the tiled batch-pair weight gradient by default:
+    one launch per two Haar levels (the later ones on the low bands the previous launch writes),
+    then the finalize; the launch count the library reports matches its kernel list."""
+    B, C, H, Wd, L, k, dt = case
+    code = {"f32": 0, "bf16": 1, "f16": 2}[dt]
+    names = W.wtconv_plan_kernels(W.OP_BACKWARD_WEIGHTS, B, C, H, Wd, L, k, code)
+    assert names == ["wtconv_ptile_dw_kernel", "wtconv_dw_finalize_kernel"], names
+    assert W.wtconv_launch_count(W.OP_BACKWARD_WEIGHTS, B, C, H, Wd, L, k, code) == launches + 1
+    shape = LayerShape(*case)
+    if shape.numel <= 8_000_000:
+        inputs = make_inputs(shape, seed=13)
+        d = to_device(inputs)
+        g = W.wtconv_backward_weights(d["x"], d["dy"], *[d[p] for p in PARAMS])
+        torch.cuda.synchronize()
+        g_ref = oracle.backward(inputs["x"], inputs["dy"], inputs)
+        for n in GRADS:
+            assert_close(n, np64(g[n]), g_ref[n], TOL[shape.dtype])
+
+
 def test_input_gradient_is_forward_with_rotated_kernels():
     """dx = forward(dy) with every kernel rotated 180 degrees and no bias (transpose identity)."""
     shape = LayerShape(2, 4, 32, 32, 3, 5, "f32")
