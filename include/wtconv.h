@@ -46,13 +46,16 @@
  *   - No state carries results from one call to the next (the library caches per-shape launch
  *     plans on the host, per device); concurrent calls on different streams with distinct
  *     workspaces are safe.
- *   - The forward and the input gradient run one of four kernel sets: the batch-pair kernel
+ *   - The forward and the input gradient run one of five kernel sets: the batch-pair kernel
  *     (two batch entries per packed fp32 pair, whole pyramids of several pairs on chip; small
  *     planes), the fused whole-plane kernel (fp32 planes where it is fastest), the whole-plane
- *     kernel (planes whose pyramid fits in shared memory), or two tiled kernels (larger planes).
- *     WTCONV_FWD_PATH=pair, =fused, =plane or =tiles selects a set where it applies (same results
- *     within fp32 rounding); WTCONV_PAIR=0 / =1 keeps the batch-pair kernels off / makes them the
- *     default wherever they apply.
+ *     kernel (planes whose pyramid fits in shared memory), or, on larger planes, the deep kernel
+ *     (levels >= 2 at level-1 resolution, into the workspace) followed by a tiled shallow kernel:
+ *     the batch-pair one (tiles of x with halo and of the deep part by bulk tensor copies; planes
+ *     whose rows are a multiple of 16 bytes and of 8 elements) or else the one-warp one.
+ *     WTCONV_FWD_PATH=pair, =fused, =plane, =ptile or =tiles selects a set where it applies (same
+ *     results within fp32 rounding); WTCONV_PAIR=0 / =1 keeps the batch-pair kernels off / makes
+ *     them the default wherever they apply.
  *   - The weight gradients run the batch-pair kernel on small planes, else the fused
  *     whole-plane kernel (x and dy planes moved by bulk tensor copies, both pyramids on chip; fp32
  *     planes of at least 64 base items where both copies fit one box of at most 256 x 256), else a
@@ -64,8 +67,11 @@
  *     where it applies (same results within fp32 rounding).
  *   - Tuning restrictions for measurement runs (the plans they give are valid, only slower or
  *     faster): WTCONV_PAIR_THREADS, WTCONV_PAIR_SHAPE and WTCONV_PAIR_SLOTS fix the batch-pair
- *     kernels' CTA size, item shapes and pair slots per group; WTCONV_PTILE=TH,TW,G,threads[,narrow]
- *     fixes the first tiled batch-pair launch's tile, pair slots, CTA size and item width;
+ *     kernels' CTA size, item shapes and pair slots per group; WTCONV_PAIR_CHUNK fixes the
+ *     batch-pair weight gradient's slot groups per work unit; WTCONV_PTILE=TH,TW,G,threads[,narrow]
+ *     fixes the first tiled batch-pair weight-gradient launch's tile, pair slots, CTA size and
+ *     item width; WTCONV_PSHALLOW=TH,TW,G,threads[,rows] fixes the tiled batch-pair shallow
+ *     kernel's tile, pair slots, CTA size and item rows;
  *     WTCONV_STAGED=G,threads fixes the planes per slot group and CTA size of the whole-plane and
  *     deep kernels.
  *   - Setting the environment variable WTCONV_INJECT_FAULT=1 makes every compute entry point
@@ -160,7 +166,7 @@ const char *wtconv_plan_kernels(int op, int B, int C, int H, int W, int L, int k
  * or unsupported shape).  Planes whose Haar pyramid fits in shared memory take one launch for
  * the forward and the input gradient and two for the weight gradients (correlations +
  * finalize); larger planes take two for the forward / input gradient (levels >= 2, then the
- * base conv and level 1) and, for the weight gradients, one tiled launch per two Haar levels
+ * base conv and level 1; one when L = 1) and, for the weight gradients, one tiled launch per two Haar levels
  * plus the finalize (ceil(L / 2) + 1; with WTCONV_DW_PATH=tiles the older tiled chain, 2L + 2).
  * BACKWARD is the sum of BACKWARD_INPUT and BACKWARD_WEIGHTS.  Sides that are not multiples of
  * 2^L add the pads and the crop: two launches for FORWARD, BACKWARD_INPUT and

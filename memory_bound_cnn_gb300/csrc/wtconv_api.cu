@@ -19,6 +19,7 @@
 #include "wtconv_internal.h"
 #include "wtconv_pad.h"
 #include "wtconv_pair.cuh"
+#include "wtconv_pshallow.h"
 #include "wtconv_ptile.h"
 #include "wtconv_selftest.h"
 
@@ -527,6 +528,171 @@ bool shallow_tma_d_ok(const ShallowArgs &a) {
 CUtensorMapDataType tma_dtype(int dtype) {
     return dtype == WTCONV_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                : dtype == WTCONV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+// ------------------------------------------------------------------ tiled batch-pair shallow kernel
+
+struct PsPlan {
+    int status = WTCONV_ERR_UNSUPPORTED;
+    PsArgs a{};
+    size_t smem = 0;
+    int occ = 0;
+};
+
+// Geometry of one tile shape: false where the bulk tensor copies or the item shapes do not apply
+// (tile rows a multiple of 16 so that level 1 holds whole 8-row items; every copy origin, row and
+// box row 16-byte aligned; box extents within 256).
+bool ps_make(PsArgs &a, int B, int C, int H, int W, int K, int eb, bool deep, int TH, int TW, int G, int nt, int S) {
+    a = PsArgs{};
+    const int P = K / 2, al = 16 / eb;
+    a.B = B; a.C = C; a.H = H; a.W = W; a.K = K;
+    a.TH = TH; a.TW = TW; a.G = G; a.nthreads = nt;
+    a.HX = 2 * P;
+    a.HXL = (a.HX + al - 1) / al * al;
+    a.RXR = TH + 2 * a.HX;
+    a.RXW = (a.HXL + TW + a.HX + al - 1) / al * al;
+    if (TH <= 0 || TW <= 0 || TH % 16 != 0 || TW % 8 != 0 || H % 2 != 0 || W % 8 != 0) return false;
+    if (S != 4 && S != 8) return false;
+    if (((size_t)W * eb) % 16 != 0 || ((size_t)TW * eb) % 16 != 0) return false;
+    if (a.RXW > 256 || a.RXR > 256 || 2 * G > 256 || TW / 2 > 256 || TH / 2 > 256) return false;
+    const int TH1 = TH / 2, TW1 = TW / 2;
+    a.tiles_r = (H + TH - 1) / TH;
+    a.tiles_c = (W + TW - 1) / TW;
+    a.tiles = a.tiles_r * a.tiles_c;
+    a.npairs = (B + 1) / 2;
+    a.ngroups = (a.npairs + G - 1) / G;
+    if ((long long)C * a.tiles * a.ngroups > (long long)INT32_MAX / 2) return false;
+    a.work = C * a.tiles * a.ngroups;
+    a.q0 = 2; a.s0 = S;
+    a.ns0 = TW / 2; a.ng0 = TH / S;
+    a.ipitch0 = pg_round2(TW + 2 * P);
+    a.irows0 = TH + 2 * P;
+    a.q1 = 2; a.s1 = S;
+    a.ns1 = TW1 / 2; a.ng1 = TH1 / S;
+    a.ipitch1 = pg_round2(TW1 + 2 * P);
+    a.irows1 = TH1 + 2 * P;
+    a.iimg1 = a.ipitch1 * a.irows1;
+    a.zpitch1 = pg_round2(TW1);
+    a.zrows1 = TH1;
+    a.zimg1 = a.zpitch1 * a.zrows1;
+    a.off_x = 0;
+    a.off_y1 = a.ipitch0 * a.irows0;
+    a.off_z1 = a.off_y1 + 4 * a.iimg1;
+    a.slot = pg_round2(a.off_z1 + 5 * a.zimg1);
+    a.raw_x_bytes = (int)(((size_t)2 * G * a.RXR * a.RXW * eb + 127) / 128 * 128);
+    a.has_deep = deep ? 1 : 0;
+    a.raw_d_bytes = deep ? (int)(((size_t)2 * G * TH1 * TW1 * sizeof(float) + 127) / 128 * 128) : 0;
+    a.vec_st = 1;  // W even, items 2 columns wide at even columns
+    const int xbw = (TW + 2 * a.HX) / 2, xbh = (TH + 2 * a.HX) / 2;
+    a.dv_work_c = make_fastdiv(a.tiles * a.ngroups);
+    a.dv_ngroups = make_fastdiv(a.ngroups);
+    a.dv_tiles_c = make_fastdiv(a.tiles_c);
+    a.dv_xb = make_fastdiv(xbw * xbh);
+    a.dv_xbw = make_fastdiv(xbw);
+    a.dv_conv = make_fastdiv(4 * a.ns1 * a.ng1);
+    a.dv_ns1 = make_fastdiv(a.ns1);
+    a.dv_out = make_fastdiv(a.ns0 * a.ng0);
+    a.dv_ns0 = make_fastdiv(a.ns0);
+    a.dv_db = make_fastdiv(TH1 * TW1);
+    a.dv_dbw = make_fastdiv(TW1);
+    return true;
+}
+
+// Tuning restrictions (0: planner's choice): WTCONV_PSHALLOW=TH,TW,G,threads,item rows.
+void ps_knobs(int &th, int &tw, int &g, int &nt, int &sr) {
+    th = tw = g = nt = sr = 0;
+    const char *v = getenv("WTCONV_PSHALLOW");
+    if (v && v[0]) sscanf(v, "%d,%d,%d,%d,%d", &th, &tw, &g, &nt, &sr);
+}
+
+PsPlan plan_pshallow_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
+    PsPlan p;
+    const int eb = elem_bytes(dtype);
+    if (B < 1 || L < 1 || H % (1 << L) != 0 || W % (1 << L) != 0) return p;
+    const int sms = device_sms();
+    if (sms <= 0) { p.status = WTCONV_ERR_CUDA; return p; }
+    int kth = 0, ktw = 0, kg = 0, knt = 0, ksr = 0;
+    ps_knobs(kth, ktw, kg, knt, ksr);
+    const int Hr = (H + 15) / 16 * 16, Wr = (W + 7) / 8 * 8;
+    double best_score = -1.0;
+    for (int th0 : {16, 32}) {
+        const int TH = std::min(th0, Hr);
+        if (kth && TH != kth) continue;
+        if (th0 > 16 && TH < th0) continue;  // the same tile as th0 = 16
+        for (int tw0 : {32, 64}) {
+            const int TW = std::min(tw0, Wr);
+            if (ktw && TW != ktw) continue;
+            if (tw0 > 32 && TW < tw0) continue;
+            for (int ns : {0, 1, 2, 3}) {  // (threads, item rows): (64, 8), (64, 4), (128, 8), (128, 4)
+                const int nt = ns < 2 ? 64 : 128, S = (ns & 1) ? 4 : 8;
+                if (knt && nt != knt) continue;
+                if (ksr && S != ksr) continue;
+                for (int G = 1; G <= 8; ++G) {
+                    if (kg && G != kg) continue;
+                    PsArgs a;
+                    if (!ps_make(a, B, C, H, W, k, eb, L >= 2, TH, TW, G, nt, S)) break;
+                    if (G > a.npairs) break;
+                    const size_t smem = pshallow_smem_bytes(a);
+                    if (smem + kStaticSmemMargin > (size_t)kMaxSmem) break;
+                    const int occ = occupancy_pshallow(dtype, k, smem, nt, S);
+                    if (occ <= 0) break;
+                    // resident threads first (the FMA chains of one item are long; more warps hide
+                    // the shared-memory latency), then how evenly a group's items fill the threads,
+                    // then the share of the x tile that is halo (pass-1 work and L2 reads)
+                    const long long items = (long long)G * a.ns0 * a.ng0;
+                    const double fill = (double)items / ((double)((items + nt - 1) / nt) * nt);
+                    const double resident = std::min(768.0, (double)occ * nt) / 768.0;
+                    const double halo = (double)(TH * TW) / ((double)a.RXR * (TW + 2 * a.HX));
+                    const double tiles_used = (double)H * W / ((double)a.tiles * TH * TW);
+                    const double score = resident * std::sqrt(fill) * std::sqrt(halo) * tiles_used;
+                    const char *vb = getenv("WTCONV_VERBOSE");
+                    if (vb && vb[0] == '2')
+                        fprintf(stderr, "  pshallow candidate %dx%d G=%d nt=%d S=%d smem=%zu occ=%d fill=%.3f halo=%.3f score=%.4f\n",
+                                TH, TW, G, nt, S, smem, occ, fill, halo, score);
+                    if (score > best_score) {
+                        best_score = score;
+                        p.a = a;
+                        p.smem = smem;
+                        p.occ = occ;
+                    }
+                }
+            }
+        }
+    }
+    if (best_score <= 0.0) return p;
+    p.a.grid = (int)std::min<long long>(p.a.work, (long long)sms * p.occ);
+    p.status = WTCONV_OK;
+    return p;
+}
+
+PsPlan plan_pshallow(int B, int C, int H, int W, int L, int k, int dtype) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int, int, int, int, int, std::string>, PsPlan> cache;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        PsPlan p;
+        p.status = WTCONV_ERR_CUDA;
+        return p;
+    }
+    const char *kn = getenv("WTCONV_PSHALLOW");
+    const auto key = std::make_tuple(B, C, H, W, L, k, dtype, dev, std::string(kn ? kn : ""));
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    PsPlan p = plan_pshallow_uncached(B, C, H, W, L, k, dtype);
+    const char *verbose = getenv("WTCONV_VERBOSE");
+    if (verbose && verbose[0] == '1')
+        fprintf(stderr, "wtconv plan pshallow B=%d C=%d H=%d W=%d L=%d k=%d dtype=%d: status %d tile=%dx%d G=%d "
+                        "threads=%d rows=%d work=%d grid=%d smem=%zu occ=%d\n",
+                B, C, H, W, L, k, dtype, p.status, p.a.TH, p.a.TW, p.a.G, p.a.nthreads, p.a.s0, p.a.work, p.a.grid,
+                p.smem, p.occ);
+    if (p.status == WTCONV_OK || p.status == WTCONV_ERR_UNSUPPORTED) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache.emplace(key, p);
+    }
+    return p;
 }
 
 // Tiled weight gradient: the shallow kernel's tiles (bulk tensor copies of x and dy, tiles of a
@@ -1385,17 +1551,20 @@ PtPlan plan_ptile_dw(int B, int C, int H, int W, int L, int k, int dtype) {
     return p;
 }
 
-// Forward / input-gradient path of a shape (WTCONV_FWD_PATH=fused / tiles / plane selects a path
-// where it applies).  By default the fused whole-plane kernel runs where it measured fastest on
-// GB300: fp32 planes with at least 64 output items and three or more resident CTAs per SM; else
-// the whole-plane kernel where the pyramid fits; else the tiled kernels.
-enum FwdPath { FWD_FUSED, FWD_PLANE, FWD_TILES, FWD_PAIR };
+// Forward / input-gradient path of a shape (WTCONV_FWD_PATH=pair / fused / plane / ptile / tiles
+// selects a path where it applies).  By default the batch-pair whole-plane kernel runs where it
+// measured fastest; else the fused whole-plane kernel where it measured fastest on GB300: fp32
+// planes with at least 64 output items and three or more resident CTAs per SM; else the
+// whole-plane kernel where the pyramid fits; else the deep kernel followed by the tiled batch-pair
+// shallow kernel; else the deep kernel followed by the one-warp tiled shallow kernel.
+enum FwdPath { FWD_FUSED, FWD_PLANE, FWD_TILES, FWD_PAIR, FWD_PTILE };
 struct FwdChoice {
     int status = WTCONV_OK;
     FwdPath path = FWD_PLANE;
     PPlan pp;
     Plan pf;
     PairPlan pr;
+    PsPlan ps;
 };
 
 FwdChoice choose_fwd(int B, int C, int H, int W, int L, int k, int dtype) {
@@ -1405,6 +1574,15 @@ FwdChoice choose_fwd(int B, int C, int H, int W, int L, int k, int dtype) {
     const bool want_tiles = env && strcmp(env, "tiles") == 0;
     const bool want_plane = env && strcmp(env, "plane") == 0;
     const bool want_pair = env && strcmp(env, "pair") == 0;
+    const bool want_ptile = env && strcmp(env, "ptile") == 0;
+    if (want_ptile) {
+        f.ps = plan_pshallow(B, C, H, W, L, k, dtype);
+        if (f.ps.status != WTCONV_OK && f.ps.status != WTCONV_ERR_UNSUPPORTED) { f.status = f.ps.status; return f; }
+        if (f.ps.status == WTCONV_OK) {
+            f.path = FWD_PTILE;
+            return f;
+        }
+    }
     if (!want_tiles && !want_plane && !want_fused) {
         f.pr = plan_pair_fwd(B, C, H, W, L, k, dtype);
         if (f.pr.status != WTCONV_OK && f.pr.status != WTCONV_ERR_UNSUPPORTED) { f.status = f.pr.status; return f; }
@@ -1429,6 +1607,14 @@ FwdChoice choose_fwd(int B, int C, int H, int W, int L, int k, int dtype) {
         return f;
     }
     if (f.pf.status != WTCONV_OK && f.pf.status != WTCONV_ERR_UNSUPPORTED) { f.status = f.pf.status; return f; }
+    if (!want_tiles) {
+        f.ps = plan_pshallow(B, C, H, W, L, k, dtype);
+        if (f.ps.status != WTCONV_OK && f.ps.status != WTCONV_ERR_UNSUPPORTED) { f.status = f.ps.status; return f; }
+        if (f.ps.status == WTCONV_OK) {
+            f.path = FWD_PTILE;
+            return f;
+        }
+    }
     f.path = FWD_TILES;
     return f;
 }
@@ -1662,6 +1848,7 @@ static const char *plan_kernels_inner(int op, int B, int C, int H, int W, int L,
         f = fc.path == FWD_PAIR ? "wtconv_pair_fwd_kernel"
             : fc.path == FWD_FUSED ? "wtconv_plane_kernel"
             : fc.path == FWD_PLANE ? "wtconv_fwd_kernel"
+            : fc.path == FWD_PTILE ? (L >= 2 ? "wtconv_deep_kernel+wtconv_pshallow_kernel" : "wtconv_pshallow_kernel")
             : (L >= 2 ? "wtconv_deep_kernel+wtconv_shallow_kernel" : "wtconv_shallow_kernel");
         if (fwd) return f;
     }
@@ -1725,7 +1912,7 @@ static int launch_count_inner(int op, int B, int C, int H, int W, int L, int k, 
     if (op == WTCONV_OP_FORWARD || op == WTCONV_OP_BACKWARD_INPUT || op == WTCONV_OP_BACKWARD) {
         const FwdChoice f = choose_fwd(B, C, H, W, L, k, dtype);
         if (f.status != WTCONV_OK) return 0;
-        n += f.path == FWD_TILES ? (L >= 2 ? 2 : 1) : 1;
+        n += (f.path == FWD_TILES || f.path == FWD_PTILE) ? (L >= 2 ? 2 : 1) : 1;
     }
     if (op == WTCONV_OP_BACKWARD_WEIGHTS || op == WTCONV_OP_BACKWARD) {
         const DwChoice d = choose_dw(B, C, H, W, L, k, dtype);
@@ -1790,8 +1977,11 @@ static int run_operator(int B, int C, int H, int W, int L, int k, int dtype, con
         pd = plan_deep(B, C, H, W, L, k, dtype);
         if (pd.status != WTCONV_OK) return pd.status;
     }
-    SPlan ps = plan_shallow(B, C, H, W, L, k, dtype);
-    if (ps.status != WTCONV_OK) return ps.status;
+    SPlan ps;
+    if (fc.path == FWD_TILES) {
+        ps = plan_shallow(B, C, H, W, L, k, dtype);
+        if (ps.status != WTCONV_OK) return ps.status;
+    }
     if (workspace_bytes < dbytes || (dbytes > 0 && !aligned16(workspace))) return WTCONV_ERR_WORKSPACE;
     float *deep = L >= 2 ? static_cast<float *>(workspace) : nullptr;
     if (L >= 2) {
@@ -1800,6 +1990,25 @@ static int run_operator(int B, int C, int H, int W, int L, int k, int dtype, con
         pd.a.flip = flip ? 1 : 0;
         pd.a.with_bias = 0;
         if (launch_deep(pd.a, deep, dtype, pd.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
+    }
+    const int eb = elem_bytes(dtype);
+    if (fc.path == FWD_PTILE) {
+        PsArgs a = fc.ps.a;
+        a.x = src;
+        a.deep = deep;
+        a.out = dst;
+        a.base_w = base_w; a.base_bias = base_bias; a.base_scale = base_scale;
+        a.wavelet_w = wavelet_w; a.wavelet_scale = wavelet_scale;
+        a.flip = flip ? 1 : 0;
+        a.with_bias = flip ? 0 : 1;
+        a.timeout = timeout_flag();
+        if (a.timeout == nullptr) return WTCONV_ERR_CUDA;
+        if (!encode_map(&a.tmap_x, tma_dtype(dtype), eb, src, W, H, C, B, a.RXW, a.RXR, 2 * a.G))
+            return WTCONV_ERR_CUDA;
+        if (deep != nullptr && !encode_map(&a.tmap_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, deep, W / 2, H / 2, C, B,
+                                           a.TW / 2, a.TH / 2, 2 * a.G))
+            return WTCONV_ERR_CUDA;
+        return cuda_status(launch_pshallow(a, dtype, fc.ps.smem, s));
     }
     ShallowArgs &a = ps.a;
     a.x = src;
@@ -1811,7 +2020,6 @@ static int run_operator(int B, int C, int H, int W, int L, int k, int dtype, con
     a.with_bias = flip ? 0 : 1;
     a.timeout = timeout_flag();
     if (a.timeout == nullptr) return WTCONV_ERR_CUDA;
-    const int eb = elem_bytes(dtype);
     a.tma_x = shallow_tma_x_ok(a, eb) &&
               encode_map(&a.tmap_x, tma_dtype(dtype), eb, src, W, H, C, B, a.sg.xw, a.sg.xrows, a.sg.G);
     a.tma_d = deep != nullptr && shallow_tma_d_ok(a) &&

@@ -93,8 +93,10 @@ __device__ __forceinline__ void store_row(const f2_t (&acc)[Q], T *d0, T *d1, in
 // soon as its window is complete: an even row 2m adds the level-1 inverse butterflies of row m of
 // Z^1 (LL already holding the deeper levels) for a = 0 and keeps those for a = 1 until row 2m+1:
 // pixel (a, b) of position (m, p) gains LL + (-1)^b LH + (-1)^a HL + (-1)^(a+b) HH.
-// SKIP: as in pair_conv_strip, the first zt and last zb window rows are zero padding.
-template <int K, int Q, int S, typename T, bool SKIP = false>
+// SKIP: as in pair_conv_strip, the first zt and last zb window rows are zero padding.  DEEP: a
+// fifth image after the four subband images of z1 (at z1 + 4 zimg) holds the contribution of the
+// deeper levels at level-1 resolution, which enters with the low band (all four pixels).
+template <int K, int Q, int S, typename T, bool SKIP = false, bool DEEP = false>
 __device__ __forceinline__ void pair_out_item(const f2_t *__restrict__ in, int pitch, const f2_t (&w)[K * K],
                                               f2_t bias2, const f2_t *__restrict__ z1, int zpitch, int zimg, T *d0,
                                               T *d1, int W, int nrows, int ncols, bool vec, int zt = 0, int zb = 0) {
@@ -144,8 +146,14 @@ __device__ __forceinline__ void pair_out_item(const f2_t *__restrict__ in, int p
                 const ulonglong2 a3 = *reinterpret_cast<const ulonglong2 *>(zr + 3 * zimg);
                 ll[0] = a0.x; ll[1] = a0.y; lh[0] = a1.x; lh[1] = a1.y;
                 hl[0] = a2.x; hl[1] = a2.y; hh[0] = a3.x; hh[1] = a3.y;
+                if constexpr (DEEP) {
+                    const ulonglong2 a4 = *reinterpret_cast<const ulonglong2 *>(zr + 4 * zimg);
+                    ll[0] = fadd2(ll[0], a4.x);
+                    ll[1] = fadd2(ll[1], a4.y);
+                }
             } else {
                 ll[0] = zr[0]; lh[0] = zr[zimg]; hl[0] = zr[2 * zimg]; hh[0] = zr[3 * zimg];
+                if constexpr (DEEP) ll[0] = fadd2(ll[0], zr[4 * zimg]);
             }
 #pragma unroll
             for (int m = 0; m < QL; ++m) {

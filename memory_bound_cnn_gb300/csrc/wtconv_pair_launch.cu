@@ -3,6 +3,7 @@
 #include "wtconv_pair_dw.cuh"
 #include "wtconv_pair_fwd.cuh"
 #include "wtconv_pair_specs.h"
+#include "wtconv_pshallow.cuh"
 #include "wtconv_ptile_dw.cuh"
 
 namespace wtconv {
@@ -132,6 +133,35 @@ int occupancy_ptile_dw(int dtype, int K, int LT, int base, size_t smem, int nthr
     case 0: return occupancy_ptile_dw_f32(K, LT, base, smem, nthreads, iq);
     case 1: return occupancy_ptile_dw_bf16(K, LT, base, smem, nthreads, iq);
     case 2: return occupancy_ptile_dw_f16(K, LT, base, smem, nthreads, iq);
+    default: return 0;
+    }
+}
+
+// ---------------------------------------------------------------- tiled batch-pair shallow kernel
+
+cudaError_t launch_pshallow_f32(const PsArgs &a, size_t smem, cudaStream_t st);
+cudaError_t launch_pshallow_bf16(const PsArgs &a, size_t smem, cudaStream_t st);
+cudaError_t launch_pshallow_f16(const PsArgs &a, size_t smem, cudaStream_t st);
+int occupancy_pshallow_f32(int K, size_t smem, int nthreads, int s);
+int occupancy_pshallow_bf16(int K, size_t smem, int nthreads, int s);
+int occupancy_pshallow_f16(int K, size_t smem, int nthreads, int s);
+
+size_t pshallow_smem_bytes(const PsArgs &a) { return pshallow_layout(a).total; }
+
+cudaError_t launch_pshallow(const PsArgs &a, int dtype, size_t smem, cudaStream_t st) {
+    switch (dtype) {
+    case 0: return launch_pshallow_f32(a, smem, st);
+    case 1: return launch_pshallow_bf16(a, smem, st);
+    case 2: return launch_pshallow_f16(a, smem, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int occupancy_pshallow(int dtype, int K, size_t smem, int nthreads, int s) {
+    switch (dtype) {
+    case 0: return occupancy_pshallow_f32(K, smem, nthreads, s);
+    case 1: return occupancy_pshallow_bf16(K, smem, nthreads, s);
+    case 2: return occupancy_pshallow_f16(K, smem, nthreads, s);
     default: return 0;
     }
 }

@@ -1,0 +1,13 @@
+// Tiled batch-pair shallow kernel instantiations for float activations.
+#include "wtconv_pshallow.cuh"
+
+namespace wtconv {
+
+cudaError_t launch_pshallow_f32(const PsArgs &a, size_t smem, cudaStream_t st) {
+    return launch_pshallow_typed<float>(a, smem, st);
+}
+int occupancy_pshallow_f32(int K, size_t smem, int nthreads, int s) {
+    return occupancy_pshallow_typed<float>(K, smem, nthreads, s);
+}
+
+}  // namespace wtconv

@@ -43,7 +43,7 @@ def check_layer(shape: LayerShape, inputs: dict, split: bool = True):
     d = to_device(inputs)
     y_ref = oracle.forward(inputs["x"], inputs)
     g_ref = oracle.backward(inputs["x"], inputs["dy"], inputs)
-    for path in ("default", "pair", "plane", "tiles", "fused"):
+    for path in ("default", "pair", "plane", "ptile", "tiles", "fused"):
         with fwd_path(path):
             y = gpu_forward(d)
             dx, g = gpu_backward(d)
@@ -167,6 +167,42 @@ def test_large_planes_run_the_tiled_pair_weight_gradient(case, launches):
             assert_close(n, np64(g[n]), g_ref[n], TOL[shape.dtype])
 
 
+PTILE_FWD = [
+    # (B, C, H, W, L, k, dtype): ragged last tile rows / columns, an odd batch (a half pair), L = 1
+    # (no deeper levels), every kernel size and activation type
+    (3, 2, 40, 200, 3, 5, "bf16"),
+    (2, 3, 64, 96, 1, 3, "f32"),
+    (5, 2, 48, 72, 2, 7, "f16"),
+    (4, 2, 256, 256, 5, 5, "bf16"),
+    (1, 3, 128, 64, 4, 7, "f32"),
+]
+
+
+@pytest.mark.parametrize("case", PTILE_FWD, ids=lambda c: "x".join(map(str, c)))
+def test_tiled_pair_forward(case):
+    """The tiled batch-pair shallow kernel (after the deep kernel where L >= 2), selected where it
+    applies, against the oracle for the forward and the input gradient."""
+    B, C, H, Wd, L, k, dt = case
+    code = {"f32": 0, "bf16": 1, "f16": 2}[dt]
+    with fwd_path("ptile"):
+        names = W.wtconv_plan_kernels(W.OP_FORWARD, B, C, H, Wd, L, k, code)
+        n = W.wtconv_launch_count(W.OP_FORWARD, B, C, H, Wd, L, k, code)
+    want = (["wtconv_deep_kernel"] if L >= 2 else []) + ["wtconv_pshallow_kernel"]
+    assert names == want, names
+    assert n == len(want)
+    shape = LayerShape(*case)
+    inputs = make_inputs(shape, seed=17)
+    d = to_device(inputs)
+    tol = TOL[shape.dtype]
+    with fwd_path("ptile"):
+        y = gpu_forward(d)
+        dx = W.wtconv_backward_input(d["dy"], *[d[p] for p in PARAMS])
+    torch.cuda.synchronize()
+    assert_close("y [ptile]", np64(y), oracle.forward(inputs["x"], inputs), tol)
+    g_ref = oracle.backward(inputs["x"], inputs["dy"], inputs)
+    assert_close("dx [ptile]", np64(dx), g_ref["dx"], tol)
+
+
 def test_input_gradient_is_forward_with_rotated_kernels():
     """dx = forward(dy) with every kernel rotated 180 degrees and no bias (transpose identity)."""
     shape = LayerShape(2, 4, 32, 32, 3, 5, "f32")
@@ -181,7 +217,7 @@ def test_input_gradient_is_forward_with_rotated_kernels():
     assert_close("dx vs rotated forward", np64(dx), np64(y), 1e-6)
 
 
-@pytest.mark.parametrize("path", ["default", "pair", "plane", "tiles", "fused"])
+@pytest.mark.parametrize("path", ["default", "pair", "plane", "ptile", "tiles", "fused"])
 def test_outputs_stay_in_bounds_and_inputs_untouched(path):
     """Canary words around every output; inputs byte-identical after the calls."""
     shape = LayerShape(3, 5, 24, 16, 3, 5, "bf16")
