@@ -1121,7 +1121,11 @@ PairPlan plan_pair_fwd_uncached(int B, int C, int H, int W, int L, int k, int dt
             }
         }
     }
-    if (best.status == WTCONV_OK) pair_grid(best.a, sms, best.occ, 1);
+    if (best.status == WTCONV_OK) {
+        const char *ks = getenv("WTCONV_PAIR_SPLIT");  // tuning: 0 keeps every warp on every level
+        best.a.split = (L >= 3 && best.a.nthreads >= 128 && !(ks && ks[0] == '0')) ? 1 : 0;
+        pair_grid(best.a, sms, best.occ, 1);
+    }
     return best;
 }
 
@@ -1251,7 +1255,7 @@ PairPlan plan_pair_dw_uncached(int B, int C, int H, int W, int L, int k, int dty
 
 PairPlan cached_pair_plan(int kind, int B, int C, int H, int W, int L, int k, int dtype) {
     static std::mutex mu;
-    static std::map<PlanKey, PairPlan> cache;
+    static std::map<std::pair<PlanKey, std::string>, PairPlan> cache;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         PairPlan p;
@@ -1259,11 +1263,14 @@ PairPlan cached_pair_plan(int kind, int B, int C, int H, int W, int L, int k, in
         return p;
     }
     // the tuning restrictions are part of the key: a restricted plan is a different plan
-    const char *vt = getenv("WTCONV_PAIR_THREADS"), *vs = getenv("WTCONV_PAIR_SHAPE"), *vg = getenv("WTCONV_PAIR_SLOTS");
-    const char *vc = getenv("WTCONV_PAIR_CHUNK");
-    const int knobs = (((vc && vc[0] ? atoi(vc) : 0) * 128 + (vg && vg[0] ? atoi(vg) : 0)) * 512 +
-                       (vt && vt[0] ? atoi(vt) : 0)) * 16 + (vs && vs[0] ? atoi(vs) + 1 : 0);
-    const PlanKey key(kind + 1000 * knobs, B, C, H, W, L, k, dtype, dev);
+    std::string knobs;
+    for (const char *kn : {"WTCONV_PAIR_THREADS", "WTCONV_PAIR_SHAPE", "WTCONV_PAIR_SLOTS", "WTCONV_PAIR_CHUNK",
+                           "WTCONV_PAIR_SPLIT"}) {
+        const char *v = getenv(kn);
+        knobs += v ? v : "";
+        knobs += ';';
+    }
+    const auto key = std::make_pair(PlanKey(kind, B, C, H, W, L, k, dtype, dev), knobs);
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = cache.find(key);

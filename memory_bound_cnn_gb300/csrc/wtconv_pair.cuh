@@ -95,6 +95,8 @@ struct PairArgs {
     int raw_pair_bytes;     // raw bytes of one pair slot (two planes, or four for the weight gradient)
     int vec_st;             // 1: rows allow 4-element vector stores / loads of activations
     int spec;               // >= 0: the shape-specialised instantiation of this index runs (else -1)
+    int split;              // forward, L >= 3, 128 threads or more: the last warp builds and convolves
+                            // levels >= 3 while the others convolve levels 1 and 2
     const void *x;          // forward: x; input gradient: dy; weight gradient: x
     const void *dy;         // weight gradient: dy
     void *out;              // y or dx

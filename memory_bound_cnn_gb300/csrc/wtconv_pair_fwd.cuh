@@ -185,15 +185,15 @@ __device__ __forceinline__ int divq(int n, int d, const FastDiv &f) {
 // (base + e) % nt == tid.  The level's geometry sits in registers for the whole loop.
 template <int K, int Q, int S, bool FIX, bool SKIP = false>
 __device__ __forceinline__ void conv_level(const PairArgs &a, const PairGeo &g, f2_t *slots, const f2_t *wts, int np,
-                                           int l, int base) {
+                                           int l, int base, int t0 = 0, int nt = 0) {
     constexpr int WP = wpairs(K), KK = K * K;
-    const int nt = blockDim.x;
+    if (nt == 0) nt = blockDim.x;
     const int ns = g.ns[l], per_img = ns * g.ng[l];
     const int ip = g.ipitch[l], zp = g.zpitch[l], ii = g.iimg[l], zi = g.zimg[l];
     const int oy = g.off_y[l], oz = g.off_z[l], slot = g.slot;
     const FastDiv dpi = a.dv_lvl[l], dns = a.dv_lvl_ns[l];
     const int n = np * 4 * per_img;
-    int e = (int)threadIdx.x - base % nt;
+    int e = (int)threadIdx.x - t0 - base % nt;
     if (e < 0) e += nt;
     for (; e < n; e += nt) {
         const int img = divq<FIX>(e, per_img, dpi), rem = e - img * per_img;
@@ -211,15 +211,16 @@ __device__ __forceinline__ void conv_level(const PairArgs &a, const PairGeo &g, 
 
 // Analysis pass building level l0 (and l0+1 when it exists) of every slot's pyramid from the
 // low band of level l0-1 (an interior image of the slot).  Blocks are 4x4 of the finer low band
-// when two levels are built, 2x2 otherwise.
-__device__ __forceinline__ void analysis_deep_pass(const PairGeo &g, f2_t *slots, int np, int l0, int L) {
+// when two levels are built, 2x2 otherwise.  Threads t0 .. t0+nt-1 share the blocks.
+__device__ __forceinline__ void analysis_deep_pass(const PairGeo &g, f2_t *slots, int np, int l0, int L, int t0,
+                                                   int nt) {
     const bool two = l0 + 1 <= L;
     const int hs = g.h[l0 - 1], ws = g.w[l0 - 1];
     const int bsz = two ? 4 : 2;
     const int bw = ws / bsz, n = (hs / bsz) * bw;
     const int P = g.P;
     const int sp = g.ipitch[l0 - 1];
-    for (int t = threadIdx.x; t < np * n; t += blockDim.x) {
+    for (int t = (int)threadIdx.x - t0; t < np * n; t += nt) {
         const int gs = t / n, e = t - gs * n;
         const int bi = e / bw, bj = e - bi * bw;
         f2_t *slot = slots + (size_t)gs * g.slot;
@@ -392,14 +393,33 @@ __device__ __forceinline__ void pass1(const PairArgs &a, const PairGeo &g, f2_t 
 // Conv items of levels LV .. L of an instantiation with a compile-time geometry: each level's
 // item shape is a constant (rows drop to 4 on images of at most 4 rows), so shapes outside the
 // run-time menu (e.g. 7-row items on 28 x 28 planes) work as well.
-template <int K, class Spec, int LV>
+template <int K, class Spec, int LV, int LAST = Spec::kL>
 __device__ __forceinline__ void conv_levels_fixed(const PairArgs &a, const PairGeo &g, f2_t *slots, const f2_t *wts,
-                                                  int np, int first) {
-    if constexpr (LV <= Spec::kL) {
+                                                  int np, int first, int t0 = 0, int nt = 0) {
+    if constexpr (LV <= LAST) {
         constexpr int Q = LV == 1 ? Spec::kQL : Spec::kQD;
         constexpr int S = (Spec::kH >> LV) <= 4 ? 4 : (LV == 1 ? Spec::kSL : Spec::kSD);
-        conv_level<K, Q, S, true, Spec::kSkip>(a, g, slots, wts, np, LV, np * first);
-        conv_levels_fixed<K, Spec, LV + 1>(a, g, slots, wts, np, first + 4 * g.ns[LV] * g.ng[LV]);
+        conv_level<K, Q, S, true, Spec::kSkip>(a, g, slots, wts, np, LV, np * first, t0, nt);
+        conv_levels_fixed<K, Spec, LV + 1, LAST>(a, g, slots, wts, np, first + 4 * g.ns[LV] * g.ng[LV], t0, nt);
+    }
+}
+
+// Conv items of levels l_lo .. l_hi of a run-time geometry, on threads t0 .. t0+nt-1.
+template <int K>
+__device__ __forceinline__ void conv_levels_dyn(const PairArgs &a, const PairGeo &g, f2_t *slots, const f2_t *wts,
+                                                int np, int l_lo, int l_hi, int t0, int nt) {
+    int first = 0;  // conv items of the levels before l, per slot
+    for (int l = l_lo; l <= l_hi; ++l) {
+        const int base_l = np * first;
+        first += 4 * g.ns[l] * g.ng[l];
+        const int Ql = g.Q[l], Sl = g.S[l];
+        if (Ql == 4) {
+            if (Sl == 8) conv_level<K, 4, 8, false>(a, g, slots, wts, np, l, base_l, t0, nt);
+            else conv_level<K, 4, 4, false>(a, g, slots, wts, np, l, base_l, t0, nt);
+        } else {
+            if (Sl == 8) conv_level<K, 2, 8, false>(a, g, slots, wts, np, l, base_l, t0, nt);
+            else conv_level<K, 2, 4, false>(a, g, slots, wts, np, l, base_l, t0, nt);
+        }
     }
 }
 
@@ -436,7 +456,8 @@ __device__ __forceinline__ void pair_fwd_body(const PairArgs &a, const PairGeo &
     const int u1 = (int)((long long)(blockIdx.x + 1) * a.units / a.grid);
     T *raw = reinterpret_cast<T *>(base + lay.raw);
     const int raw_pair = a.raw_pair_bytes / (int)sizeof(T);
-    // thread 0: the bulk copies of unit u's planes
+    // thread 0: the bulk copies of unit u's planes (a warp-wide issue measured slower: the extra
+    // registers it costs outweigh the shorter issue)
     auto issue = [&](int u) {
         const int cu = u / a.ngroups, p0 = (u - cu * a.ngroups) * a.G, np = min(a.G, a.npairs - p0);
         const uint32_t pb = (uint32_t)(HW * sizeof(T));
@@ -454,6 +475,10 @@ __device__ __forceinline__ void pair_fwd_body(const PairArgs &a, const PairGeo &
     if (a.tma && tid == 0 && u0 < u1) issue(u0);
     int cur_c = -1;
     float bias = 0.f;
+    // L >= 3 on CTAs of 128 threads or more: the last warp builds levels >= 3 and runs their conv
+    // items while the other warps run the conv items of levels 1 and 2
+    const bool split = a.split != 0 && L >= 3 && nt >= 128;
+    const int nmain = split ? nt - 32 : nt;
 
     for (int u = u0; u < u1; ++u) {
         const int c = u / a.ngroups, grp = u - c * a.ngroups;
@@ -480,29 +505,37 @@ __device__ __forceinline__ void pair_fwd_body(const PairArgs &a, const PairGeo &
         else pass1<2, T, FIX>(a, g, slots, np, plane);
         __syncthreads();
         if (a.tma && tid == 0 && u + 1 < u1) issue(u + 1);  // the raw planes are free
-        // ---- deeper passes: levels 3 (and 4), then 5
+        // ---- conv items of every subband image of every level; levels 3 (and 4), then 5, are
+        // built first, on the last warp when the CTA splits, else by every thread
+        if (split) {
+            if (tid >= nmain) {
 #pragma unroll(FIX ? 2 : 1)
-        for (int l0 = 3; l0 <= L; l0 += 2) {
-            analysis_deep_pass(g, slots, np, l0, L);
-            __syncthreads();
-        }
-        // ---- conv items of every subband image of every level
-        if constexpr (FIX) {
-            conv_levels_fixed<K, Spec, 1>(a, g, slots, wts, np, 0);
-        } else {
-            int first = 0;  // conv items of the levels before l, per slot
-#pragma unroll(FIX ? kMaxLevels : 1)
-            for (int l = 1; l <= L; ++l) {
-                const int base_l = np * first;
-                first += 4 * g.ns[l] * g.ng[l];
-                const int Ql = g.Q[l], Sl = g.S[l];
-                if (Ql == 4) {
-                    if (Sl == 8) conv_level<K, 4, 8, FIX>(a, g, slots, wts, np, l, base_l);
-                    else conv_level<K, 4, 4, FIX>(a, g, slots, wts, np, l, base_l);
-                } else {
-                    if (Sl == 8) conv_level<K, 2, 8, FIX>(a, g, slots, wts, np, l, base_l);
-                    else conv_level<K, 2, 4, FIX>(a, g, slots, wts, np, l, base_l);
+                for (int l0 = 3; l0 <= L; l0 += 2) {
+                    analysis_deep_pass(g, slots, np, l0, L, nmain, 32);
+                    __syncwarp();
                 }
+                if constexpr (FIX) {
+                    conv_levels_fixed<K, Spec, 3>(a, g, slots, wts, np, 0, nmain, 32);
+                } else {
+                    conv_levels_dyn<K>(a, g, slots, wts, np, 3, L, nmain, 32);
+                }
+            } else {
+                if constexpr (FIX) {
+                    conv_levels_fixed<K, Spec, 1, (Spec::kL < 2 ? Spec::kL : 2)>(a, g, slots, wts, np, 0, 0, nmain);
+                } else {
+                    conv_levels_dyn<K>(a, g, slots, wts, np, 1, 2, 0, nmain);
+                }
+            }
+        } else {
+#pragma unroll(FIX ? 2 : 1)
+            for (int l0 = 3; l0 <= L; l0 += 2) {
+                analysis_deep_pass(g, slots, np, l0, L, 0, nt);
+                __syncthreads();
+            }
+            if constexpr (FIX) {
+                conv_levels_fixed<K, Spec, 1>(a, g, slots, wts, np, 0);
+            } else {
+                conv_levels_dyn<K>(a, g, slots, wts, np, 1, L, 0, nt);
             }
         }
         __syncthreads();
