@@ -109,14 +109,16 @@ __device__ __forceinline__ float analysis_from_global(const LayerArgs &a, const 
     return sum;
 }
 
-// Later passes: levels l (and l+1 when l+1 <= L) from the low band of level l-1 in shared memory.
+// Later passes: levels l (and l+1 when l+1 <= L) from the low band of level l-1 in shared memory,
+// on threads t0 .. t0+nt-1 (nt = 0: the whole CTA).
 template <int P>
 __device__ __forceinline__ void analysis_from_shared(const LayerArgs &a, const Geo &geo, float *slots, int G,
-                                                     const int *pyr_off, int l) {
+                                                     const int *pyr_off, int l, int t0 = 0, int nt = 0) {
     const bool two = (l + 1 <= geo.L);
     const FastDiv &dn = a.dv.a_n[l], &dw = a.dv.a_w[l];
     const int bw = (int)dw.d, n = (int)dn.d;
-    for (int it = threadIdx.x; it < G * n; it += blockDim.x) {
+    if (nt == 0) nt = blockDim.x;
+    for (int it = (int)threadIdx.x - t0; it < G * n; it += nt) {
         const int g = fdiv(dn, it), e = it - g * n;
         const int bi = fdiv(dw, e), bj = e - bi * bw;
         float *slot = slots + (size_t)g * geo.slot_floats;

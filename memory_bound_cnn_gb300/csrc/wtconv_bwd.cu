@@ -8,7 +8,9 @@
 // Every thread is pinned to one of these 1+4L correlations for the whole CTA and owns a fixed
 // share of its sliding-window items, so its k*k tap sums stay in registers (packed f32x2 pairs)
 // across all planes; they are reduced once, at the end, in a fixed order -- no atomics, so the
-// result is deterministic.  Each CTA writes one partial per (channel, subband, tap).
+// result is deterministic.  With L >= 3, when the items of levels >= 3 fit on one warp at the same
+// items per thread, that warp is the CTA's last: it builds levels >= 3 of both pyramids while the
+// other threads already correlate levels 0 .. 2.  Each CTA writes one partial per (channel, subband, tap).
 // wtconv_dw_finalize_kernel sums the partials of a channel in CTA order and unfolds the scales
 // by the chain rule through the folding W' = s w, b' = s_b b: dw = s dW', ds = sum_t w dW'
 // (+ b db' for the base path), db = s_b db'.
@@ -38,8 +40,8 @@ __global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_dw_kerne
     constexpr int kMaxImg = 1 + 2 * kMaxLevels;
     extern __shared__ __align__(16) float smem[];
     __shared__ Geo geo;
-    __shared__ int tstart[kMaxImg + 1];
-    __shared__ int per_thread;
+    __shared__ int tstart[kMaxImg + 1], tend[kMaxImg];
+    __shared__ int per_thread, per_thread_deep, split;
     const int c = blockIdx.x % a.C;
     const int nbi = blockIdx.x / a.C;
     const int G = a.G, nimg = 1 + 2 * a.L, nsig = 1 + 4 * a.L;
@@ -47,30 +49,46 @@ __global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_dw_kerne
 
     if (threadIdx.x == 0) {
         geo = a.geo;
-        // items per thread d: the smallest d for which every image's items fit on whole threads
-        int tot = 0;
-        for (int ci = 0; ci < nimg; ++ci) {
+        const int nt = blockDim.x;
+        auto items = [&](int ci) {
             const int l = ci == 0 ? 0 : (ci - 1) / 2 + 1;
-            tot += G * a.geo.rseg[l] * a.geo.cstr[l];
-        }
-        int d = (tot + (int)blockDim.x - 1) / (int)blockDim.x;
+            return G * a.geo.rseg[l] * a.geo.cstr[l];
+        };
+        int tot = 0;
+        for (int ci = 0; ci < nimg; ++ci) tot += items(ci);
+        // items per thread d: the smallest d for which every image's items fit on whole threads
+        int d = (tot + nt - 1) / nt;
         if (d < 1) d = 1;
         for (;; ++d) {
             int need = 0;
-            for (int ci = 0; ci < nimg; ++ci) {
-                const int l = ci == 0 ? 0 : (ci - 1) / 2 + 1;
-                need += (G * a.geo.rseg[l] * a.geo.cstr[l] + d - 1) / d;
-            }
-            if (need <= (int)blockDim.x) break;
+            for (int ci = 0; ci < nimg; ++ci) need += (items(ci) + d - 1) / d;
+            if (need <= nt) break;
         }
+        // the split layout at the same d: levels 0 .. 2 (images 0 .. 4) on threads [0, nt - 32),
+        // levels >= 3 on the last warp with the fewest items per thread dd that fit it (the warp
+        // builds those levels first, so fewer items keep it off the critical path)
+        const int cdeep = 5;
+        int lo = 0;
+        for (int ci = 0; ci < cdeep && ci < nimg; ++ci) lo += (items(ci) + d - 1) / d;
+        int dd = 1;
+        for (;; ++dd) {
+            int hi = 0;
+            for (int ci = cdeep; ci < nimg; ++ci) hi += (items(ci) + dd - 1) / dd;
+            if (hi <= 32 || dd >= d) break;
+        }
+        int hi = 0;
+        for (int ci = cdeep; ci < nimg; ++ci) hi += (items(ci) + dd - 1) / dd;
+        split = (a.L >= 3 && nt >= 128 && lo <= nt - 32 && hi <= 32) ? 1 : 0;
         int t0 = 0;
         for (int ci = 0; ci < nimg; ++ci) {
-            const int l = ci == 0 ? 0 : (ci - 1) / 2 + 1;
+            if (split && ci == cdeep) t0 = nt - 32;
             tstart[ci] = t0;
-            t0 += (G * a.geo.rseg[l] * a.geo.cstr[l] + d - 1) / d;
+            t0 += (items(ci) + (split && ci >= cdeep ? dd : d) - 1) / (split && ci >= cdeep ? dd : d);
+            tend[ci] = t0;
         }
         tstart[nimg] = t0;
         per_thread = d;
+        per_thread_deep = split ? dd : d;
     }
     {
         float4 *s4 = reinterpret_cast<float4 *>(slots);
@@ -82,13 +100,15 @@ __global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_dw_kerne
     // this thread's image and item range
     int my = -1, item_begin = 0, item_end = 0;
     for (int ci = 0; ci < nimg; ++ci)
-        if ((int)threadIdx.x >= tstart[ci] && (int)threadIdx.x < tstart[ci + 1]) my = ci;
+        if ((int)threadIdx.x >= tstart[ci] && (int)threadIdx.x < tend[ci]) my = ci;
+    const bool deep_warp = split && (int)threadIdx.x >= (int)blockDim.x - 32;
     const int lvl = my <= 0 ? 0 : (my - 1) / 2 + 1;
     const int pp = my <= 0 ? 0 : (my - 1) & 1;
     if (my >= 0) {
         const int items = G * geo.rseg[lvl] * geo.cstr[lvl];
-        item_begin = (threadIdx.x - tstart[my]) * per_thread;
-        item_end = min(items, item_begin + per_thread);
+        const int pt = my >= 5 ? per_thread_deep : per_thread;
+        item_begin = (threadIdx.x - tstart[my]) * pt;
+        item_end = min(items, item_begin + pt);
     }
     const int pitch = geo.pitch[lvl];
     const int y_off = lvl == 0 ? geo.off_x : geo.off_y[lvl] + pp * geo.pimg[lvl];
@@ -129,10 +149,20 @@ __global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_dw_kerne
             stage_planes<T>(dy, stg_dy, a.B, a.C, c, b0 + G, G, HW, a.dv.stage_chunks);
             cp_async_commit();
         }
-        for (int l = 3; l <= geo.L; l += 2) {
-            analysis_from_shared<P>(a, geo, slots, G, geo.off_y, l);
-            analysis_from_shared<P>(a, geo, slots, G, geo.off_g, l);
-            __syncthreads();
+        if (split) {
+            if (deep_warp) {
+                for (int l = 3; l <= geo.L; l += 2) {
+                    analysis_from_shared<P>(a, geo, slots, G, geo.off_y, l, blockDim.x - 32, 32);
+                    analysis_from_shared<P>(a, geo, slots, G, geo.off_g, l, blockDim.x - 32, 32);
+                    __syncwarp();
+                }
+            }
+        } else {
+            for (int l = 3; l <= geo.L; l += 2) {
+                analysis_from_shared<P>(a, geo, slots, G, geo.off_y, l);
+                analysis_from_shared<P>(a, geo, slots, G, geo.off_g, l);
+                __syncthreads();
+            }
         }
         if (!stg_x && grp + 1 < ngrp && ((HW * sizeof(T)) & 15) == 0 && (int)threadIdx.x < 2 * G) {
             const int bn = b0 + G + (threadIdx.x >> 1);
@@ -177,7 +207,7 @@ __global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_dw_kerne
                 ci = 1 + 2 * (l - 1) + (sb >> 1);
                 half = sb & 1;
             }
-            for (int th = tstart[ci]; th < tstart[ci + 1]; ++th) s += red[th * NR + half * KK + t];
+            for (int th = tstart[ci]; th < tend[ci]; ++th) s += red[th * NR + half * KK + t];
         } else if (sig == 0) {
             for (int th = 0; th < (int)blockDim.x; ++th) s += red[th * NR + 2 * KK];
         }
