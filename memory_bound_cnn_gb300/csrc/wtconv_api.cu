@@ -1047,6 +1047,24 @@ void add_phase(double &work, double &tim, long long n, double c, double eff, int
     tim += (double)((n + T - 1) / T) * T * c / eff;
 }
 
+// A group's planes as one tensor copy per activation: each H x W plane viewed as R rows of Wr
+// elements (Wr dividing H W, rows of a multiple of 16 bytes, Wr and R at most 256, the box limit).
+// WTCONV_PAIR_TMAP=0 keeps one bulk copy per plane.
+void pair_tma_map_geometry(PairArgs &a, int eb) {
+    a.tma_map = 0;
+    const char *kn = getenv("WTCONV_PAIR_TMAP");
+    if (!a.tma || (kn && kn[0] == '0') || 2 * a.G > 256) return;
+    const int HW = a.H * a.W;
+    for (int wr = std::min(256, HW); wr >= 1; --wr) {
+        if (HW % wr != 0 || ((size_t)wr * eb) % 16 != 0) continue;
+        if (HW / wr > 256) break;
+        a.tma_map = 1;
+        a.tma_rlen = wr;
+        a.tma_rows = HW / wr;
+        return;
+    }
+}
+
 // Forward / input gradient on batch pairs: every pair's pyramid and outputs in shared memory.
 PairPlan plan_pair_fwd_uncached(int B, int C, int H, int W, int L, int k, int dtype) {
     PairPlan best;
@@ -1124,6 +1142,7 @@ PairPlan plan_pair_fwd_uncached(int B, int C, int H, int W, int L, int k, int dt
     if (best.status == WTCONV_OK) {
         const char *ks = getenv("WTCONV_PAIR_SPLIT");  // tuning: 0 keeps every warp on every level
         best.a.split = (L >= 3 && best.a.nthreads >= 128 && !(ks && ks[0] == '0')) ? 1 : 0;
+        pair_tma_map_geometry(best.a, eb);
         pair_grid(best.a, sms, best.occ, 1);
     }
     return best;
@@ -1248,6 +1267,7 @@ PairPlan plan_pair_dw_uncached(int B, int C, int H, int W, int L, int k, int dty
         const char *kc = getenv("WTCONV_PAIR_CHUNK");  // tuning: groups per work unit
         if (kc && kc[0] && atoi(kc) > 0) cg = std::min(atoi(kc), a.ngroups);
         pair_grid(a, sms, best.occ, cg);
+        pair_tma_map_geometry(a, eb);
         best.workspace = ((size_t)a.nchunks * C * nsig * (KK + 1) * sizeof(float) + 255) / 256 * 256;
     }
     return best;
@@ -1265,7 +1285,7 @@ PairPlan cached_pair_plan(int kind, int B, int C, int H, int W, int L, int k, in
     // the tuning restrictions are part of the key: a restricted plan is a different plan
     std::string knobs;
     for (const char *kn : {"WTCONV_PAIR_THREADS", "WTCONV_PAIR_SHAPE", "WTCONV_PAIR_SLOTS", "WTCONV_PAIR_CHUNK",
-                           "WTCONV_PAIR_SPLIT"}) {
+                           "WTCONV_PAIR_SPLIT", "WTCONV_PAIR_TMAP"}) {
         const char *v = getenv(kn);
         knobs += v ? v : "";
         knobs += ';';
@@ -1950,6 +1970,9 @@ static int run_operator(int B, int C, int H, int W, int L, int k, int dtype, con
         a.with_bias = flip ? 0 : 1;
         a.timeout = timeout_flag();
         if (a.timeout == nullptr) return WTCONV_ERR_CUDA;
+        if (a.tma_map && !encode_map(&a.tmap_x, tma_dtype(dtype), elem_bytes(dtype), src, a.tma_rlen, a.tma_rows, C, B,
+                                     a.tma_rlen, a.tma_rows, 2 * a.G))
+            return WTCONV_ERR_CUDA;
         return cuda_status(launch_pair_fwd(a, dtype, fc.pr.smem, s));
     }
     if (fc.path == FWD_FUSED) {
@@ -2156,6 +2179,14 @@ static int run_dw_pair(const PairPlan &pp, int dtype, const void *x, const void 
     a.partials = partials;
     a.timeout = timeout_flag();
     if (a.timeout == nullptr) return WTCONV_ERR_CUDA;
+    if (a.tma_map) {
+        const int eb = elem_bytes(dtype);
+        if (!encode_map(&a.tmap_x, tma_dtype(dtype), eb, x, a.tma_rlen, a.tma_rows, a.C, a.B, a.tma_rlen, a.tma_rows,
+                        2 * a.G) ||
+            !encode_map(&a.tmap_dy, tma_dtype(dtype), eb, dy, a.tma_rlen, a.tma_rows, a.C, a.B, a.tma_rlen,
+                        a.tma_rows, 2 * a.G))
+            return WTCONV_ERR_CUDA;
+    }
     if (launch_pair_dw(a, dtype, pp.smem, s) != cudaSuccess) return WTCONV_ERR_CUDA;
     fin.B = a.B; fin.C = a.C; fin.H = a.H; fin.W = a.W; fin.L = a.L; fin.K = a.K;
     fin.nb = a.nb;

@@ -97,6 +97,11 @@ struct PairArgs {
     int spec;               // >= 0: the shape-specialised instantiation of this index runs (else -1)
     int split;              // forward, L >= 3, 128 threads or more: the last warp builds and convolves
                             // levels >= 3 while the others convolve levels 1 and 2
+    int tma_map;            // 1: a group's planes arrive as one tensor copy per activation (tmap_x,
+                            // tmap_dy: each plane viewed as tma_rows rows of tma_rlen elements, box
+                            // tma_rlen x tma_rows x 1 x 2G at (0, 0, channel, first batch entry));
+                            // 0: one bulk copy per plane
+    int tma_rlen, tma_rows;
     const void *x;          // forward: x; input gradient: dy; weight gradient: x
     const void *dy;         // weight gradient: dy
     void *out;              // y or dx
@@ -117,6 +122,7 @@ struct PairArgs {
     FastDiv dv_gw;          // level-2 positions per row
     FastDiv dv_xn, dv_xw;   // X build: two-pixel steps per plane, per row
     PairGeo geo;
+    CUtensorMap tmap_x, tmap_dy;
 };
 
 // Per activation type T (float, __nv_bfloat16, __half), defined in that type's translation unit.

@@ -24,6 +24,11 @@ struct PairDwLayout {
     size_t slots, raw, red, total;  // byte offsets from a 128-byte aligned base
 };
 
+// Bytes of one activation's raw planes of a group (2G planes, 128-byte rounded).
+__host__ __device__ inline size_t pair_dw_raw_half(const PairArgs &a) {
+    return ((size_t)a.G * a.raw_pair_bytes / 2 + 127) / 128 * 128;
+}
+
 // Slots, then the raw staging area (the next group's copies land there while the current group
 // is worked on), then the reduction buffer of the per-unit flush (one row of k*k+1 floats per
 // thread).
@@ -32,8 +37,9 @@ __host__ __device__ inline PairDwLayout pair_dw_layout(const PairArgs &a) {
     size_t o = 0;
     p.slots = o;
     o += (size_t)a.G * a.geo.slot * sizeof(f2_t);
-    p.raw = o;
-    if (a.tma) o += (size_t)a.G * a.raw_pair_bytes;
+    o = (o + 127) / 128 * 128;
+    p.raw = o;  // x planes of the group, then (128-byte aligned) its dy planes
+    if (a.tma) o += 2 * pair_dw_raw_half(a);
     p.red = o;
     o += (size_t)a.nthreads * (a.K * a.K + 1) * sizeof(float);
     p.total = o + 128;
@@ -242,11 +248,17 @@ __global__ void __launch_bounds__(NT, NT == 64 ? (K <= 5 ? 6 : 4) : NT == 128 ? 
     auto first_group = [&](int u) { return (u % a.nchunks) * a.chunk_groups; };
     auto end_group = [&](int u) { return min(a.ngroups, first_group(u) + a.chunk_groups); };
     auto raw_of = [&](int gs, int which) -> T * {  // which: 0 x, 1 dy; two planes each
-        return reinterpret_cast<T *>(base + lay.raw + (size_t)gs * a.raw_pair_bytes) + (size_t)which * 2 * HW;
+        return reinterpret_cast<T *>(base + lay.raw + (size_t)which * pair_dw_raw_half(a)) + (size_t)gs * 2 * HW;
     };
     auto issue = [&](int cu, int grp) {  // thread 0: the copies of group grp of channel cu
         const int p0 = grp * a.G, np = min(a.G, a.npairs - p0);
         const uint32_t pb = (uint32_t)(HW * sizeof(T));
+        if (a.tma_map) {  // one copy per activation of the 2G planes (zero past B; whole boxes)
+            mbar_arrive_expect_tx(&bar, (uint32_t)(4 * a.G) * pb);
+            tma_load_4d(raw_of(0, 0), &a.tmap_x, 0, 0, cu, 2 * p0, &bar);
+            tma_load_4d(raw_of(0, 1), &a.tmap_dy, 0, 0, cu, 2 * p0, &bar);
+            return;
+        }
         uint32_t bytes = 0;
         for (int gs = 0; gs < np; ++gs)
             for (int q = 0; q < 2; ++q)

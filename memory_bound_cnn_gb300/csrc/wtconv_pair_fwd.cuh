@@ -33,6 +33,7 @@ __host__ __device__ inline PairFwdLayout pair_fwd_layout(const PairArgs &a) {
     size_t o = 0;
     p.slots = o;
     o += (size_t)a.G * a.geo.slot * sizeof(f2_t);
+    o = (o + 127) / 128 * 128;
     p.raw = o;  // raw planes of the group (the next group's copies land here once pass 1 is done)
     if (a.tma) o += (size_t)a.G * a.raw_pair_bytes;
     o = (o + 15) / 16 * 16;
@@ -461,6 +462,11 @@ __device__ __forceinline__ void pair_fwd_body(const PairArgs &a, const PairGeo &
     auto issue = [&](int u) {
         const int cu = u / a.ngroups, p0 = (u - cu * a.ngroups) * a.G, np = min(a.G, a.npairs - p0);
         const uint32_t pb = (uint32_t)(HW * sizeof(T));
+        if (a.tma_map) {  // one copy of the 2G planes (zero past B; the byte count is the whole box)
+            mbar_arrive_expect_tx(&bar, (uint32_t)(2 * a.G) * pb);
+            tma_load_4d(raw, &a.tmap_x, 0, 0, cu, 2 * p0, &bar);
+            return;
+        }
         uint32_t bytes = 0;
         for (int gs = 0; gs < np; ++gs)
             for (int q = 0; q < 2; ++q)
@@ -616,8 +622,16 @@ struct PairShapeSpec {
     }
 };
 
+// Resident CTAs the register budget is cut for: a shape-specialised instantiation of 128 threads
+// at k = 5 fits four CTAs' shared memory (16 x 16 planes, four pairs), so it is held to 128
+// registers (it needs about 122) rather than losing the fourth CTA to a few extra registers.
+template <int K, int NT, class Spec>
+constexpr int pair_fwd_min_blocks() {
+    return NT == 64 ? (K <= 5 ? 6 : 4) : NT == 128 ? (K <= 3 ? 4 : (K == 5 ? (Spec::fixed ? 4 : 3) : 2)) : 1;
+}
+
 template <int K, typename T, int NT, class Spec>
-__global__ void __launch_bounds__(NT, NT == 64 ? (K <= 5 ? 6 : 4) : NT == 128 ? (K <= 3 ? 4 : (K == 5 ? 3 : 2)) : 1)
+__global__ void __launch_bounds__(NT, (pair_fwd_min_blocks<K, NT, Spec>()))
     wtconv_pair_fwd_kernel(const __grid_constant__ PairArgs a) {
     if constexpr (Spec::fixed) {
         pair_fwd_body<K, T, Spec>(a, Spec::template geo<K, 0>());
