@@ -585,7 +585,7 @@ bool ps_make(PsArgs &a, int B, int C, int H, int W, int K, int eb, bool deep, in
     a.vec_st = 1;  // W even, items 2 columns wide at even columns
     const int xbw = (TW + 2 * a.HX) / 2, xbh = (TH + 2 * a.HX) / 2;
     a.dv_work_c = make_fastdiv(a.tiles * a.ngroups);
-    a.dv_ngroups = make_fastdiv(a.ngroups);
+    a.dv_tiles = make_fastdiv(a.tiles);
     a.dv_tiles_c = make_fastdiv(a.tiles_c);
     a.dv_xb = make_fastdiv(xbw * xbh);
     a.dv_xbw = make_fastdiv(xbw);
@@ -1420,7 +1420,7 @@ bool pt_make(PtileArgs &a, int B, int C, int H, int W, int in_pitch, int eb, int
     a.dv_n1 = make_fastdiv(std::max(1, a.n1));
     a.dv_n2 = make_fastdiv(std::max(1, a.n2));
     for (int l = 0; l <= kPtMaxLevels; ++l) a.dv_ns[l] = make_fastdiv(l <= LT ? a.lv[l].ns : 1);
-    a.dv_ngroups = make_fastdiv(a.ngroups);
+    a.dv_tiles = make_fastdiv(a.tiles);
     a.dv_tiles_c = make_fastdiv(a.tiles_c);
     const int xbw = (TW + 2 * a.HX) / BS, xbh = (TH + 2 * a.HX) / BS;
     a.dv_xbw = make_fastdiv(xbw);

@@ -100,14 +100,14 @@ __global__ void __launch_bounds__(NT, (K <= 5 ? 512 : 384) / NT) wtconv_pshallow
 
     const int w0 = (int)((long long)blockIdx.x * a.work / a.grid);
     const int w1 = (int)((long long)(blockIdx.x + 1) * a.work / a.grid);
-    const int per_c = (int)a.dv_work_c.d;  // work items per channel: tiles * ngroups
+    const int per_c = (int)a.dv_work_c.d;  // work items per channel: ngroups * tiles
     const uint32_t box_x = (uint32_t)(2 * G * RXR * RXW * (int)sizeof(T));
     const uint32_t box_d = a.has_deep ? (uint32_t)(2 * G * TH1 * TW1 * (int)sizeof(float)) : 0u;
     // work item w -> channel, tile row / column, first pair
     auto decode = [&](int w, int &c, int &tr, int &tc, int &p0) {
         c = (int)fdiv(a.dv_work_c, (uint32_t)w);
         const int rem = w - c * per_c;
-        const int t = (int)fdiv(a.dv_ngroups, (uint32_t)rem), grp = rem - t * a.ngroups;
+        const int grp = (int)fdiv(a.dv_tiles, (uint32_t)rem), t = rem - grp * a.tiles;
         tr = (int)fdiv(a.dv_tiles_c, (uint32_t)t);
         tc = t - tr * a.tiles_c;
         p0 = grp * G;

@@ -20,7 +20,9 @@ struct PsArgs {
     int RXR, RXW;                  // raw x tile rows / row length (elements)
     int tiles_r, tiles_c, tiles;
     int G, npairs, ngroups;        // pair slots per group; ceil(B / 2); groups per tile
-    int work;                      // work items (channel, tile, group), channel-major
+    int work;                      // work items (channel, group, tile): channel-major, tiles innermost, so
+                                   // that a CTA walks neighbouring tiles of one pair of planes (their
+                                   // halos are still in L2)
     int grid, nthreads;            // persistent grid: CTA i takes work [i*work/grid, (i+1)*work/grid)
     // slot geometry (pairs): X padded (interior at (P, P)), level 1 padded (4 images), level-1 conv
     // outputs Z1 (4 compact images) followed by D (one more image of the same shape)
@@ -31,7 +33,7 @@ struct PsArgs {
     int raw_x_bytes, raw_d_bytes;  // one group's raw tiles (128-byte rounded)
     int has_deep;                  // L >= 2: D tiles arrive with the x tiles
     int vec_st;                    // rows allow vector stores
-    FastDiv dv_work_c, dv_ngroups, dv_tiles_c, dv_xb, dv_xbw, dv_conv, dv_ns1, dv_out, dv_ns0, dv_db, dv_dbw;
+    FastDiv dv_work_c, dv_tiles, dv_tiles_c, dv_xb, dv_xbw, dv_conv, dv_ns1, dv_out, dv_ns0, dv_db, dv_dbw;
     const void *x;                 // forward: x; input gradient: dy
     const float *deep;             // D [B][C][H/2][W/2] fp32, or null
     void *out;

@@ -39,7 +39,8 @@ struct PtileArgs {
     int RXR, RXW;                  // raw x tile rows / row length (elements)
     int tiles_r, tiles_c, tiles;
     int G, npairs, ngroups;        // pair slots per group; ceil(B / 2); groups per tile
-    int work;                      // work items per channel: tiles * ngroups (tile-major)
+    int work;                      // work items per channel: ngroups * tiles (tiles innermost: neighbouring
+                                   // tiles of one pair group follow each other, so their halos hit L2)
     int nchunks;                   // partial rows per channel; chunk n covers work [n*work/nchunks, (n+1)*work/nchunks)
     int units, grid, nthreads;     // units = C * nchunks (channel-major); persistent grid
     int per_pair;                  // correlation items per pair
@@ -50,7 +51,7 @@ struct PtileArgs {
     int ll_out;                    // 1: write the level-2 LL bands of x and dy to ll_x / ll_dy
     int ll_h, ll_w, ll_pitch;      // LL planes: ll_h x ll_w positions, row pitch ll_pitch (floats)
     PtLevel lv[kPtMaxLevels + 1];
-    FastDiv dv_pp, dv_n1, dv_n2, dv_ns[kPtMaxLevels + 1], dv_ngroups, dv_tiles_c;
+    FastDiv dv_pp, dv_n1, dv_n2, dv_ns[kPtMaxLevels + 1], dv_tiles, dv_tiles_c;
     FastDiv dv_xb, dv_xbw, dv_db, dv_dbw;  // pass 1: x blocks per pair / per row, dy blocks per pair / per row
     const void *x, *dy;
     float *ll_x, *ll_dy;

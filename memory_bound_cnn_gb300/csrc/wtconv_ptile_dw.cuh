@@ -5,7 +5,7 @@
 // plane (paper, Principais Contribuicoes: all parameter gradients from the same on-chip pyramids;
 // Metodologia: the butterflies are recomputed on chip, no intermediate tensor in HBM).
 //
-// A CTA walks through work units (channel, run of tiles x pair groups).  Per work item one thread
+// A CTA walks through work units (channel, run of pair groups x tiles).  Per work item one thread
 // issues two bulk tensor copies: the x tile of G batch pairs with a halo of 2^LT * P positions
 // (zero outside the plane), and the dy tile.  One pass over 2^LT x 2^LT blocks builds, as
 // batch-pair images, the padded x copy and its level 1 (and 2) subbands where the correlations
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(NT, pt_min_blocks<K, IQ, NT>()) wtconv_ptile_d
     const uint32_t box_dy = (uint32_t)(2 * G * TH * TW * (int)sizeof(T));
     auto issue = [&](int u, int w) {  // thread 0: the two tiles of work item w of unit u
         const int c = u / a.nchunks;
-        const int t = (int)fdiv(a.dv_ngroups, (uint32_t)w), grp = w - t * a.ngroups;
+        const int grp = (int)fdiv(a.dv_tiles, (uint32_t)w), t = w - grp * a.tiles;
         const int tr = (int)fdiv(a.dv_tiles_c, (uint32_t)t), tc = t - tr * a.tiles_c;
         const int r0 = tr * TH, c0 = tc * TW, b0 = 2 * grp * G;
         mbar_arrive_expect_tx(&bar, box_x + box_dy);
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(NT, pt_min_blocks<K, IQ, NT>()) wtconv_ptile_d
         f2_t dysum = 0ull;
         const int w1 = we(u);
         for (int w = wb(u); w < w1; ++w, ++step) {
-            const int t = (int)fdiv(a.dv_ngroups, (uint32_t)w), grp = w - t * a.ngroups;
+            const int grp = (int)fdiv(a.dv_tiles, (uint32_t)w), t = w - grp * a.tiles;
             const int tr = (int)fdiv(a.dv_tiles_c, (uint32_t)t), tc = t - tr * a.tiles_c;
             const int p0 = grp * G, np = min(G, a.npairs - p0);
             if (tid == 0) copy_ok = mbar_wait(&bar, step & 1, a.timeout) ? 1 : 0;
