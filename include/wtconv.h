@@ -68,7 +68,10 @@
  *   - Tuning restrictions for measurement runs (the plans they give are valid, only slower or
  *     faster): WTCONV_PAIR_THREADS, WTCONV_PAIR_SHAPE and WTCONV_PAIR_SLOTS fix the batch-pair
  *     kernels' CTA size, item shapes and pair slots per group; WTCONV_PAIR_CHUNK fixes the
- *     batch-pair weight gradient's slot groups per work unit; WTCONV_PTILE=TH,TW,G,threads[,narrow]
+ *     batch-pair weight gradient's slot groups per work unit; WTCONV_PAIR_SPLIT=0 keeps every
+ *     warp of the batch-pair forward on every level (by default, with L >= 3, the last warp builds
+ *     and convolves levels >= 3 while the others convolve levels 1 and 2); WTCONV_PAIR_TMAP=0
+ *     brings a group's planes by one bulk copy per plane instead of one tensor copy per input; WTCONV_PTILE=TH,TW,G,threads[,narrow]
  *     fixes the first tiled batch-pair weight-gradient launch's tile, pair slots, CTA size and
  *     item width; WTCONV_PSHALLOW=TH,TW,G,threads[,rows] fixes the tiled batch-pair shallow
  *     kernel's tile, pair slots, CTA size and item rows;
