@@ -21,14 +21,15 @@
 //   60.1 vs 74.4 us (76.4 with 8-row items); weight gradient 76 us with 7-row items on
 //   128 threads, against 82.5 on 64 threads, 80 with 8-row items on 128 threads and 94 on the
 //   whole-plane kernel
-//   56x56 L3 fp32: forward 131 with 7-row items at levels >= 1 (154 with 8-row) vs 119 us on the
-//   fused whole-plane kernel; weight gradient 169 vs 156 us
+//   56x56 L3 fp32: forward 113 us with 7-row items at levels >= 1 on 256 threads (136 with
+//   8-row items) vs 118 on the fused whole-plane kernel, since the last warp builds and
+//   convolves level 3 beside levels 1-2 (131 before); weight gradient 167 vs 159 us
 #define WTCONV_SPEC_b64l4 b64l4, 64, 64, 4, 5, __nv_bfloat16, 1, 2, 8, 4, 8, 2, 8, 256, 1, 1, 0, 0, -1
 #define WTCONV_SPEC_b32l3 b32l3, 32, 32, 3, 5, __nv_bfloat16, 1, 2, 8, 4, 8, 2, 8, 256, 4, 1, 0, 0, -1
 #define WTCONV_SPEC_b16l2 b16l2, 16, 16, 2, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 128, 4, 1, 1, 0, -1
 #define WTCONV_SPEC_b8l1 b8l1, 8, 8, 1, 5, __nv_bfloat16, 1, 2, 8, 2, 8, 2, 8, 64, 8, 1, 1, 0, -1
 #define WTCONV_SPEC_b28l2 b28l2, 28, 28, 2, 5, __nv_bfloat16, 1, 2, 14, 2, 7, 2, 7, 0, 0, 1, 1, 128, 6
-#define WTCONV_SPEC_f56l3 f56l3, 56, 56, 3, 5, float, 0, 2, 8, 2, 7, 2, 7, 0, 0, 0, 0, 0, -1
+#define WTCONV_SPEC_f56l3 f56l3, 56, 56, 3, 5, float, 0, 2, 8, 2, 7, 2, 7, 256, 1, 1, 0, 0, -1
 
 #define WTCONV_PAIR_SPEC_LIST(X)                                                                    \
     X(WTCONV_SPEC_b64l4) X(WTCONV_SPEC_b32l3) X(WTCONV_SPEC_b16l2) X(WTCONV_SPEC_b8l1)             \
