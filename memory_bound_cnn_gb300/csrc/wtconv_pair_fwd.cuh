@@ -97,10 +97,13 @@ __device__ __forceinline__ void store_row(const f2_t (&acc)[Q], T *d0, T *d1, in
 // SKIP: as in pair_conv_strip, the first zt and last zb window rows are zero padding.  DEEP: a
 // fifth image after the four subband images of z1 (at z1 + 4 zimg) holds the contribution of the
 // deeper levels at level-1 resolution, which enters with the low band (all four pixels).
-template <int K, int Q, int S, typename T, bool SKIP = false, bool DEEP = false>
+// DREG (Q = 2 only): dreg[m] holds the deeper levels' contribution for the item's level-1 row m,
+// added with the low band in place of a deep image.
+template <int K, int Q, int S, typename T, bool SKIP = false, bool DEEP = false, bool DREG = false>
 __device__ __forceinline__ void pair_out_item(const f2_t *__restrict__ in, int pitch, const f2_t (&w)[K * K],
                                               f2_t bias2, const f2_t *__restrict__ z1, int zpitch, int zimg, T *d0,
-                                              T *d1, int W, int nrows, int ncols, bool vec, int zt = 0, int zb = 0) {
+                                              T *d1, int W, int nrows, int ncols, bool vec, int zt = 0, int zb = 0,
+                                              const f2_t *dreg = nullptr) {
     constexpr int NW = Q + K - 1, NL = (NW + 1) / 2, QL = Q / 2;
     f2_t acc[S][Q];
     f2_t pend[Q];  // the odd row's synthesis terms
@@ -155,6 +158,7 @@ __device__ __forceinline__ void pair_out_item(const f2_t *__restrict__ in, int p
             } else {
                 ll[0] = zr[0]; lh[0] = zr[zimg]; hl[0] = zr[2 * zimg]; hh[0] = zr[3 * zimg];
                 if constexpr (DEEP) ll[0] = fadd2(ll[0], zr[4 * zimg]);
+                if constexpr (DREG) ll[0] = fadd2(ll[0], dreg[jd >> 1]);
             }
 #pragma unroll
             for (int m = 0; m < QL; ++m) {
@@ -265,8 +269,41 @@ __device__ __forceinline__ void analysis_deep_pass(const PairGeo &g, f2_t *slots
     }
 }
 
+// The contribution of levels >= 2 to level-1 positions (i1 + m, j1), m < 4 (i1 a multiple of 4):
+// per level-2 position (i2, j2) the closed form adds, at level-1 position (2 i2 + a, 2 j2 + b),
+// LL + (-1)^b LH + (-1)^a (HL + (-1)^b HH) of level 2 plus the levels >= 3 term v(i2, j2), whose
+// signs come from the bits of (i2, j2) as in the gather phase.
+__device__ __forceinline__ void deep_col4(const PairGeo &g, const f2_t *slot, int i1, int j1, f2_t (&d)[4]) {
+    const int j2 = j1 >> 1;
+    const bool b = j1 & 1;
+    const int zi2 = g.zimg[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i2 = (i1 >> 1) + h;
+        f2_t v = pk2(0.f, 0.f);
+#pragma unroll
+        for (int l = 3; l <= kMaxLevels; ++l) {
+            if (l > g.L) break;
+            const int sh = l - 2;
+            const f2_t *zl = slot + g.off_z[l] + (i2 >> sh) * g.zpitch[l] + (j2 >> sh);
+            const int zi = g.zimg[l];
+            const bool ra = (i2 >> (sh - 1)) & 1, cb = (j2 >> (sh - 1)) & 1;
+            const f2_t pp = ra ? fsub2(zl[0], zl[2 * zi]) : fadd2(zl[0], zl[2 * zi]);
+            const f2_t rr = ra ? fsub2(zl[zi], zl[3 * zi]) : fadd2(zl[zi], zl[3 * zi]);
+            v = fadd2(v, cb ? fsub2(pp, rr) : fadd2(pp, rr));
+        }
+        const f2_t *z2 = slot + g.off_z[2] + i2 * g.zpitch[2] + j2;
+        const f2_t t0 = fadd2(fadd2(z2[0], z2[2 * zi2]), v), t1 = fadd2(fsub2(z2[0], z2[2 * zi2]), v);
+        const f2_t u0 = fadd2(z2[zi2], z2[3 * zi2]), u1 = fsub2(z2[zi2], z2[3 * zi2]);
+        d[2 * h] = b ? fsub2(t0, u0) : fadd2(t0, u0);
+        d[2 * h + 1] = b ? fsub2(t1, u1) : fadd2(t1, u1);
+    }
+}
+
 // Output items of every slot with item shape Q x S (the base kernel in registers for the loop).
-template <int K, int Q, int S, typename T, bool FIX, bool SKIP = false>
+// FOLD (Q = 2, S a multiple of 8, L >= 2): the items add the levels >= 2 themselves (deep_col4)
+// instead of reading them from a gather phase.
+template <int K, int Q, int S, typename T, bool FIX, bool SKIP = false, bool FOLD = false>
 __device__ __forceinline__ void out_phase(const PairArgs &a, const PairGeo &g, const f2_t *slots, const f2_t *wts,
                                           int np, int p0, int c, f2_t bias2, T *out) {
     constexpr int KK = K * K;
@@ -286,8 +323,23 @@ __device__ __forceinline__ void out_phase(const PairArgs &a, const PairGeo &g, c
         T *d0 = out + ((size_t)b0 * C + c) * HW + (size_t)r0 * W + c0;
         T *d1 = b0 + 1 < B ? d0 + (size_t)C * HW : nullptr;
         const int zt = max(0, K / 2 - r0), zb = max(0, r0 + S + K / 2 - H);
-        pair_out_item<K, Q, S, T, SKIP>(sl + ox + r0 * ip0 + c0, ip0, w, bias2, sl + oz1 + (r0 >> 1) * zp1 + (c0 >> 1),
-                                        zp1, zi1, d0, d1, W, min(S, H - r0), min(Q, W - c0), vec, zt, zb);
+        if constexpr (FOLD) {
+            static_assert(Q == 2 && S % 8 == 0, "FOLD: items of 2 columns and a multiple of 8 rows");
+            f2_t dr[S / 2];
+#pragma unroll
+            for (int m = 0; m < S / 2; m += 4) {
+                f2_t d4[4];
+                deep_col4(g, sl, (r0 >> 1) + m, c0 >> 1, d4);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) dr[m + q] = d4[q];
+            }
+            pair_out_item<K, Q, S, T, SKIP, false, true>(sl + ox + r0 * ip0 + c0, ip0, w, bias2,
+                                                         sl + oz1 + (r0 >> 1) * zp1 + (c0 >> 1), zp1, zi1, d0, d1, W,
+                                                         min(S, H - r0), min(Q, W - c0), vec, zt, zb, dr);
+        } else {
+            pair_out_item<K, Q, S, T, SKIP>(sl + ox + r0 * ip0 + c0, ip0, w, bias2, sl + oz1 + (r0 >> 1) * zp1 + (c0 >> 1),
+                                            zp1, zi1, d0, d1, W, min(S, H - r0), min(Q, W - c0), vec, zt, zb);
+        }
     }
 }
 
@@ -424,6 +476,16 @@ __device__ __forceinline__ void conv_levels_dyn(const PairArgs &a, const PairGeo
     }
 }
 
+// Whether an instantiation's output items add the levels >= 2 themselves (no gather phase): the
+// shape-specialised ones with L >= 3 and 2 x 8k output items.  Measured on GB300: 64 x 64 L4 bf16
+// 234 -> 230 us (the phase and its barrier cost more than the items' extra loads); 32 x 32 L3
+// bf16 and 56 x 56 L3 fp32 unchanged.
+template <class Spec>
+__host__ __device__ constexpr bool fold_deep() {
+    if constexpr (Spec::fixed) return Spec::kL >= 3 && Spec::kQ0 == 2 && Spec::kH > 4 && Spec::kS0 % 8 == 0;
+    else return false;
+}
+
 template <int K, typename T, class Spec>
 __device__ __forceinline__ void pair_fwd_body(const PairArgs &a, const PairGeo &g) {
     constexpr bool FIX = Spec::fixed;
@@ -545,8 +607,10 @@ __device__ __forceinline__ void pair_fwd_body(const PairArgs &a, const PairGeo &
             }
         }
         __syncthreads();
-        // ---- levels >= 2 synthesised into the level-1 LL outputs
-        if (L >= 2) {
+        // ---- levels >= 2 synthesised into the level-1 LL outputs (unless the output items add
+        // them themselves: the shape-specialised instantiations with L >= 3 and 2-column items)
+        constexpr bool kFold = fold_deep<Spec>();
+        if (L >= 2 && !kFold) {
             const int w2 = g.w[2];
             const int zp1 = g.zpitch[1];
             const int n_gather = g.h[2] * w2;
@@ -587,7 +651,7 @@ __device__ __forceinline__ void pair_fwd_body(const PairArgs &a, const PairGeo &
         const int Q0 = g.Q[0], S0 = g.S[0];
         if constexpr (FIX) {
             constexpr int kS0 = Spec::kH <= 4 ? 4 : Spec::kS0;
-            out_phase<K, Spec::kQ0, kS0, T, true, Spec::kSkip>(a, g, slots, wts, np, p0, c, bias2, out);
+            out_phase<K, Spec::kQ0, kS0, T, true, Spec::kSkip, kFold>(a, g, slots, wts, np, p0, c, bias2, out);
         } else if (Q0 == 4) {
             if (S0 == 8) out_phase<K, 4, 8, T, FIX>(a, g, slots, wts, np, p0, c, bias2, out);
             else out_phase<K, 4, 4, T, FIX>(a, g, slots, wts, np, p0, c, bias2, out);

@@ -203,6 +203,35 @@ def test_tiled_pair_forward(case):
     assert_close("dx [ptile]", np64(dx), g_ref["dx"], tol)
 
 
+@pytest.mark.parametrize("knobs", [{"WTCONV_PAIR_SPLIT": "0"}, {"WTCONV_PAIR_TMAP": "0"},
+                                   {"WTCONV_PAIR_SPLIT": "0", "WTCONV_PAIR_TMAP": "0"}],
+                         ids=lambda k: "+".join(f"{a}={b}" for a, b in k.items()))
+@pytest.mark.parametrize("case", [(6, 8, 64, 64, 4, 5, "bf16"), (5, 6, 32, 32, 3, 3, "f16"), (3, 4, 56, 56, 3, 5, "f32"),
+                                  (9, 8, 8, 8, 1, 7, "bf16"), (4, 6, 28, 28, 2, 5, "bf16")],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_pair_kernels_without_level_split_or_tensor_copies(case, knobs):
+    """The batch-pair kernels' other schedules against the oracle: every warp on every level
+    (no last-warp split for levels >= 3) and one bulk copy per plane (no group tensor copy)."""
+    shape = LayerShape(*case)
+    inputs = make_inputs(shape, seed=21)
+    d = to_device(inputs)
+    tol = TOL[shape.dtype]
+    with contextlib.ExitStack() as stack:
+        for var, val in knobs.items():
+            stack.enter_context(env_path(var, val))
+        stack.enter_context(fwd_path("pair"))
+        stack.enter_context(env_path("WTCONV_DW_PATH", "pair"))
+        y = gpu_forward(d)
+        dx, g = gpu_backward(d)
+        torch.cuda.synchronize()
+    y_ref = oracle.forward(inputs["x"], inputs)
+    g_ref = oracle.backward(inputs["x"], inputs["dy"], inputs)
+    assert_close("y", np64(y), y_ref, tol)
+    assert_close("dx", np64(dx), g_ref["dx"], tol)
+    for n in GRADS:
+        assert_close(n, np64(g[n]), g_ref[n], tol)
+
+
 def test_input_gradient_is_forward_with_rotated_kernels():
     """dx = forward(dy) with every kernel rotated 180 degrees and no bias (transpose identity)."""
     shape = LayerShape(2, 4, 32, 32, 3, 5, "f32")
