@@ -482,7 +482,8 @@ __device__ __forceinline__ void conv_levels_dyn(const PairArgs &a, const PairGeo
 // bf16 and 56 x 56 L3 fp32 unchanged.
 template <class Spec>
 __host__ __device__ constexpr bool fold_deep() {
-    if constexpr (Spec::fixed) return Spec::kL >= 3 && Spec::kQ0 == 2 && Spec::kH > 4 && Spec::kS0 % 8 == 0;
+    if constexpr (Spec::fixed)
+        return Spec::kL >= 3 && Spec::kQ0 == 2 && Spec::kH > 4 && Spec::kS0 % 8 == 0 && Spec::kH % Spec::kS0 == 0;
     else return false;
 }
 
