@@ -92,6 +92,14 @@ __global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_deep_ker
         }
         cstart[ci1] = tot;
     }
+    const T *x = static_cast<const T *>(a.x);
+    const size_t HW = (size_t)a.H * a.W;
+    // the first group's planes start towards L2 now, while the slots are cleared and the kernels
+    // staged (the later groups' planes are prefetched one group ahead in the loop below)
+    if (!a.stage && ((HW * sizeof(T)) & 15) == 0 && (int)threadIdx.x < G) {
+        const int b = nbi * a.groups_per_cta * G + (int)threadIdx.x;
+        if (b < a.B) prefetch_l2(x + ((size_t)b * a.C + c) * HW, (uint32_t)(HW * sizeof(T)));
+    }
     {
         float4 *s4 = reinterpret_cast<float4 *>(slots);
         const int n4 = G * a.geo.slot_floats / 4;
@@ -100,8 +108,6 @@ __global__ void __launch_bounds__(kMaxThreads, (K <= 5 ? 2 : 1)) wtconv_deep_ker
     stage_weights<K>(a, c, wts);
     __syncthreads();
 
-    const T *x = static_cast<const T *>(a.x);
-    const size_t HW = (size_t)a.H * a.W;
     const int H1 = a.H >> 1, W1 = a.W >> 1;
     T *stg = a.stage ? reinterpret_cast<T *>(reinterpret_cast<char *>(smem) + a.stage_off) : nullptr;
     const int nitems = cstart[ci1];
